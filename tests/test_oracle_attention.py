@@ -1,0 +1,184 @@
+"""Pins of the oracle's attention arithmetic against things other than itself:
+brute force in plain Python loops, closed forms, and the merge identity.
+
+The definitions being pinned: decode attention out = sum_t softmax_t(scale q.k_t)
+v_t; the partial triple (o unnormalised, m = max, s = sum exp) of each phase
+and their rescaled-sum merge [ChunkAttention explainer blog, "Two-Phase
+Partition": phase equations, output combination and the two-phase function].
+"""
+import math
+import random
+
+import numpy as np
+import pytest
+
+from oracle import attention as A
+from oracle.pakv import OracleError, OracleTrie
+
+
+def brute_force(q, k, v, scale):
+    """Plain-Python triple loop: for each head, scores, exponentials, weighted
+    sum.  No numpy, no max shift (inputs are kept small enough not to
+    overflow)."""
+    n, H, D = len(k), len(q), len(q[0])
+    out = []
+    for h in range(H):
+        e = []
+        for t in range(n):
+            dot = 0.0
+            for d in range(D):
+                dot += q[h][d] * k[t][h][d]
+            e.append(math.exp(scale * dot))
+        z = sum(e)
+        out.append([sum(e[t] * v[t][h][d] for t in range(n)) / z for d in range(D)])
+    return out
+
+
+def rand(shape, rng, lo=-1.0, hi=1.0):
+    return rng.uniform(lo, hi, size=shape)
+
+
+def test_hand_computed_two_token_example():
+    # q = (1, 0), keys (1, 0) and (0, 0), values (1, 2) and (3, 4), scale 1:
+    # scores 1 and 0, weights e/(1+e) and 1/(1+e).
+    q = np.array([[1.0, 0.0]])
+    k = np.array([[[1.0, 0.0]], [[0.0, 0.0]]])
+    v = np.array([[[1.0, 2.0]], [[3.0, 4.0]]])
+    e = math.e
+    want = np.array([[(e + 3) / (1 + e), (2 * e + 4) / (1 + e)]])
+    np.testing.assert_allclose(A.softmax_attention(q, k, v, 1.0), want, rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("n,H,D", [(1, 1, 1), (3, 2, 4), (17, 3, 5), (40, 2, 8)])
+def test_softmax_attention_matches_brute_force(n, H, D):
+    rng = np.random.default_rng(n * 100 + H * 10 + D)
+    q, k, v = rand((H, D), rng), rand((n, H, D), rng), rand((n, H, D), rng)
+    scale = 1 / math.sqrt(D)
+    got = A.softmax_attention(q, k, v, scale)
+    want = brute_force(q.tolist(), k.tolist(), v.tolist(), scale)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-13)
+
+
+def test_constant_v_returns_v():
+    rng = np.random.default_rng(1)
+    H, D, n = 3, 16, 50
+    q, k = rand((H, D), rng, -4, 4), rand((n, H, D), rng, -4, 4)
+    row = rand((H, D), rng)
+    v = np.broadcast_to(row, (n, H, D))
+    np.testing.assert_allclose(A.softmax_attention(q, k, v, 0.7), row, rtol=0, atol=1e-14)
+
+
+def test_zero_query_gives_mean_of_v():
+    rng = np.random.default_rng(2)
+    H, D, n = 2, 8, 33
+    k, v = rand((n, H, D), rng), rand((n, H, D), rng)
+    got = A.softmax_attention(np.zeros((H, D)), k, v, 0.3)
+    np.testing.assert_allclose(got, v.mean(axis=0), rtol=0, atol=1e-14)
+
+
+def test_single_token_context_returns_its_value():
+    rng = np.random.default_rng(3)
+    q, k, v = rand((4, 8), rng), rand((1, 4, 8), rng), rand((1, 4, 8), rng)
+    np.testing.assert_allclose(A.softmax_attention(q, k, v, 2.0), v[0], rtol=0, atol=1e-15)
+
+
+def test_dominant_key_returns_its_value():
+    rng = np.random.default_rng(4)
+    H, D, n = 2, 8, 20
+    q = np.ones((H, D))
+    k, v = rand((n, H, D), rng, -0.1, 0.1), rand((n, H, D), rng)
+    k[7] = 10.0                                     # score 80 * scale above the rest
+    np.testing.assert_allclose(A.softmax_attention(q, k, v, 1.0), v[7], rtol=0, atol=1e-30 + 1e-12)
+
+
+def test_scores_use_the_scale():
+    # Doubling the scale equals doubling q; a missing or misplaced scale fails.
+    rng = np.random.default_rng(5)
+    q, k, v = rand((2, 4), rng), rand((9, 2, 4), rng), rand((9, 2, 4), rng)
+    np.testing.assert_allclose(A.softmax_attention(q, k, v, 2.0),
+                               A.softmax_attention(2 * q, k, v, 1.0), rtol=1e-13, atol=1e-14)
+    assert not np.allclose(A.softmax_attention(q, k, v, 2.0), A.softmax_attention(q, k, v, 1.0))
+
+
+def test_partial_triple_against_brute_force():
+    rng = np.random.default_rng(6)
+    H, D, n = 2, 4, 11
+    q, k, v = rand((H, D), rng), rand((n, H, D), rng), rand((n, H, D), rng)
+    o, m, s = A.partial(q, k, v, 0.5)
+    for h in range(H):
+        x = [0.5 * sum(q[h][d] * k[t][h][d] for d in range(D)) for t in range(n)]
+        mm = max(x)
+        assert m[h] == pytest.approx(mm, abs=1e-15)
+        assert s[h] == pytest.approx(sum(math.exp(xi - mm) for xi in x), rel=1e-14)
+        for d in range(D):
+            want = sum(math.exp(x[t] - mm) * v[t][h][d] for t in range(n))
+            assert o[h][d] == pytest.approx(want, rel=1e-13, abs=1e-15)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_merge_identity_any_split(seed):
+    """Splitting a context into parts and merging their partials equals the
+    softmax over the whole context (the merge rule), including empty parts."""
+    rng = np.random.default_rng(100 + seed)
+    H, D, n = 3, 8, int(rng.integers(1, 60))
+    q, k, v = rand((H, D), rng, -3, 3), rand((n, H, D), rng, -3, 3), rand((n, H, D), rng)
+    cuts = sorted(rng.integers(0, n + 1, size=int(rng.integers(0, 6))).tolist())
+    bounds = [0] + cuts + [n]
+    parts = [A.partial(q, k[a:z], v[a:z], 0.9) for a, z in zip(bounds[:-1], bounds[1:])]
+    random.Random(seed).shuffle(parts)                 # order of parts is free
+    np.testing.assert_allclose(A.merge(parts), A.softmax_attention(q, k, v, 0.9),
+                               rtol=1e-12, atol=1e-13)
+
+
+def test_merge_of_only_empty_parts_is_an_error():
+    q = np.zeros((1, 2))
+    empty = A.partial(q, np.zeros((0, 1, 2)), np.zeros((0, 1, 2)), 1.0)
+    with pytest.raises(OracleError):
+        A.merge([empty, empty])
+
+
+def test_merge_needs_the_rescale():
+    # Parts whose maxima differ by a lot: a merge that skipped e^{m_j - m*}
+    # would weight the small part as much as the large one.
+    q = np.array([[1.0]])
+    k1, v1 = np.array([[[10.0]]]), np.array([[[1.0]]])
+    k2, v2 = np.array([[[0.0]]]), np.array([[[-1.0]]])
+    got = A.merge([A.partial(q, k1, v1, 1.0), A.partial(q, k2, v2, 1.0)])
+    w = math.exp(10) / (math.exp(10) + 1)
+    assert got[0, 0] == pytest.approx(w - (1 - w), rel=1e-14)
+
+
+def test_two_phase_single_prefix_equals_definition():
+    rng = np.random.default_rng(7)
+    b, H, D, ns = 5, 2, 8, 13
+    q = rand((b, H, D), rng, -2, 2)
+    pk, pv = rand((ns, H, D), rng, -2, 2), rand((ns, H, D), rng)
+    sk = [rand((int(rng.integers(0, 9)), H, D), rng, -2, 2) for _ in range(b)]
+    sv = [rand((x.shape[0], H, D), rng) for x in sk]
+    got = A.two_phase_single_prefix(q, pk, pv, sk, sv, 0.4)
+    for i in range(b):
+        want = brute_force(q[i].tolist(), np.concatenate([pk, sk[i]]).tolist(),
+                           np.concatenate([pv, sv[i]]).tolist(), 0.4)
+        np.testing.assert_allclose(got[i], want, rtol=1e-12, atol=1e-13)
+
+
+def test_decode_attention_over_trie_matches_brute_force():
+    rng = np.random.default_rng(8)
+    L, H, D, c = 2, 2, 4, 3
+    trie = OracleTrie(c, 64)
+    prefix = list(range(7))
+    pk, pv = rand((L, 7, H, D), rng), rand((L, 7, H, D), rng)
+    ctx = {}
+    for s in range(4):
+        tail = [100 + 10 * s + i for i in range(s + 1)]
+        tk, tv = rand((L, len(tail), H, D), rng), rand((L, len(tail), H, D), rng)
+        k, v = np.concatenate([pk, tk], 1), np.concatenate([pv, tv], 1)
+        trie.insert(s, prefix + tail, k, v)
+        ctx[s] = (k, v)
+    q = rand((4, H, D), rng)
+    for layer in range(L):
+        out = A.decode_attention(trie, [3, 1, 0, 2], layer, q, 0.5)
+        for i, s in enumerate([3, 1, 0, 2]):
+            k, v = ctx[s]
+            want = brute_force(q[i].tolist(), k[layer].tolist(), v[layer].tolist(), 0.5)
+            np.testing.assert_allclose(out[i], want, rtol=1e-12, atol=1e-13)

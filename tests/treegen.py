@@ -1,0 +1,31 @@
+"""Random prefix trees for tests: token lists only (no attention arithmetic)."""
+import numpy as np
+
+
+def random_token_lists(seed: int, n_seqs: int, chunk: int, alphabet: int = 3,
+                       max_len: int = 24, n_stems: int = 3):
+    """Sequences built from a few random stems plus random tails.  A small
+    alphabet makes chunk tuples collide across branches, so the tree gets
+    shared chunks, branch points, sequences ending at inner nodes and partial
+    leaves."""
+    rng = np.random.default_rng(seed)
+    stems = [rng.integers(0, alphabet, size=int(rng.integers(0, max_len))).tolist()
+             for _ in range(n_stems)]
+    out = []
+    for _ in range(n_seqs):
+        stem = stems[int(rng.integers(0, n_stems))]
+        cut = int(rng.integers(0, len(stem) + 1))
+        tail = rng.integers(0, alphabet, size=int(rng.integers(0, max_len // 2))).tolist()
+        toks = stem[:cut] + tail
+        if not toks:
+            toks = [int(rng.integers(0, alphabet))]
+        out.append(toks)
+    return out
+
+
+def lcp_chunks(a, b, c):
+    """Longest common prefix of two token lists, in whole chunks."""
+    k = 0
+    while (k + 1) * c <= min(len(a), len(b)) and a[k * c:(k + 1) * c] == b[k * c:(k + 1) * c]:
+        k += 1
+    return k
