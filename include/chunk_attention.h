@@ -1,0 +1,233 @@
+/*
+ * chunk_attention.h — C ABI of the prefix-shared decode attention library
+ * (libchunk_attention.so), a GB300 (sm_103a) implementation of ChunkAttention's
+ * decode hot path.
+ *
+ * Sources: "ChunkAttention: Efficient Self-Attention with Prefix-Aware KV Cache
+ * and Two-Phase Partition" (arXiv 2402.15220v4 summary), cited [CA §n], and
+ * the explainer "ACL 2024論文解説: ChunkAttention — プレフィックスKVキャッシュ共有
+ * によるマルチテナント推論高速化", cited [CA-blog, <section>].
+ *
+ * Model of the problem [CA §2.2, §3.1]: requests join with a prompt whose
+ * keys/values came from prefill, decode one token per step under iteration
+ * batching, and leave when done.  Their K/V live in fixed-size chunks that form
+ * a prefix tree; a chunk is stored once however many sequences share it.  Each
+ * decode step runs attention for the whole batch in two phases [CA §3.2]:
+ * chunk-first (every chunk shared by >= 2 batch sequences, against the batched
+ * queries of its sharers, on tensor cores) and sequence-first (each sequence's
+ * own chunks), whose partial results are merged by the log-sum-exp rule
+ * [CA-blog, Two-Phase Partition, output-combination equation].
+ *
+ * Conventions
+ *  - Every call returns an int status: CA_OK (0) or a negative CA_ERR_* code.
+ *    No C++ exception crosses this boundary and nothing aborts the process.
+ *    ca_error_string() names a code.
+ *  - Pointers named *_dev are device pointers the caller owns (e.g. torch
+ *    tensors); the library never frees them.  Host arrays are read during
+ *    the call only.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  All device work is enqueued asynchronously on it.
+ *  - Objects are not thread-safe: serialise calls on one pool.
+ *  - Element type of K, V, Q and out is IEEE fp16; accumulation is fp32.
+ */
+#ifndef CHUNK_ATTENTION_H
+#define CHUNK_ATTENTION_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define CA_OK                 0
+#define CA_ERR_INVALID       -1  /* bad argument, size, alignment or state    */
+#define CA_ERR_OOM           -2  /* no free chunk slots; the pool is unchanged */
+#define CA_ERR_NOT_FOUND     -3  /* unknown seq_id                             */
+#define CA_ERR_EXISTS        -4  /* seq_id already present                     */
+#define CA_ERR_STALE         -5  /* schedule built before the tree last changed */
+#define CA_ERR_CUDA          -6  /* a CUDA runtime/driver call failed          */
+#define CA_ERR_DEVICE_BOUNDS -7  /* a kernel saw a table index out of range    */
+#define CA_ERR_TIMEOUT       -8  /* a kernel wait gave up after ~1 s           */
+#define CA_ERR_UNSUPPORTED   -9  /* shape the kernels are not built for        */
+
+/* ---- pool flags -------------------------------------------------------- */
+/* Never match prefixes: every sequence owns a private chain of chunks.  This
+ * is the flat paged-KV layout [CA §5, PagedAttention] used as the control. */
+#define CA_NO_SHARING        1u
+
+/* ---- schedule flags ---------------------------------------------------- */
+/* Treat every chunk as sequence-first even when the batch shares it (no
+ * two-phase partition; shared chunks are read once per sharer).  Reproduces
+ * the pages' PagedAttn* comparator: physically shared KV without TPP
+ * [CA §4.1, Table 3]. */
+#define CA_SCHED_NO_TPP      1u
+
+typedef struct ca_pool  ca_pool;
+typedef struct ca_sched ca_sched;
+
+/* Shape of a pool.  head_dim must be 64 or 128, chunk 16, 32 or 64 tokens
+ * (the paper's kernel default is 64 [CA §4.1]); n_layers, n_heads and
+ * capacity_slots >= 1. */
+typedef struct {
+    int32_t  n_layers;
+    int32_t  n_heads;
+    int32_t  head_dim;
+    int32_t  chunk;           /* c: tokens per chunk                           */
+    int32_t  capacity_slots;  /* chunk slots in the device pool                */
+    uint32_t flags;           /* CA_NO_SHARING or 0                            */
+} ca_pool_config;
+
+typedef struct {
+    int64_t live_slots;       /* slots holding a chunk                         */
+    int64_t free_slots;
+    int64_t refcount_sum;     /* sum over live chunks of their refcount        */
+    int64_t live_seqs;
+    int64_t generation;       /* bumped by every insert and remove             */
+} ca_stats;
+
+/* ---- pool ----------------------------------------------------------------
+ * Device layout (row-major, fp16):
+ *     kv[slot][layer][K|V][head][c][head_dim]
+ * so one chunk of one head is a contiguous c x head_dim tile (16 KiB at
+ * c = 64, D = 128) that the kernels fetch whole with TMA.
+ */
+
+/* Bytes of device memory a pool with this shape needs (for kv_dev). */
+int ca_pool_bytes(const ca_pool_config* cfg, size_t* bytes_out);
+
+/* Create a pool over caller-owned device memory kv_dev of kv_bytes >=
+ * ca_pool_bytes(cfg); kv_dev must be 1024-byte aligned and must outlive the
+ * pool.  kv_dev == NULL creates a host-only pool (trie, allocator and
+ * schedule tables work; nothing touches a GPU; decode returns
+ * CA_ERR_INVALID).  [CA §3.1: chunked KV tensors in a prefix tree.] */
+int ca_pool_create(const ca_pool_config* cfg, void* kv_dev, size_t kv_bytes,
+                   ca_pool** pool_out);
+int ca_pool_destroy(ca_pool* pool);
+
+/* Leading tokens of tokens[0..n) whose K/V the pool already holds: the
+ * longest path of full chunks matching chunk by chunk from the root (a
+ * multiple of c; 0 with CA_NO_SHARING).  Lets a caller skip prefill of the
+ * matched prefix.  Does not change the pool. [CA-blog, 動的プレフィックス検出] */
+int ca_match_prefix(const ca_pool* pool, const int32_t* tokens, int32_t n,
+                    int32_t* n_matched_out);
+
+/* Add sequence seq_id with context tokens[0..n), n >= 1 [CA §3.1: new
+ * sequences add paths].  Full chunks that match the tree along the path gain a
+ * reference; every other chunk (and always the trailing partial chunk) gets a
+ * new slot, lowest free index first, and its K/V rows are copied on `stream`
+ * from k_dev / v_dev: fp16 [n_layers][n][n_heads][head_dim], contiguous, 16-byte
+ * aligned.  Rows of matched tokens are not read (the first inserter's rows are
+ * kept).  k_dev/v_dev must be NULL for a host-only pool and non-NULL
+ * otherwise.  n_shared_out (may be NULL) receives the matched token count.
+ * Errors: CA_ERR_EXISTS, CA_ERR_OOM (not enough free slots), CA_ERR_INVALID;
+ * on any error the pool is unchanged. */
+int ca_insert_tokens(ca_pool* pool, int64_t seq_id, const int32_t* tokens,
+                     int32_t n, const void* k_dev, const void* v_dev,
+                     void* stream, int32_t* n_shared_out);
+
+/* Remove a finished sequence [CA §3.1: completed sequences remove their
+ * path].  Every chunk on its path loses one reference; chunks left with none
+ * return their slot to the free list [CA-blog, 動的プレフィックス検出]. */
+int ca_remove_seq(ca_pool* pool, int64_t seq_id);
+
+int ca_pool_stats(const ca_pool* pool, ca_stats* out);
+
+/* Slots along seq_id's path, root first (test and inspection helper).
+ * Writes min(cap, path length) entries; *n_out = path length. */
+int ca_seq_slots(const ca_pool* pool, int64_t seq_id, int32_t* slots, int32_t cap,
+                 int32_t* n_out);
+
+/* ---- schedule -------------------------------------------------------------
+ * The per-step context of the two-phase kernel [CA §3.2, §3.3] for the batch
+ * seq_ids[0..b): which chunks are chunk-first and which sequences share each
+ * (one contiguous range of a depth-first batch order), each sequence's
+ * sequence-first chunks, and the merge lists; plus the kernels' work plan.
+ * *inout == NULL allocates a schedule; otherwise it is reused, and when the
+ * pool has not changed since it was built and the batch is identical it is
+ * returned untouched (the pages: context copies are cached until the tree
+ * changes [CA §3.3]).  Tables are copied to a library-owned device buffer
+ * with cudaMemcpyAsync on `stream` (none for a host-only pool).
+ * Errors: CA_ERR_NOT_FOUND (unknown seq_id), CA_ERR_INVALID (b < 1, duplicate
+ * ids), CA_ERR_CUDA. */
+int ca_build_schedule(ca_pool* pool, const int64_t* seq_ids, int32_t b,
+                      uint32_t flags, ca_sched** inout, void* stream);
+int ca_sched_destroy(ca_sched* sched);
+
+/* Table sizes, then the tables themselves (host copies; for bit-exact tests).
+ * counts[0..5] = b, R (chunk-first rows), U (runs), S (sequence-first
+ * chunks), M (merge entries), n_units (kernel work units). */
+int ca_sched_counts(const ca_sched* sched, int32_t counts[6]);
+/* Any pointer may be NULL to skip that table.  Layouts (int32):
+ *   seq_perm[b]           DFS position -> row of Q / out (index into seq_ids)
+ *   cf_rows[R][4]         (slot, ntok, lo, hi), DFS pre-order
+ *   cf_runs[U][4]         (row0, nrows, lo, hi)
+ *   sf_offsets[b+1], sf_chunks[S][2] (slot, ntok)
+ *   merge_offsets[b+1], merge_runs[M] */
+int ca_export_tables(const ca_sched* sched, int32_t* seq_perm, int32_t* cf_rows,
+                     int32_t* cf_runs, int32_t* sf_offsets, int32_t* sf_chunks,
+                     int32_t* merge_offsets, int32_t* merge_runs);
+
+/* The kernel work plan derived from the tables (inspection and tests).
+ * counts[0..3] = n_units, grid (CTAs), n_pbase (= b * n_heads + 1),
+ * n_chunks.  Any array may be NULL.  Layouts (int32):
+ *   units[n_units][8]  (kind 0 = chunk-first / 1 = sequence-first, head,
+ *                       pos_lo, pos_hi, chunk_begin, chunk_end, part, 0)
+ *   cta_begin[grid+1]  unit range of each CTA
+ *   pbase[n_pbase]     partial ids of (position p, head h) are
+ *                      [pbase[p*H+h], pbase[p*H+h+1]); a unit writes id
+ *                      pbase[p*H+h] + part for each position it covers
+ *   chunks[n_chunks][2] (slot, ntok) list the units index into */
+int ca_export_plan(const ca_sched* sched, int32_t counts[4], int32_t* units,
+                   int32_t* cta_begin, int32_t* pbase, int32_t* chunks);
+
+/* Bytes of caller-owned device workspace ca_decode_attention needs for this
+ * schedule (partial results and merge counters). */
+int ca_workspace_bytes(const ca_sched* sched, size_t* bytes_out);
+
+/* ---- decode attention -----------------------------------------------------
+ * out[i][h][:] = sum_t softmax_t(scale * q[i][h] . k_t) v_t over every token
+ * t of sequence seq_ids[i]'s context, computed by the two-phase partition
+ * [CA §3.2; CA-blog, Two-Phase Partition].
+ *   q_dev    fp16 [b][n_heads][head_dim], row i = seq_ids[i] of the schedule
+ *   out_dev  fp16 [b][n_heads][head_dim], written
+ *   layer    0 <= layer < n_layers
+ *   ws_dev   >= ca_workspace_bytes(sched) bytes, 256-byte aligned, caller
+ *            owned.  It must be zero-filled before its first use; every
+ *            completed call leaves it ready for the next one (any schedule).
+ *            Calls sharing one workspace must not overlap on the GPU.
+ * Errors: CA_ERR_STALE if the pool changed after the schedule was built;
+ * CA_ERR_INVALID for a host-only pool, bad layer, NULL or misaligned pointers
+ * or a small workspace; CA_ERR_CUDA if a launch fails.  Kernel-side faults
+ * (an index out of range, a wait that timed out) are reported by
+ * ca_sched_device_status(). */
+int ca_decode_attention(const ca_pool* pool, const ca_sched* sched, int32_t layer,
+                        const void* q_dev, void* out_dev, float scale,
+                        void* ws_dev, size_t ws_bytes, void* stream);
+
+/* The same computation with q and out in HOST memory (pinned for overlap):
+ * copies q in, runs the kernels and copies out back, all on `stream`; the
+ * caller synchronises.  ws_dev needs ca_workspace_bytes_host(sched) bytes
+ * (the device staging for q and out lives at its end). */
+int ca_workspace_bytes_host(const ca_sched* sched, size_t* bytes_out);
+int ca_decode_attention_host(const ca_pool* pool, const ca_sched* sched,
+                             int32_t layer, const void* q_host, void* out_host,
+                             float scale, void* ws_dev, size_t ws_bytes,
+                             void* stream);
+
+/* Synchronise `stream` and read the schedule's device status word: CA_OK,
+ * CA_ERR_DEVICE_BOUNDS or CA_ERR_TIMEOUT; the word is then cleared. */
+int ca_sched_device_status(const ca_sched* sched, void* stream);
+
+/* Optional timing hook: when both are non-NULL, ca_decode_attention records
+ * event_begin (a cudaEvent_t) just before its main kernel and event_end just
+ * after it, on `stream`.  Pass NULLs to turn it off. */
+int ca_sched_set_profile_events(ca_sched* sched, void* event_begin, void* event_end);
+
+const char* ca_error_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CHUNK_ATTENTION_H */

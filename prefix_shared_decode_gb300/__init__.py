@@ -1,0 +1,245 @@
+"""Prefix-shared decode attention (ChunkAttention's hot path) for GB300.
+
+A thin binding over libchunk_attention (include/chunk_attention.h): every
+step of the path runs in the library's C++ host code and sm_103a CUDA
+kernels; this module only marshals arguments.  PyTorch supplies device
+memory and streams.
+
+    pool = Pool(n_layers=1, n_heads=32, head_dim=128, chunk=64, capacity_slots=...)
+    pool.insert(seq_id, tokens, k, v)          # K/V fp16 [L, n, H, D] on the GPU
+    sched = pool.schedule(seq_ids)             # per-step two-phase tables
+    out = decode_attention(pool, sched, q)     # q fp16 [b, H, D] on the GPU
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+
+import numpy as np
+
+from . import capi
+from .capi import CAError, check
+
+__all__ = ["Pool", "Schedule", "decode_attention", "decode_attention_host", "CAError"]
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        import torch
+        if not torch.cuda.is_available():
+            return None
+        stream = torch.cuda.current_stream()
+    return int(getattr(stream, "cuda_stream", stream)) or None
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+class Pool:
+    """A prefix-aware KV cache: the chunk trie and its device pool.
+
+    With ``host_only=True`` no GPU memory is touched (trie, allocator and
+    schedule tables only)."""
+
+    def __init__(self, n_layers: int, n_heads: int, head_dim: int, chunk: int,
+                 capacity_slots: int, no_sharing: bool = False, host_only: bool = False,
+                 device=None):
+        L = capi.lib()
+        self.cfg = capi.PoolConfig(n_layers, n_heads, head_dim, chunk, capacity_slots,
+                                   capi.CA_NO_SHARING if no_sharing else 0)
+        self.n_layers, self.n_heads, self.head_dim, self.chunk = n_layers, n_heads, head_dim, chunk
+        self.capacity_slots = capacity_slots
+        nbytes = C.c_size_t()
+        check(L.ca_pool_bytes(C.byref(self.cfg), C.byref(nbytes)), "ca_pool_bytes")
+        self.kv_bytes = nbytes.value
+        self._kv = None
+        ptr = None
+        if not host_only:
+            import torch
+            dev = torch.device(device if device is not None else "cuda")
+            # over-allocate so the pool can start on a 1024-byte boundary
+            self._kv = torch.empty(self.kv_bytes + 1024, dtype=torch.uint8, device=dev)
+            base = self._kv.data_ptr()
+            ptr = (base + 1023) // 1024 * 1024
+            self._kv_offset = ptr - base
+        self.host_only = host_only
+        h = C.c_void_p()
+        check(L.ca_pool_create(C.byref(self.cfg), ptr, self.kv_bytes, C.byref(h)), "ca_pool_create")
+        self._h = h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            capi.lib().ca_pool_destroy(h)
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    def kv_view(self):
+        """The device pool as fp16 [slots, L, 2, H, c, D] (a view, no copy)."""
+        import torch
+        t = self._kv[self._kv_offset:self._kv_offset + self.kv_bytes].view(torch.float16)
+        return t.view(self.capacity_slots, self.n_layers, 2, self.n_heads, self.chunk, self.head_dim)
+
+    def match_prefix(self, tokens) -> int:
+        tok = _i32(tokens)
+        n = C.c_int32()
+        check(capi.lib().ca_match_prefix(self._h, tok.ctypes.data_as(C.POINTER(C.c_int32)),
+                                          len(tok), C.byref(n)), "ca_match_prefix")
+        return n.value
+
+    def insert(self, seq_id: int, tokens, k=None, v=None, stream=None) -> int:
+        """Insert a sequence; k, v are fp16 device tensors [L, n, H, D]
+        (None for a host-only pool).  Returns the number of shared tokens."""
+        tok = _i32(tokens)
+        kp = vp = None
+        if k is not None:
+            assert k.is_contiguous() and v.is_contiguous()
+            assert tuple(k.shape) == (self.n_layers, len(tok), self.n_heads, self.head_dim)
+            kp, vp = k.data_ptr(), v.data_ptr()
+        shared = C.c_int32()
+        check(capi.lib().ca_insert_tokens(self._h, int(seq_id), tok.ctypes.data_as(C.POINTER(C.c_int32)),
+                                          len(tok), kp, vp,
+                                          None if self.host_only else _stream_ptr(stream),
+                                          C.byref(shared)), "ca_insert_tokens")
+        return shared.value
+
+    def remove(self, seq_id: int) -> None:
+        check(capi.lib().ca_remove_seq(self._h, int(seq_id)), "ca_remove_seq")
+
+    def stats(self) -> dict:
+        s = capi.Stats()
+        check(capi.lib().ca_pool_stats(self._h, C.byref(s)), "ca_pool_stats")
+        return {f: getattr(s, f) for f, _ in capi.Stats._fields_}
+
+    def seq_slots(self, seq_id: int) -> list[int]:
+        n = C.c_int32()
+        check(capi.lib().ca_seq_slots(self._h, int(seq_id), None, 0, C.byref(n)), "ca_seq_slots")
+        buf = (C.c_int32 * max(1, n.value))()
+        check(capi.lib().ca_seq_slots(self._h, int(seq_id), buf, n.value, C.byref(n)), "ca_seq_slots")
+        return list(buf)[:n.value]
+
+    def schedule(self, seq_ids, no_tpp: bool = False, reuse: "Schedule | None" = None,
+                 stream=None) -> "Schedule":
+        """Per-step tables for the batch ``seq_ids`` (rows of q / out in that
+        order).  Passing the previous schedule reuses it when nothing changed."""
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        s = reuse if reuse is not None else Schedule(self)
+        h = s._h if s._h is not None else C.c_void_p()
+        check(capi.lib().ca_build_schedule(self._h, ids.ctypes.data_as(C.POINTER(C.c_int64)), len(ids),
+                                           capi.CA_SCHED_NO_TPP if no_tpp else 0, C.byref(h),
+                                           None if self.host_only else _stream_ptr(stream)),
+              "ca_build_schedule")
+        s._h = h
+        s.b = len(ids)
+        return s
+
+
+class Schedule:
+    """The two-phase context of one batch (owned by the library)."""
+
+    def __init__(self, pool: Pool):
+        self.pool = pool
+        self._h = None
+        self.b = 0
+        self._ws = None
+
+    def __del__(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            capi.lib().ca_sched_destroy(self._h)
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    def counts(self) -> dict:
+        c = (C.c_int32 * 6)()
+        check(capi.lib().ca_sched_counts(self._h, c), "ca_sched_counts")
+        return dict(zip(["b", "cf_rows", "cf_runs", "sf_chunks", "merge_runs", "units"], list(c)))
+
+    def tables(self) -> dict[str, np.ndarray]:
+        n = self.counts()
+        b, R, U, S, M = n["b"], n["cf_rows"], n["cf_runs"], n["sf_chunks"], n["merge_runs"]
+        out = {"seq_perm": np.zeros(b, np.int32), "cf_rows": np.zeros((R, 4), np.int32),
+               "cf_runs": np.zeros((U, 4), np.int32), "sf_offsets": np.zeros(b + 1, np.int32),
+               "sf_chunks": np.zeros((S, 2), np.int32), "merge_offsets": np.zeros(b + 1, np.int32),
+               "merge_runs": np.zeros(M, np.int32)}
+        ptr = lambda a: a.ctypes.data_as(C.POINTER(C.c_int32))
+        check(capi.lib().ca_export_tables(self._h, *[ptr(out[k]) for k in
+                                                     ["seq_perm", "cf_rows", "cf_runs", "sf_offsets",
+                                                      "sf_chunks", "merge_offsets", "merge_runs"]]),
+              "ca_export_tables")
+        return out
+
+    def plan(self) -> dict[str, np.ndarray]:
+        """The kernel work plan (units, per-CTA ranges, partial-id CSR, chunk list)."""
+        cnt = (C.c_int32 * 4)()
+        L = capi.lib()
+        check(L.ca_export_plan(self._h, cnt, None, None, None, None), "ca_export_plan")
+        n_units, grid, n_pbase, n_chunks = list(cnt)
+        out = {"units": np.zeros((n_units, 8), np.int32), "cta_begin": np.zeros(grid + 1, np.int32),
+               "pbase": np.zeros(n_pbase, np.int32), "chunks": np.zeros((n_chunks, 2), np.int32)}
+        ptr = lambda a: a.ctypes.data_as(C.POINTER(C.c_int32))
+        check(L.ca_export_plan(self._h, cnt, ptr(out["units"]), ptr(out["cta_begin"]),
+                               ptr(out["pbase"]), ptr(out["chunks"])), "ca_export_plan")
+        out["grid"] = grid
+        return out
+
+    def workspace_bytes(self, host_io: bool = False) -> int:
+        n = C.c_size_t()
+        fn = capi.lib().ca_workspace_bytes_host if host_io else capi.lib().ca_workspace_bytes
+        check(fn(self._h, C.byref(n)), "ca_workspace_bytes")
+        return n.value
+
+    def workspace(self, host_io: bool = False):
+        """A zero-filled device workspace large enough for this schedule
+        (cached and grown on demand)."""
+        import torch
+        need = self.workspace_bytes(host_io)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=self.pool._kv.device)
+        return self._ws
+
+    def device_status(self, stream=None) -> int:
+        return capi.lib().ca_sched_device_status(self._h, _stream_ptr(stream))
+
+    def set_profile_events(self, begin=None, end=None) -> None:
+        bp = begin.cuda_event if begin is not None else None
+        ep = end.cuda_event if end is not None else None
+        check(capi.lib().ca_sched_set_profile_events(self._h, bp, ep), "ca_sched_set_profile_events")
+
+
+def decode_attention(pool: Pool, sched: Schedule, q, out=None, layer: int = 0, scale: float | None = None,
+                     workspace=None, stream=None):
+    """out[i, h] = softmax(scale q[i, h] . K^T) V over sequence seq_ids[i]'s
+    context, via the two-phase kernel.  q: fp16 [b, H, D] on the GPU."""
+    import torch
+    assert q.dtype == torch.float16 and q.is_contiguous()
+    assert tuple(q.shape) == (sched.b, pool.n_heads, pool.head_dim)
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(pool.head_dim)
+    ws = workspace if workspace is not None else sched.workspace()
+    check(capi.lib().ca_decode_attention(pool._h, sched._h, layer, q.data_ptr(), out.data_ptr(),
+                                         float(scale), ws.data_ptr(), ws.numel(), _stream_ptr(stream)),
+          "ca_decode_attention")
+    return out
+
+
+def decode_attention_host(pool: Pool, sched: Schedule, q_host, out_host, layer: int = 0,
+                          scale: float | None = None, workspace=None, stream=None):
+    """The same with q / out in (pinned) host memory; copies in, computes and
+    copies out on ``stream``; the caller synchronises."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(pool.head_dim)
+    ws = workspace if workspace is not None else sched.workspace(host_io=True)
+    check(capi.lib().ca_decode_attention_host(pool._h, sched._h, layer, q_host.data_ptr(),
+                                              out_host.data_ptr(), float(scale), ws.data_ptr(),
+                                              ws.numel(), _stream_ptr(stream)),
+          "ca_decode_attention_host")
+    return out_host

@@ -1,0 +1,166 @@
+// Internal declarations shared by the host library (C++17) and the CUDA
+// kernels of libchunk_attention.  Nothing here is part of the public C ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <memory>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include <vector_types.h>
+
+#include "../../include/chunk_attention.h"
+
+namespace ca {
+
+// ---------------------------------------------------------------------------
+// Work plan read by the attention kernel (uploaded to the device as one blob).
+//
+// A unit is one stretch of chunks that one CTA streams for one head:
+//  * UNIT_CF (chunk-first): rows [c_begin, c_end) of one run of chunks shared
+//    by batch positions [q_lo, q_hi) (at most 64 of them), all against the
+//    batched queries of those positions [ChunkAttention §3.2: the queries of
+//    the sequences that share a chunk form a matrix for tensor-core matmul].
+//  * UNIT_SF (sequence-first): some of position q_lo's own chunks.
+// Every unit leaves one partial triple (o, m, s) per covered position; the
+// partials of (position p, head h) occupy ids [pbase[p*H+h], pbase[p*H+h+1]).
+// ---------------------------------------------------------------------------
+enum : int32_t { UNIT_CF = 0, UNIT_SF = 1 };
+
+struct ChunkRef {      // one chunk the kernel reads
+    int32_t slot;      // pool slot
+    int32_t ntok;      // valid tokens in it (1..c)
+};
+
+struct Unit {
+    int32_t kind;      // UNIT_CF or UNIT_SF
+    int32_t head;
+    int32_t q_lo;      // first batch position
+    int32_t q_hi;      // one past the last batch position
+    int32_t c_begin;   // chunk range in the ChunkRef list
+    int32_t c_end;
+    int32_t part;      // partial index within each covered (position, head)
+    int32_t pad;
+};
+
+// Offsets (in bytes) of the arrays inside the device plan blob.
+struct PlanLayout {
+    size_t chunks, units, cta_begin, seq_perm, pbase, status, total;
+};
+
+// Parameters of the attention kernel (passed by value).
+struct AttnParams {
+    const ChunkRef* chunks;
+    const Unit* units;
+    const int32_t* cta_begin;    // [grid + 1] unit ranges per CTA
+    const int32_t* seq_perm;     // [b] position -> row of q / out
+    const int32_t* pbase;        // [b*H + 1] partial-id CSR per (position, head)
+    int32_t* status;             // device status word (CA_ERR_* or 0)
+    const uint16_t* q;           // fp16 [b][H][D]
+    uint16_t* out;               // fp16 [b][H][D]
+    int32_t* counters;           // [b*H] merge arrival counters (zero between calls)
+    float* part_o;               // [P][D] unnormalised partial outputs
+    float2* part_ms;             // [P] (running max in log2 units, sum of exp2)
+    int32_t n_layers, n_heads, layer, capacity;
+    float scale_log2;            // scale * log2(e)
+    int32_t n_stages;
+};
+
+// Workspace layout for a schedule.
+struct WsLayout {
+    size_t counters, part_o, part_ms, total;        // device-resident inputs
+    size_t q_stage, out_stage, total_host;          // + staging for host I/O
+};
+
+// ---------------------------------------------------------------------------
+// Host objects.
+// ---------------------------------------------------------------------------
+struct Node {
+    int32_t slot = -1;
+    std::vector<int32_t> tokens;   // the chunk's token ids (ntok = size)
+    Node* parent = nullptr;
+    std::vector<Node*> children;   // insertion order
+    // full shareable chunks only, keyed by their token tuple
+    std::unordered_map<std::string, Node*> match;
+    int32_t refcount = 0;
+    int32_t mark = 0;              // scratch for schedule building
+    int32_t row = -1;              // scratch: chunk-first row while building
+};
+
+struct Sequence {
+    std::vector<Node*> path;
+    int32_t length = 0;
+};
+
+struct Pool {
+    ca_pool_config cfg{};
+    void* kv = nullptr;            // device pool (nullptr: host only)
+    size_t kv_bytes = 0;
+    int device = -1;
+    int num_sms = 0;
+    alignas(64) unsigned char tmap[128];  // CUtensorMap over the pool
+    std::unique_ptr<Node> root;
+    std::vector<std::unique_ptr<Node>> nodes_by_slot;  // owner, indexed by slot
+    std::vector<int32_t> heap;     // min-heap of free slots
+    std::unordered_map<int64_t, Sequence> seqs;
+    int64_t generation = 0;
+};
+
+struct Tables {
+    int32_t b = 0;
+    std::vector<int32_t> seq_perm, cf_rows, cf_runs, sf_offsets, sf_chunks,
+        merge_offsets, merge_runs;
+};
+
+struct Plan {
+    std::vector<ChunkRef> chunks;
+    std::vector<Unit> units;
+    std::vector<int32_t> cta_begin;
+    std::vector<int32_t> pbase;
+    int32_t grid = 0;
+    int64_t n_partials = 0;
+};
+
+struct Sched {
+    const Pool* pool = nullptr;
+    int64_t generation = -1;
+    uint32_t flags = 0;
+    std::vector<int64_t> seq_ids;
+    Tables t;
+    Plan plan;
+    PlanLayout layout{};
+    WsLayout ws{};
+    std::vector<unsigned char> blob;   // host copy of the device plan
+    void* dev = nullptr;               // device plan blob
+    size_t dev_bytes = 0;
+    void* host_pinned = nullptr;       // pinned staging of the blob
+    size_t host_pinned_bytes = 0;
+    void* ev_begin = nullptr;
+    void* ev_end = nullptr;
+};
+
+// pool.cpp
+int pool_insert(Pool& p, int64_t seq_id, const int32_t* tokens, int32_t n,
+                std::vector<std::pair<int32_t, int32_t>>* new_chunks,  // (first token, slot)
+                int32_t* n_shared);
+int pool_remove(Pool& p, int64_t seq_id);
+int32_t pool_match(const Pool& p, const int32_t* tokens, int32_t n);
+
+// schedule.cpp
+int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flags, Tables& t);
+void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan);
+void layout_plan(const Plan& plan, int32_t b, PlanLayout& lay, std::vector<unsigned char>& blob,
+                 const Tables& t);
+void layout_ws(const Plan& plan, const Pool& p, int32_t b, WsLayout& ws);
+
+// kernels.cu
+int kernel_smem_bytes(int chunk, int head_dim, int* n_stages, size_t* bytes);
+int kernel_ctas_per_sm(int chunk, int head_dim, int* ctas);
+int make_tensor_map(Pool& p);
+int launch_scatter(const Pool& p, const void* k, const void* v, int32_t n,
+                   const std::vector<std::pair<int32_t, int32_t>>& new_chunks, void* stream);
+int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void* stream);
+
+}  // namespace ca

@@ -1,0 +1,368 @@
+// The C ABI of libchunk_attention (declared in include/chunk_attention.h):
+// argument checks, object lifetimes and the host side of each call.  No C++
+// exception crosses this boundary.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <new>
+
+#include "ca_internal.h"
+
+using namespace ca;
+
+struct ca_pool : Pool {};
+struct ca_sched : Sched {};
+
+namespace {
+
+constexpr int32_t kHostOnlyGrid = 2 * 152;   // plan grid for a pool with no GPU
+
+template <class F>
+int guard(F&& f) {
+    try {
+        return f();
+    } catch (const std::bad_alloc&) {
+        return CA_ERR_OOM;
+    } catch (...) {
+        return CA_ERR_INVALID;
+    }
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_cfg(const ca_pool_config* c) {
+    if (!c) return CA_ERR_INVALID;
+    if (c->n_layers < 1 || c->n_heads < 1 || c->capacity_slots < 1) return CA_ERR_INVALID;
+    if (c->head_dim != 64 && c->head_dim != 128) return CA_ERR_UNSUPPORTED;
+    if (c->chunk != 16 && c->chunk != 32 && c->chunk != 64) return CA_ERR_UNSUPPORTED;
+    if (c->flags & ~CA_NO_SHARING) return CA_ERR_INVALID;
+    // TMA row coordinates are 32-bit.
+    const long double rows = (long double)c->capacity_slots * c->n_layers * 2 * c->n_heads * c->chunk;
+    if (rows > 2147483647.0L) return CA_ERR_UNSUPPORTED;
+    return CA_OK;
+}
+
+size_t pool_bytes(const ca_pool_config& c) {
+    return (size_t)c.capacity_slots * c.n_layers * 2 * c.n_heads * c.chunk * c.head_dim * 2;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? CA_OK : CA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int ca_pool_bytes(const ca_pool_config* cfg, size_t* bytes_out) {
+    int st = check_cfg(cfg);
+    if (st) return st;
+    if (!bytes_out) return CA_ERR_INVALID;
+    *bytes_out = pool_bytes(*cfg);
+    return CA_OK;
+}
+
+int ca_pool_create(const ca_pool_config* cfg, void* kv_dev, size_t kv_bytes, ca_pool** pool_out) {
+    return guard([&] {
+        int st = check_cfg(cfg);
+        if (st) return st;
+        if (!pool_out) return CA_ERR_INVALID;
+        *pool_out = nullptr;
+        if (kv_dev && (!aligned(kv_dev, 1024) || kv_bytes < pool_bytes(*cfg))) return CA_ERR_INVALID;
+        std::unique_ptr<ca_pool> p(new ca_pool());
+        p->cfg = *cfg;
+        p->kv = kv_dev;
+        p->kv_bytes = kv_bytes;
+        p->root.reset(new Node());
+        p->nodes_by_slot.resize(cfg->capacity_slots);
+        p->heap.resize(cfg->capacity_slots);
+        for (int32_t i = 0; i < cfg->capacity_slots; ++i) p->heap[i] = i;   // sorted = min-heap
+        if (kv_dev) {
+            if (cudaGetDevice(&p->device) != cudaSuccess) return CA_ERR_CUDA;
+            if (cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess)
+                return CA_ERR_CUDA;
+            int ctas = 1;
+            st = kernel_ctas_per_sm(cfg->chunk, cfg->head_dim, &ctas);
+            if (st) return st;
+            p->num_sms *= ctas;   // grid = resident CTAs
+            st = make_tensor_map(*p);
+            if (st) return st;
+        }
+        *pool_out = p.release();
+        return CA_OK;
+    });
+}
+
+int ca_pool_destroy(ca_pool* pool) {
+    delete pool;
+    return CA_OK;
+}
+
+int ca_match_prefix(const ca_pool* pool, const int32_t* tokens, int32_t n, int32_t* n_matched_out) {
+    if (!pool || !n_matched_out || n < 0 || (n > 0 && !tokens)) return CA_ERR_INVALID;
+    return guard([&] {
+        *n_matched_out = pool_match(*pool, tokens, n);
+        return CA_OK;
+    });
+}
+
+int ca_insert_tokens(ca_pool* pool, int64_t seq_id, const int32_t* tokens, int32_t n,
+                     const void* k_dev, const void* v_dev, void* stream, int32_t* n_shared_out) {
+    if (!pool || n <= 0 || !tokens) return CA_ERR_INVALID;
+    if (pool->kv) {
+        if (!k_dev || !v_dev || !aligned(k_dev, 16) || !aligned(v_dev, 16)) return CA_ERR_INVALID;
+    } else if (k_dev || v_dev) {
+        return CA_ERR_INVALID;
+    }
+    return guard([&] {
+        std::vector<std::pair<int32_t, int32_t>> fresh;
+        int32_t shared = 0;
+        const int64_t gen = pool->generation;
+        int st = pool_insert(*pool, seq_id, tokens, n, &fresh, &shared);
+        if (st) return st;
+        if (pool->kv) {
+            st = launch_scatter(*pool, k_dev, v_dev, n, fresh, stream);
+            if (st) {                       // undo: the pool must be unchanged
+                pool_remove(*pool, seq_id);
+                pool->generation = gen;
+                return st;
+            }
+        }
+        if (n_shared_out) *n_shared_out = shared;
+        return CA_OK;
+    });
+}
+
+int ca_remove_seq(ca_pool* pool, int64_t seq_id) {
+    if (!pool) return CA_ERR_INVALID;
+    return guard([&] { return pool_remove(*pool, seq_id); });
+}
+
+int ca_pool_stats(const ca_pool* pool, ca_stats* out) {
+    if (!pool || !out) return CA_ERR_INVALID;
+    return guard([&] {
+        ca_stats s{};
+        s.free_slots = (int64_t)pool->heap.size();
+        s.live_slots = pool->cfg.capacity_slots - s.free_slots;
+        for (const auto& n : pool->nodes_by_slot)
+            if (n) s.refcount_sum += n->refcount;
+        s.live_seqs = (int64_t)pool->seqs.size();
+        s.generation = pool->generation;
+        *out = s;
+        return CA_OK;
+    });
+}
+
+int ca_seq_slots(const ca_pool* pool, int64_t seq_id, int32_t* slots, int32_t cap, int32_t* n_out) {
+    if (!pool || !n_out || cap < 0 || (cap > 0 && !slots)) return CA_ERR_INVALID;
+    auto it = pool->seqs.find(seq_id);
+    if (it == pool->seqs.end()) return CA_ERR_NOT_FOUND;
+    const auto& path = it->second.path;
+    for (int32_t i = 0; i < cap && i < (int32_t)path.size(); ++i) slots[i] = path[i]->slot;
+    *n_out = (int32_t)path.size();
+    return CA_OK;
+}
+
+int ca_build_schedule(ca_pool* pool, const int64_t* seq_ids, int32_t b, uint32_t flags,
+                      ca_sched** inout, void* stream) {
+    if (!pool || !inout || !seq_ids || b < 1 || (flags & ~CA_SCHED_NO_TPP)) return CA_ERR_INVALID;
+    return guard([&] {
+        ca_sched* s = *inout;
+        if (s && s->pool == pool && s->generation == pool->generation && s->flags == flags &&
+            (int32_t)s->seq_ids.size() == b && std::equal(seq_ids, seq_ids + b, s->seq_ids.begin()))
+            return CA_OK;                   // context unchanged since the tree last changed
+        Tables t;
+        int st = build_tables(*pool, seq_ids, b, flags, t);
+        if (st) return st;
+        std::unique_ptr<ca_sched> fresh;
+        if (!s) {
+            fresh.reset(new ca_sched());
+            s = fresh.get();
+        }
+        s->pool = pool;
+        s->flags = flags;
+        s->seq_ids.assign(seq_ids, seq_ids + b);
+        s->t = std::move(t);
+        build_plan(*pool, s->t, pool->kv ? pool->num_sms : kHostOnlyGrid, s->plan);
+        layout_plan(s->plan, b, s->layout, s->blob, s->t);
+        layout_ws(s->plan, *pool, b, s->ws);
+        if (pool->kv) {
+            if (s->dev_bytes < s->blob.size()) {
+                if (s->dev) cudaFree(s->dev);
+                s->dev = nullptr;
+                s->dev_bytes = 0;
+                if (cudaMalloc(&s->dev, s->blob.size()) != cudaSuccess) {
+                    s->generation = -1;
+                    return CA_ERR_CUDA;
+                }
+                s->dev_bytes = s->blob.size();
+            }
+            if (cudaMemcpyAsync(s->dev, s->blob.data(), s->blob.size(), cudaMemcpyHostToDevice,
+                                static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+                s->generation = -1;
+                return CA_ERR_CUDA;
+            }
+        }
+        s->generation = pool->generation;
+        if (fresh) *inout = fresh.release();
+        return CA_OK;
+    });
+}
+
+int ca_sched_destroy(ca_sched* sched) {
+    if (!sched) return CA_OK;
+    if (sched->dev) cudaFree(sched->dev);
+    delete sched;
+    return CA_OK;
+}
+
+int ca_sched_counts(const ca_sched* s, int32_t counts[6]) {
+    if (!s || !counts) return CA_ERR_INVALID;
+    counts[0] = s->t.b;
+    counts[1] = (int32_t)(s->t.cf_rows.size() / 4);
+    counts[2] = (int32_t)(s->t.cf_runs.size() / 4);
+    counts[3] = (int32_t)(s->t.sf_chunks.size() / 2);
+    counts[4] = (int32_t)s->t.merge_runs.size();
+    counts[5] = (int32_t)s->plan.units.size();
+    return CA_OK;
+}
+
+int ca_export_tables(const ca_sched* s, int32_t* seq_perm, int32_t* cf_rows, int32_t* cf_runs,
+                     int32_t* sf_offsets, int32_t* sf_chunks, int32_t* merge_offsets,
+                     int32_t* merge_runs) {
+    if (!s) return CA_ERR_INVALID;
+    auto put = [](int32_t* dst, const std::vector<int32_t>& v) {
+        if (dst && !v.empty()) std::memcpy(dst, v.data(), v.size() * sizeof(int32_t));
+    };
+    put(seq_perm, s->t.seq_perm);
+    put(cf_rows, s->t.cf_rows);
+    put(cf_runs, s->t.cf_runs);
+    put(sf_offsets, s->t.sf_offsets);
+    put(sf_chunks, s->t.sf_chunks);
+    put(merge_offsets, s->t.merge_offsets);
+    put(merge_runs, s->t.merge_runs);
+    return CA_OK;
+}
+
+int ca_export_plan(const ca_sched* s, int32_t counts[4], int32_t* units, int32_t* cta_begin,
+                   int32_t* pbase, int32_t* chunks) {
+    if (!s || !counts) return CA_ERR_INVALID;
+    counts[0] = (int32_t)s->plan.units.size();
+    counts[1] = s->plan.grid;
+    counts[2] = (int32_t)s->plan.pbase.size();
+    counts[3] = (int32_t)s->plan.chunks.size();
+    static_assert(sizeof(Unit) == 8 * sizeof(int32_t), "Unit is 8 int32");
+    static_assert(sizeof(ChunkRef) == 2 * sizeof(int32_t), "ChunkRef is 2 int32");
+    if (units && !s->plan.units.empty())
+        std::memcpy(units, s->plan.units.data(), s->plan.units.size() * sizeof(Unit));
+    if (cta_begin) std::memcpy(cta_begin, s->plan.cta_begin.data(), s->plan.cta_begin.size() * sizeof(int32_t));
+    if (pbase) std::memcpy(pbase, s->plan.pbase.data(), s->plan.pbase.size() * sizeof(int32_t));
+    if (chunks && !s->plan.chunks.empty())
+        std::memcpy(chunks, s->plan.chunks.data(), s->plan.chunks.size() * sizeof(ChunkRef));
+    return CA_OK;
+}
+
+int ca_workspace_bytes(const ca_sched* s, size_t* bytes_out) {
+    if (!s || !bytes_out) return CA_ERR_INVALID;
+    *bytes_out = s->ws.total;
+    return CA_OK;
+}
+
+int ca_workspace_bytes_host(const ca_sched* s, size_t* bytes_out) {
+    if (!s || !bytes_out) return CA_ERR_INVALID;
+    *bytes_out = s->ws.total_host;
+    return CA_OK;
+}
+
+static int decode_checks(const ca_pool* pool, const ca_sched* s, int32_t layer, void* ws_dev,
+                         size_t ws_bytes, size_t need) {
+    if (!pool || !s || !pool->kv || s->pool != pool || !s->dev) return CA_ERR_INVALID;
+    if (s->generation != pool->generation) return CA_ERR_STALE;
+    if (layer < 0 || layer >= pool->cfg.n_layers) return CA_ERR_INVALID;
+    if (!ws_dev || !aligned(ws_dev, 256) || ws_bytes < need) return CA_ERR_INVALID;
+    return CA_OK;
+}
+
+static int decode_launch(const ca_pool* pool, const ca_sched* s, int32_t layer, const void* q,
+                         void* out, float scale, void* ws_dev, void* stream) {
+    unsigned char* dev = static_cast<unsigned char*>(s->dev);
+    unsigned char* ws = static_cast<unsigned char*>(ws_dev);
+    AttnParams a{};
+    a.chunks = reinterpret_cast<const ChunkRef*>(dev + s->layout.chunks);
+    a.units = reinterpret_cast<const Unit*>(dev + s->layout.units);
+    a.cta_begin = reinterpret_cast<const int32_t*>(dev + s->layout.cta_begin);
+    a.seq_perm = reinterpret_cast<const int32_t*>(dev + s->layout.seq_perm);
+    a.pbase = reinterpret_cast<const int32_t*>(dev + s->layout.pbase);
+    a.status = reinterpret_cast<int32_t*>(dev + s->layout.status);
+    a.q = static_cast<const uint16_t*>(q);
+    a.out = static_cast<uint16_t*>(out);
+    a.counters = reinterpret_cast<int32_t*>(ws + s->ws.counters);
+    a.part_o = reinterpret_cast<float*>(ws + s->ws.part_o);
+    a.part_ms = reinterpret_cast<float2*>(ws + s->ws.part_ms);
+    a.n_layers = pool->cfg.n_layers;
+    a.n_heads = pool->cfg.n_heads;
+    a.layer = layer;
+    a.capacity = pool->cfg.capacity_slots;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    return launch_attention(*pool, *s, a, stream);
+}
+
+int ca_decode_attention(const ca_pool* pool, const ca_sched* s, int32_t layer, const void* q_dev,
+                        void* out_dev, float scale, void* ws_dev, size_t ws_bytes, void* stream) {
+    int st = decode_checks(pool, s, layer, ws_dev, ws_bytes, s ? s->ws.total : 0);
+    if (st) return st;
+    if (!q_dev || !out_dev || !aligned(q_dev, 16) || !aligned(out_dev, 16)) return CA_ERR_INVALID;
+    return decode_launch(pool, s, layer, q_dev, out_dev, scale, ws_dev, stream);
+}
+
+int ca_decode_attention_host(const ca_pool* pool, const ca_sched* s, int32_t layer,
+                             const void* q_host, void* out_host, float scale, void* ws_dev,
+                             size_t ws_bytes, void* stream) {
+    int st = decode_checks(pool, s, layer, ws_dev, ws_bytes, s ? s->ws.total_host : 0);
+    if (st) return st;
+    if (!q_host || !out_host) return CA_ERR_INVALID;
+    const size_t bytes = (size_t)s->t.b * pool->cfg.n_heads * pool->cfg.head_dim * 2;
+    unsigned char* ws = static_cast<unsigned char*>(ws_dev);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(ws + s->ws.q_stage, q_host, bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+        return CA_ERR_CUDA;
+    st = decode_launch(pool, s, layer, ws + s->ws.q_stage, ws + s->ws.out_stage, scale, ws_dev, stream);
+    if (st) return st;
+    return cuda_status(cudaMemcpyAsync(out_host, ws + s->ws.out_stage, bytes, cudaMemcpyDeviceToHost, cs));
+}
+
+int ca_sched_device_status(const ca_sched* s, void* stream) {
+    if (!s || !s->dev) return CA_ERR_INVALID;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return CA_ERR_CUDA;
+    int32_t word = 0;
+    int32_t* dev_word = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(s->dev) + s->layout.status);
+    if (cudaMemcpy(&word, dev_word, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return CA_ERR_CUDA;
+    if (word != 0 && cudaMemset(dev_word, 0, sizeof(word)) != cudaSuccess) return CA_ERR_CUDA;
+    return word;
+}
+
+int ca_sched_set_profile_events(ca_sched* s, void* event_begin, void* event_end) {
+    if (!s) return CA_ERR_INVALID;
+    const bool on = event_begin && event_end;
+    s->ev_begin = on ? event_begin : nullptr;
+    s->ev_end = on ? event_end : nullptr;
+    return CA_OK;
+}
+
+const char* ca_error_string(int status) {
+    switch (status) {
+        case CA_OK: return "ok";
+        case CA_ERR_INVALID: return "invalid argument or state";
+        case CA_ERR_OOM: return "out of chunk slots or host memory";
+        case CA_ERR_NOT_FOUND: return "unknown sequence id";
+        case CA_ERR_EXISTS: return "sequence id already present";
+        case CA_ERR_STALE: return "schedule is older than the pool";
+        case CA_ERR_CUDA: return "CUDA call failed";
+        case CA_ERR_DEVICE_BOUNDS: return "kernel saw a table index out of range";
+        case CA_ERR_TIMEOUT: return "kernel wait timed out";
+        case CA_ERR_UNSUPPORTED: return "shape not supported";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,825 @@
+// Device code of libchunk_attention: the two-phase decode attention kernel
+// and the KV scatter used by inserts.  sm_103a (GB300).
+//
+// Method: ChunkAttention's two-phase partition ("ChunkAttention: Efficient
+// Self-Attention with Prefix-Aware KV Cache and Two-Phase Partition", §3.2).
+// A shared chunk is multiplied against the batched queries of every sequence
+// holding it (chunk-first, tensor cores); each sequence's own chunks are
+// processed per query (sequence-first, CUDA cores with warp-shuffle
+// reductions); every piece of work leaves a partial triple (o, m, s) that is
+// combined by the rescaled-sum rule of the explainer blog's "Two-Phase
+// Partition" section.
+//
+// GB300 design (not the paper's A100 kernel):
+//  * one persistent launch holds both phases: CTAs take a host-balanced list
+//    of chunk-first and sequence-first units, so the tensor-core work of the
+//    shared chunks overlaps the HBM stream of the private chunks on the same
+//    SMs (two CTAs per SM);
+//  * a producer warp streams every chunk-head tile (c x D fp16, contiguous in
+//    the pool) into a ring of shared-memory stages with 2-D TMA loads,
+//    128-byte swizzled, completing on mbarriers; four consumer warps compute;
+//  * partials are merged by whichever unit finishes last for a (sequence,
+//    head), found with one atomic arrival counter per pair (the GPU-atomics
+//    merge of the paper's §3.3), so the whole step is one kernel launch;
+//  * every wait is bounded (~1 s) and reports CA_ERR_TIMEOUT instead of
+//    hanging.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+
+#include "ca_internal.h"
+
+namespace ca {
+namespace dev {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kMaxStages = 8;
+constexpr int kQRows = 64;                 // queries per chunk-first unit, max
+constexpr unsigned kFull = 0xffffffffu;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait for an mbarrier phase; false after about a second (never hangs).
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t spin = 0; spin < (1u << 28); ++spin) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((spin & 63) == 63 && global_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return false;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void consumer_sync() {   // named barrier over the 4 consumer warps
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+__device__ __forceinline__ float ex2(float x) {      // 2^x, hardware approximation
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
+    atomicCAS(status, 0, code);
+}
+
+// Byte offset of 16-byte column chunk k of row r inside a tile stored as
+// D/64 boxes of `rows` x 128 B, each 128-byte swizzled (TMA SWIZZLE_128B:
+// chunk index XOR row mod 8).
+__device__ __forceinline__ uint32_t swz(int r, int k, int rows) {
+    return (uint32_t)((k >> 3) * rows * 128 + r * 128 + (((k & 7) ^ (r & 7)) << 4));
+}
+
+// ---------------------------------------------------------------------------
+// Merge of all partials of one (position, head): the explainer's output
+// combination, m* = max m_j, out = sum 2^{m_j-m*} o_j / sum 2^{m_j-m*} s_j
+// (m in log2 units).  One warp; lane owns D/32 dims.
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ void merge_final(const AttnParams& p, int pos, int h, int lane) {
+    constexpr int DPL = D / 32;
+    const int i = pos * p.n_heads + h;
+    const int a = p.pbase[i], z = p.pbase[i + 1];
+    float M = -INFINITY;
+    for (int j = a; j < z; ++j) M = fmaxf(M, __ldcg(&p.part_ms[j]).x);
+    float acc[DPL];
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
+    float S = 0.f;
+    for (int j = a; j < z; ++j) {
+        const float2 ms = __ldcg(&p.part_ms[j]);
+        const float w = (ms.x == -INFINITY) ? 0.f : ex2(ms.x - M);
+        S += w * ms.y;
+        const float* po = p.part_o + (size_t)j * D + lane * DPL;
+        if constexpr (DPL == 4) {
+            const float4 o = __ldcg(reinterpret_cast<const float4*>(po));
+            acc[0] += w * o.x; acc[1] += w * o.y; acc[2] += w * o.z; acc[3] += w * o.w;
+        } else {
+            const float2 o = __ldcg(reinterpret_cast<const float2*>(po));
+            acc[0] += w * o.x; acc[1] += w * o.y;
+        }
+    }
+    const float inv = 1.f / S;
+    uint16_t* dst = p.out + ((size_t)p.seq_perm[pos] * p.n_heads + h) * D + lane * DPL;
+    if constexpr (DPL == 4) {
+        uint2 v;
+        v.x = pack_half2(acc[0] * inv, acc[1] * inv);
+        v.y = pack_half2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(dst) = v;
+    } else {
+        *reinterpret_cast<uint32_t*>(dst) = pack_half2(acc[0] * inv, acc[1] * inv);
+    }
+}
+
+// Publish one partial and, if it was the last one of its (position, head),
+// produce the output.  Called by one lane per (position, head); the partial's
+// data must already be written and fenced by the writing lanes.
+__device__ __forceinline__ bool arrive_is_last(const AttnParams& p, int pos, int h) {
+    const int i = pos * p.n_heads + h;
+    const int need = p.pbase[i + 1] - p.pbase[i];
+    const int old = atomicAdd(&p.counters[i], 1);
+    if (old == need - 1) {
+        __threadfence();
+        p.counters[i] = 0;      // ready for the next call
+        return true;
+    }
+    return false;
+}
+
+// ---------------------------------------------------------------------------
+// Sequence-first: one chunk-head tile against one query, warp w taking
+// tokens [w*NT, (w+1)*NT) of the chunk.  Lane L owns dims [L*DPL, (L+1)*DPL).
+// Scores are reduce-scattered across the warp so that each lane ends with
+// the score of token (L >> (5 - log2 NT)); online softmax in log2 units.
+// ---------------------------------------------------------------------------
+template <int C, int D>
+__device__ __forceinline__ void sf_chunk(const uint8_t* kt, const uint8_t* vt, int ntok,
+                                         const float (&q)[D / 32], float& m, float& s,
+                                         float (&o)[D / 32], int w, int lane) {
+    constexpr int DPL = D / 32;
+    constexpr int NT = C / kConsumerWarps;
+    constexpr int LOGNT = NT == 16 ? 4 : NT == 8 ? 3 : 2;
+    constexpr int BPL = DPL * 2;                      // bytes per lane per row
+    const int kidx = (lane * BPL) >> 4, within = (lane * BPL) & 15;
+
+    float part[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const int r = w * NT + t;
+        const uint8_t* src = kt + swz(r, kidx, C) + within;
+        if constexpr (DPL == 4) {
+            const uint2 raw = *reinterpret_cast<const uint2*>(src);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+            part[t] = q[0] * a.x + q[1] * a.y + q[2] * b.x + q[3] * b.y;
+        } else {
+            const uint32_t raw = *reinterpret_cast<const uint32_t*>(src);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw));
+            part[t] = q[0] * a.x + q[1] * a.y;
+        }
+    }
+    // Reduce-scatter: after log2(NT) halving stages lane L holds the sum of
+    // token (L >> (5-LOGNT)) over the lanes differing in its top bits; the
+    // remaining stages sum over the low bits.
+#pragma unroll
+    for (int n = NT, off = 16; n > 1; n >>= 1, off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float keep = upper ? part[i + n / 2] : part[i];
+            const float send = upper ? part[i] : part[i + n / 2];
+            part[i] = keep + __shfl_xor_sync(kFull, send, off);
+        }
+    }
+#pragma unroll
+    for (int off = 16 >> LOGNT; off >= 1; off >>= 1) part[0] += __shfl_xor_sync(kFull, part[0], off);
+
+    const int j = lane >> (5 - LOGNT);
+    float x = (w * NT + j < ntok) ? part[0] : -INFINITY;
+    float mx = x;
+#pragma unroll
+    for (int off = 16; off >= (32 >> LOGNT); off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+    const float mnew = fmaxf(m, mx);
+    const float mu = (mnew == -INFINITY) ? 0.f : mnew;
+    const float alpha = ex2(m - mu);
+    const float pj = ex2(x - mu);
+    float ps = pj;
+#pragma unroll
+    for (int off = 16; off >= (32 >> LOGNT); off >>= 1) ps += __shfl_xor_sync(kFull, ps, off);
+    s = s * alpha + ps;
+    m = mnew;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) o[d] *= alpha;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const float pt = __shfl_sync(kFull, pj, t << (5 - LOGNT));
+        const uint8_t* src = vt + swz(w * NT + t, kidx, C) + within;
+        if constexpr (DPL == 4) {
+            const uint2 raw = *reinterpret_cast<const uint2*>(src);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+            o[0] += pt * a.x; o[1] += pt * a.y; o[2] += pt * b.x; o[3] += pt * b.y;
+        } else {
+            const uint32_t raw = *reinterpret_cast<const uint32_t*>(src);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw));
+            o[0] += pt * a.x; o[1] += pt * a.y;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Chunk-first: one chunk-head tile against up to 16 batched queries (one m16
+// row block) with mma.sync m16n8k16 (fp16 in, fp32 accumulate).  The warp
+// takes tokens [tok0, tok0 + NT) of the chunk.  Row state per thread: rows
+// g = lane/4 and g + 8 of the block.
+// ---------------------------------------------------------------------------
+template <int C, int D, int NT>
+__device__ __forceinline__ void cf_chunk(uint32_t kt, uint32_t vt, int ntok, int tok0,
+                                         const uint32_t (&qa)[D / 16][4], float scale_log2,
+                                         float (&m)[2], float (&s)[2], float (&o)[D / 8][4],
+                                         int lane) {
+    float sacc[NT / 8][4];
+#pragma unroll
+    for (int i = 0; i < NT / 8; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
+    // S = Q K^T over the D dims, 16 at a time.
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+        for (int np = 0; np < NT / 16; ++np) {
+            const int tok = tok0 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
+            const int kc = 2 * kk + ((lane >> 3) & 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kt + swz(tok, kc, C), b0, b1, b2, b3);
+            mma16816(sacc[2 * np], qa[kk], b0, b1);
+            mma16816(sacc[2 * np + 1], qa[kk], b2, b3);
+        }
+    }
+    // Online softmax per row (log2 units); columns past ntok are masked.
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < NT / 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int col = tok0 + nt * 8 + 2 * (lane & 3) + (e & 1);
+            const float x = (col < ntok) ? sacc[nt][e] * scale_log2 : -INFINITY;
+            sacc[nt][e] = x;
+            mx[e >> 1] = fmaxf(mx[e >> 1], x);
+        }
+    }
+    float alpha[2], mu[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], 2));
+        const float mnew = fmaxf(m[r], mx[r]);
+        mu[r] = (mnew == -INFINITY) ? 0.f : mnew;
+        alpha[r] = ex2(m[r] - mu[r]);
+        m[r] = mnew;
+        s[r] *= alpha[r];
+    }
+    uint32_t pa[NT / 16][4];
+#pragma unroll
+    for (int nt = 0; nt < NT / 8; ++nt) {
+        const float p0 = ex2(sacc[nt][0] - mu[0]), p1 = ex2(sacc[nt][1] - mu[0]);
+        const float p2 = ex2(sacc[nt][2] - mu[1]), p3 = ex2(sacc[nt][3] - mu[1]);
+        s[0] += p0 + p1;
+        s[1] += p2 + p3;
+        // accumulator layout of n-tile nt == A-operand layout of k-step nt/2
+        pa[nt >> 1][(nt & 1) * 2 + 0] = pack_half2(p0, p1);
+        pa[nt >> 1][(nt & 1) * 2 + 1] = pack_half2(p2, p3);
+    }
+#pragma unroll
+    for (int dt = 0; dt < D / 8; ++dt) {
+        o[dt][0] *= alpha[0]; o[dt][1] *= alpha[0];
+        o[dt][2] *= alpha[1]; o[dt][3] *= alpha[1];
+    }
+    // O += P V over this warp's NT tokens.
+#pragma unroll
+    for (int j = 0; j < NT / 16; ++j) {
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+            const int tok = tok0 + 16 * j + (lane & 7) + (((lane >> 3) & 1) << 3);
+            const int kc = 2 * dp + (lane >> 4);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vt + swz(tok, kc, C), b0, b1, b2, b3);
+            mma16816(o[2 * dp], pa[j], b0, b1);
+            mma16816(o[2 * dp + 1], pa[j], b2, b3);
+        }
+    }
+}
+
+// Shared-memory map of one CTA.
+template <int C, int D>
+struct Smem {
+    static constexpr int kTile = C * D * 2;     // one K or V tile of one chunk-head
+    static constexpr int kStage = 2 * kTile;    // K then V
+    static constexpr int kQBytes = kQRows * D * 2;
+    static constexpr int kXmsBytes = 512;
+    static constexpr int kBarBytes = 2 * kMaxStages * 8;
+    static size_t bytes(int stages) { return (size_t)stages * kStage + kQBytes + kXmsBytes + kBarBytes; }
+};
+
+// ---------------------------------------------------------------------------
+// The persistent two-phase kernel.
+// ---------------------------------------------------------------------------
+template <int C, int D>
+__global__ void __launch_bounds__(kThreads, 2)
+two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnParams p) {
+    using SM = Smem<C, D>;
+    constexpr int DPL = D / 32;
+    constexpr int BOXES = D / 64;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int S = p.n_stages;
+    uint8_t* stages = smem;
+    uint8_t* qreg = smem + (size_t)S * SM::kStage;
+    float* xms = reinterpret_cast<float*>(qreg + SM::kQBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xms) + SM::kXmsBytes);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if ((smem_u32(smem) & 1023u) != 0 || S < 1 || S > kMaxStages) {   // uniform across the CTA
+        if (threadIdx.x == 0) set_status(p.status, CA_ERR_INVALID);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(full0 + 8 * i, 1);
+            mbar_init(empty0 + 8 * i, kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+
+    const int u_begin = p.cta_begin[blockIdx.x], u_end = p.cta_begin[blockIdx.x + 1];
+    const int H = p.n_heads;
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------ producer ------------------------------
+        if (lane != 0) return;
+        const uint64_t pol = policy_evict_first();
+        int it = 0;
+        bool ok = true;
+        for (int u = u_begin; u < u_end && ok; ++u) {
+            const Unit U = p.units[u];
+            for (int c = U.c_begin; c < U.c_end; ++c, ++it) {
+                const int st = it % S;
+                const uint32_t ph = (uint32_t)(it / S) & 1u;
+                if (!mbar_wait(empty0 + 8 * st, ph ^ 1u)) {
+                    set_status(p.status, CA_ERR_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                const ChunkRef ch = p.chunks[c];
+                const uint32_t fb = full0 + 8 * st;
+                if (ch.slot < 0 || ch.slot >= p.capacity || U.head < 0 || U.head >= H) {
+                    set_status(p.status, CA_ERR_DEVICE_BOUNDS);
+                    mbar_arrive(fb);          // release the consumers without data
+                    continue;
+                }
+                mbar_expect_tx(fb, SM::kStage);
+                const uint32_t dst = smem_u32(stages + (size_t)st * SM::kStage);
+                const int rowK = (((ch.slot * p.n_layers + p.layer) * 2 + 0) * H + U.head) * C;
+                const int rowV = rowK + H * C;
+#pragma unroll
+                for (int bx = 0; bx < BOXES; ++bx) {
+                    tma_load_2d(dst + bx * C * 128, &tmap, bx * 64, rowK, fb, pol);
+                    tma_load_2d(dst + SM::kTile + bx * C * 128, &tmap, bx * 64, rowV, fb, pol);
+                }
+            }
+        }
+        if (!ok) {
+            // Give the copies already issued a bounded chance to land before
+            // the CTA can exit.
+            for (int k = (it > S ? it - S : 0); k < it; ++k)
+                mbar_wait(full0 + 8 * (k % S), (uint32_t)(k / S) & 1u);
+        }
+        return;
+    }
+
+    // ------------------------------ consumers --------------------------------
+    const int w = warp;
+    int it = 0;
+    for (int u = u_begin; u < u_end; ++u) {
+        const Unit U = p.units[u];
+        const int h = U.head;
+        consumer_sync();   // previous unit (and its exchange reads) finished
+        if (U.kind == UNIT_SF) {
+            const int pos = U.q_lo;
+            float q[DPL], o[DPL], m = -INFINITY, s = 0.f;
+            {
+                const uint16_t* qp = p.q + ((size_t)p.seq_perm[pos] * H + h) * D + lane * DPL;
+                if constexpr (DPL == 4) {
+                    const uint2 raw = *reinterpret_cast<const uint2*>(qp);
+                    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+                    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+                    q[0] = a.x; q[1] = a.y; q[2] = b.x; q[3] = b.y;
+                } else {
+                    const uint32_t raw = *reinterpret_cast<const uint32_t*>(qp);
+                    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw));
+                    q[0] = a.x; q[1] = a.y;
+                }
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) { q[d] *= p.scale_log2; o[d] = 0.f; }
+            }
+            for (int c = U.c_begin; c < U.c_end; ++c, ++it) {
+                const int st = it % S;
+                if (!mbar_wait(full0 + 8 * st, (uint32_t)(it / S) & 1u)) {
+                    set_status(p.status, CA_ERR_TIMEOUT);
+                    return;
+                }
+                const int ntok = min(max(p.chunks[c].ntok, 0), C);
+                const uint8_t* kt = stages + (size_t)st * SM::kStage;
+                sf_chunk<C, D>(kt, kt + SM::kTile, ntok, q, m, s, o, w, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8 * st);
+            }
+            // Combine the four warps' states, write the partial.
+            float* xo = reinterpret_cast<float*>(qreg);          // [4][D]
+            xo[w * D + lane * DPL + 0] = o[0];
+            xo[w * D + lane * DPL + 1] = o[1];
+            if constexpr (DPL == 4) {
+                xo[w * D + lane * DPL + 2] = o[2];
+                xo[w * D + lane * DPL + 3] = o[3];
+            }
+            if (lane == 0) { xms[2 * w] = m; xms[2 * w + 1] = s; }
+            consumer_sync();
+            if (w == 0) {
+                float M = -INFINITY;
+#pragma unroll
+                for (int v = 0; v < kConsumerWarps; ++v) M = fmaxf(M, xms[2 * v]);
+                float acc[DPL], sum = 0.f;
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
+#pragma unroll
+                for (int v = 0; v < kConsumerWarps; ++v) {
+                    const float mv = xms[2 * v];
+                    const float wt = (mv == -INFINITY) ? 0.f : ex2(mv - M);
+                    sum += wt * xms[2 * v + 1];
+#pragma unroll
+                    for (int d = 0; d < DPL; ++d) acc[d] += wt * xo[v * D + lane * DPL + d];
+                }
+                const int pid = p.pbase[pos * H + h] + U.part;
+                float* dst = p.part_o + (size_t)pid * D + lane * DPL;
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) dst[d] = acc[d];
+                if (lane == 0) p.part_ms[pid] = make_float2(M, sum);
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) last = arrive_is_last(p, pos, h);
+                last = __shfl_sync(kFull, last, 0);
+                if (last) merge_final<D>(p, pos, h, lane);
+            }
+        } else {
+            // ---------------------------- chunk-first ----------------------------
+            const int m_rows = U.q_hi - U.q_lo;
+            const int rblocks = m_rows <= 16 ? 1 : m_rows <= 32 ? 2 : 4;
+            int T = kConsumerWarps / rblocks;            // warps splitting the tokens
+            if (T * 16 > C) T = C / 16;
+            const int rb = w / T, tp = w % T;
+            const bool active = rb < rblocks && rb * 16 < m_rows;
+            // Load the unit's queries [q_lo, q_hi) of head h into the swizzled
+            // Q tile; rows past m_rows are zero.
+            for (int idx = threadIdx.x; idx < kQRows * (D / 8); idx += kConsumerWarps * 32) {
+                const int r = idx / (D / 8), k = idx % (D / 8);
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (r < m_rows)
+                    v = *reinterpret_cast<const uint4*>(
+                        p.q + ((size_t)p.seq_perm[U.q_lo + r] * H + h) * D + k * 8);
+                *reinterpret_cast<uint4*>(qreg + swz(r, k, kQRows)) = v;
+            }
+            consumer_sync();
+            uint32_t qa[D / 16][4];
+            float o[D / 8][4], m[2] = {-INFINITY, -INFINITY}, s[2] = {0.f, 0.f};
+#pragma unroll
+            for (int dt = 0; dt < D / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+            if (active) {
+                const uint32_t qbase = smem_u32(qreg);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ldsm_x4(qbase + swz(rb * 16 + (lane & 15), 2 * kk + (lane >> 4), kQRows),
+                            qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+            }
+            const int NTw = C / T;
+            for (int c = U.c_begin; c < U.c_end; ++c, ++it) {
+                const int st = it % S;
+                if (!mbar_wait(full0 + 8 * st, (uint32_t)(it / S) & 1u)) {
+                    set_status(p.status, CA_ERR_TIMEOUT);
+                    return;
+                }
+                if (active) {
+                    const int ntok = min(max(p.chunks[c].ntok, 0), C);
+                    const uint32_t kt = smem_u32(stages + (size_t)st * SM::kStage);
+                    const uint32_t vt = kt + SM::kTile;
+                    if (NTw == 16) {
+                        cf_chunk<C, D, 16>(kt, vt, ntok, tp * 16, qa, p.scale_log2, m, s, o, lane);
+                    } else if constexpr (C >= 32) {
+                        // 32 tokens at a time keeps the score tile in registers
+                        for (int t0 = tp * NTw; t0 < (tp + 1) * NTw; t0 += 32)
+                            cf_chunk<C, D, 32>(kt, vt, ntok, t0, qa, p.scale_log2, m, s, o, lane);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8 * st);
+            }
+            // Row sums are per thread so far: reduce over the quad.
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                s[r] += __shfl_xor_sync(kFull, s[r], 1);
+                s[r] += __shfl_xor_sync(kFull, s[r], 2);
+            }
+            // Tree-combine the T warps that split the tokens of one row block,
+            // through the (now free) Q tile: round `half` moves warps with
+            // tp in [half, 2*half) onto tp - half.
+            float* xo = reinterpret_cast<float*>(qreg);
+            for (int half = T / 2; half >= 1; half /= 2) {
+                consumer_sync();
+                const bool writer = active && tp >= half && tp < 2 * half;
+                const int slot = rb * (T / 2) + (tp - half);    // < 2 writers per round
+                if (writer) {
+                    float* dst = xo + (size_t)slot * (16 * D);
+#pragma unroll
+                    for (int dt = 0; dt < D / 8; ++dt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) dst[(dt * 4 + e) * 32 + lane] = o[dt][e];
+                    if ((lane & 3) == 0) {
+                        const int g = lane >> 2;
+                        xms[slot * 64 + g * 4 + 0] = m[0];
+                        xms[slot * 64 + g * 4 + 1] = s[0];
+                        xms[slot * 64 + g * 4 + 2] = m[1];
+                        xms[slot * 64 + g * 4 + 3] = s[1];
+                    }
+                }
+                consumer_sync();
+                if (active && tp < half) {
+                    const int src = rb * (T / 2) + tp;
+                    const float* so = xo + (size_t)src * (16 * D);
+                    const int g = lane >> 2;
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const float m2 = xms[src * 64 + g * 4 + 2 * r];
+                        const float s2 = xms[src * 64 + g * 4 + 2 * r + 1];
+                        const float M = fmaxf(m[r], m2);
+                        const float Mu = (M == -INFINITY) ? 0.f : M;
+                        const float a1 = ex2(m[r] - Mu), a2 = ex2(m2 - Mu);
+                        s[r] = s[r] * a1 + s2 * a2;
+                        m[r] = M;
+#pragma unroll
+                        for (int dt = 0; dt < D / 8; ++dt) {
+                            o[dt][2 * r] = o[dt][2 * r] * a1 + so[(dt * 4 + 2 * r) * 32 + lane] * a2;
+                            o[dt][2 * r + 1] =
+                                o[dt][2 * r + 1] * a1 + so[(dt * 4 + 2 * r + 1) * 32 + lane] * a2;
+                        }
+                    }
+                }
+            }
+            // Warps with tp == 0 now hold their row block: write one partial
+            // per valid row, then count arrivals and merge where last.
+            if (active && tp == 0) {
+                const int g = lane >> 2, t4 = lane & 3;
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int row = rb * 16 + g + 8 * r;
+                    if (row < m_rows) {
+                        const int pos = U.q_lo + row;
+                        const int pid = p.pbase[pos * H + h] + U.part;
+                        float* dst = p.part_o + (size_t)pid * D;
+#pragma unroll
+                        for (int dt = 0; dt < D / 8; ++dt)
+                            *reinterpret_cast<float2*>(dst + dt * 8 + 2 * t4) =
+                                make_float2(o[dt][2 * r], o[dt][2 * r + 1]);
+                        if (t4 == 0) p.part_ms[pid] = make_float2(m[r], s[r]);
+                    }
+                }
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                const int row = rb * 16 + lane;
+                if (lane < 16 && row < m_rows) last = arrive_is_last(p, U.q_lo + row, h);
+                unsigned todo = __ballot_sync(kFull, last);
+                while (todo) {
+                    const int l = __ffs(todo) - 1;
+                    todo &= todo - 1;
+                    merge_final<D>(p, U.q_lo + rb * 16 + l, h, lane);
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// KV scatter for inserts: rows [first, n) of k/v [L][n][H][D] into the pool
+// chunk slots listed per chunk.  16-byte vectors, grid-stride.
+// ---------------------------------------------------------------------------
+constexpr int kScatterMaxChunks = 1024;
+struct ScatterArgs {
+    const uint4* k;
+    const uint4* v;
+    uint4* pool;
+    int32_t n, first_tok, n_tok, chunk, n_layers, n_heads, vec_per_row, first_chunk;
+    int32_t slots[kScatterMaxChunks];
+};
+
+__global__ void kv_scatter_kernel(const __grid_constant__ ScatterArgs a) {
+    const long long total = (long long)a.n_layers * a.n_tok * a.n_heads * a.vec_per_row;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int vec = (int)(i % a.vec_per_row);
+        long long r = i / a.vec_per_row;
+        const int h = (int)(r % a.n_heads);
+        r /= a.n_heads;
+        const int t = a.first_tok + (int)(r % a.n_tok);
+        const int l = (int)(r / a.n_tok);
+        const int slot = a.slots[t / a.chunk - a.first_chunk];
+        const long long src = (((long long)l * a.n + t) * a.n_heads + h) * a.vec_per_row + vec;
+        const long long tile =
+            (((long long)slot * a.n_layers + l) * 2 * a.n_heads + h) * a.chunk + (t % a.chunk);
+        const long long dk = tile * a.vec_per_row + vec;
+        const long long dv = dk + (long long)a.n_heads * a.chunk * a.vec_per_row;
+        a.pool[dk] = a.k[src];
+        a.pool[dv] = a.v[src];
+    }
+}
+
+}  // namespace dev
+
+// ---------------------------------------------------------------------------
+// Host launchers.
+// ---------------------------------------------------------------------------
+namespace {
+template <int C, int D>
+void* kernel_ptr() {
+    return reinterpret_cast<void*>(&dev::two_phase_attention_kernel<C, D>);
+}
+void* pick_kernel(int chunk, int head_dim) {
+    if (head_dim == 128) {
+        if (chunk == 64) return kernel_ptr<64, 128>();
+        if (chunk == 32) return kernel_ptr<32, 128>();
+        if (chunk == 16) return kernel_ptr<16, 128>();
+    } else if (head_dim == 64) {
+        if (chunk == 64) return kernel_ptr<64, 64>();
+        if (chunk == 32) return kernel_ptr<32, 64>();
+        if (chunk == 16) return kernel_ptr<16, 64>();
+    }
+    return nullptr;
+}
+size_t smem_for(int chunk, int head_dim, int stages) {
+    const size_t stage = (size_t)2 * chunk * head_dim * 2;
+    return (size_t)stages * stage + (size_t)dev::kQRows * head_dim * 2 + 512 + 2 * dev::kMaxStages * 8;
+}
+}  // namespace
+
+// Stages that fit two CTAs per SM (113 KiB each, at most 8).
+int kernel_smem_bytes(int chunk, int head_dim, int* n_stages, size_t* bytes) {
+    if (!pick_kernel(chunk, head_dim)) return CA_ERR_UNSUPPORTED;
+    const size_t budget = 113 * 1024;
+    int st = dev::kMaxStages;
+    while (st > 1 && smem_for(chunk, head_dim, st) > budget) --st;
+    *n_stages = st;
+    *bytes = smem_for(chunk, head_dim, st);
+    return CA_OK;
+}
+
+int kernel_ctas_per_sm(int chunk, int head_dim, int* ctas) {
+    void* fn = pick_kernel(chunk, head_dim);
+    if (!fn) return CA_ERR_UNSUPPORTED;
+    int st;
+    size_t bytes;
+    kernel_smem_bytes(chunk, head_dim, &st, &bytes);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+        return CA_ERR_CUDA;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, dev::kThreads, bytes) != cudaSuccess)
+        return CA_ERR_CUDA;
+    *ctas = n < 1 ? 1 : n;
+    return CA_OK;
+}
+
+int make_tensor_map(Pool& p) {
+    using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+        return CA_ERR_CUDA;
+    const ca_pool_config& c = p.cfg;
+    // The pool as a 2-D tensor: rows of head_dim fp16, one row per
+    // (slot, layer, K|V, head, token-in-chunk).
+    const cuuint64_t rows = (cuuint64_t)c.capacity_slots * c.n_layers * 2 * c.n_heads * c.chunk;
+    const cuuint64_t dims[2] = {(cuuint64_t)c.head_dim, rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)c.chunk};
+    const cuuint32_t estr[2] = {1, 1};
+    CUtensorMap* map = reinterpret_cast<CUtensorMap*>(p.tmap);
+    CUresult r = reinterpret_cast<EncodeFn>(fn)(
+        map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.kv, dims, strides, box, estr,
+        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? CA_OK : CA_ERR_CUDA;
+}
+
+int launch_scatter(const Pool& p, const void* k, const void* v, int32_t n,
+                   const std::vector<std::pair<int32_t, int32_t>>& new_chunks, void* stream) {
+    if (new_chunks.empty()) return CA_OK;
+    const ca_pool_config& c = p.cfg;
+    size_t i = 0;
+    while (i < new_chunks.size()) {
+        const size_t cnt = std::min<size_t>(dev::kScatterMaxChunks, new_chunks.size() - i);
+        dev::ScatterArgs a;
+        std::memset(&a, 0, sizeof(a));
+        a.k = static_cast<const uint4*>(k);
+        a.v = static_cast<const uint4*>(v);
+        a.pool = static_cast<uint4*>(p.kv);
+        a.n = n;
+        a.chunk = c.chunk;
+        a.n_layers = c.n_layers;
+        a.n_heads = c.n_heads;
+        a.vec_per_row = c.head_dim / 8;
+        a.first_tok = new_chunks[i].first;
+        const int32_t end_tok = (i + cnt < new_chunks.size()) ? new_chunks[i + cnt].first : n;
+        a.n_tok = end_tok - a.first_tok;
+        a.first_chunk = new_chunks[i].first / c.chunk;
+        for (size_t j = 0; j < cnt; ++j) a.slots[j] = new_chunks[i + j].second;
+        const long long total = (long long)c.n_layers * a.n_tok * c.n_heads * a.vec_per_row;
+        long long blocks = (total + 255) / 256;
+        if (blocks > 4096) blocks = 4096;
+        dev::kv_scatter_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+        if (cudaGetLastError() != cudaSuccess) return CA_ERR_CUDA;
+        i += cnt;
+    }
+    return CA_OK;
+}
+
+int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void* stream) {
+    void* fn = pick_kernel(p.cfg.chunk, p.cfg.head_dim);
+    if (!fn) return CA_ERR_UNSUPPORTED;
+    int st;
+    size_t bytes;
+    kernel_smem_bytes(p.cfg.chunk, p.cfg.head_dim, &st, &bytes);   // attribute set at pool creation
+    AttnParams a = prm;
+    a.n_stages = st;
+    const CUtensorMap* map = reinterpret_cast<const CUtensorMap*>(p.tmap);
+    void* args[] = {const_cast<CUtensorMap*>(map), &a};
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (s.ev_begin) cudaEventRecord(static_cast<cudaEvent_t>(s.ev_begin), cs);
+    cudaError_t e = cudaLaunchKernel(fn, dim3(s.plan.grid), dim3(dev::kThreads), args, bytes, cs);
+    if (s.ev_end) cudaEventRecord(static_cast<cudaEvent_t>(s.ev_end), cs);
+    return e == cudaSuccess ? CA_OK : CA_ERR_CUDA;
+}
+
+}  // namespace ca

@@ -1,0 +1,314 @@
+// Per-step context of the two-phase partition ("ChunkAttention: Efficient
+// Self-Attention with Prefix-Aware KV Cache and Two-Phase Partition", §3.2
+// and §3.3) and the kernel work plan derived from it.
+//
+// Tables (the exact, testable part):
+//  * depth-first batch order: children in insertion order; at a node, the
+//    sequences ending there first (ascending seq_id), then its children — so
+//    every chunk's sharers are one contiguous range [lo, hi) of positions;
+//  * cf_rows: chunks held by >= 2 batch sequences, pre-order, with [lo, hi);
+//  * cf_runs: maximal parent->child stretches of rows with the same range;
+//  * sf lists: each position's chunks held by that sequence alone;
+//  * merge lists: the runs covering each position.
+//
+// Plan (GB300-specific, verified through the outputs): chunk-first runs are
+// cut into units of at most 64 queries and a balanced number of chunks;
+// sequence-first chunk-heads are spread over the CTAs in contiguous pieces so
+// that every CTA gets the same estimated time.
+#include <algorithm>
+#include <cstring>
+#include <numeric>
+#include <queue>
+#include <unordered_set>
+
+#include "ca_internal.h"
+
+namespace ca {
+
+int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flags, Tables& t) {
+    if (b < 1 || !seq_ids) return CA_ERR_INVALID;
+    {
+        std::unordered_set<int64_t> seen;
+        for (int32_t i = 0; i < b; ++i) {
+            if (!p.seqs.count(seq_ids[i])) return CA_ERR_NOT_FOUND;
+            if (!seen.insert(seq_ids[i]).second) return CA_ERR_INVALID;
+        }
+    }
+    const bool tpp = !(flags & CA_SCHED_NO_TPP);
+    // Batch holders per node (Node::mark) and sequences ending at each node.
+    std::unordered_map<const Node*, std::vector<int64_t>> ending;
+    for (int32_t i = 0; i < b; ++i) {
+        const Sequence& s = p.seqs.at(seq_ids[i]);
+        for (Node* n : s.path) n->mark += 1;
+        ending[s.path.back()].push_back(seq_ids[i]);
+    }
+    for (auto& kv : ending) std::sort(kv.second.begin(), kv.second.end());
+
+    std::vector<int64_t> order;
+    order.reserve(b);
+    t = Tables();
+    t.b = b;
+    std::vector<const Node*> row_node;
+    struct Frame { const Node* node; size_t next; };
+    std::vector<Frame> stack;
+    stack.push_back({p.root.get(), 0});
+    while (!stack.empty()) {
+        Frame& f = stack.back();
+        const Node* node = f.node;
+        if (f.next == 0 && node != p.root.get()) {
+            if (tpp && node->mark >= 2) {
+                const_cast<Node*>(node)->row = (int32_t)row_node.size();
+                row_node.push_back(node);
+                t.cf_rows.insert(t.cf_rows.end(),
+                                 {node->slot, (int32_t)node->tokens.size(), (int32_t)order.size(), -1});
+            }
+            auto e = ending.find(node);
+            if (e != ending.end()) order.insert(order.end(), e->second.begin(), e->second.end());
+        }
+        size_t ci = f.next;
+        while (ci < node->children.size() && node->children[ci]->mark == 0) ++ci;
+        if (ci < node->children.size()) {
+            f.next = ci + 1;
+            stack.push_back({node->children[ci], 0});
+        } else {
+            if (node->row >= 0) t.cf_rows[4 * node->row + 3] = (int32_t)order.size();
+            stack.pop_back();
+        }
+    }
+
+    // seq_perm: DFS position -> caller row.
+    std::unordered_map<int64_t, int32_t> caller;
+    caller.reserve(b);
+    for (int32_t i = 0; i < b; ++i) caller[seq_ids[i]] = i;
+    t.seq_perm.resize(b);
+    for (int32_t pos = 0; pos < b; ++pos) t.seq_perm[pos] = caller[order[pos]];
+
+    // Runs.
+    const int32_t R = (int32_t)row_node.size();
+    for (int32_t r = 0; r < R; ++r) {
+        const int32_t lo = t.cf_rows[4 * r + 2], hi = t.cf_rows[4 * r + 3];
+        const size_t U = t.cf_runs.size() / 4;
+        if (U > 0 && row_node[r]->parent == row_node[r - 1] && t.cf_rows[4 * (r - 1) + 2] == lo &&
+            t.cf_rows[4 * (r - 1) + 3] == hi) {
+            t.cf_runs[4 * (U - 1) + 1] += 1;
+        } else {
+            t.cf_runs.insert(t.cf_runs.end(), {r, 1, lo, hi});
+        }
+    }
+
+    // Sequence-first lists.
+    t.sf_offsets.assign(1, 0);
+    for (int32_t pos = 0; pos < b; ++pos) {
+        for (const Node* n : p.seqs.at(order[pos]).path)
+            if (!tpp || n->mark == 1) t.sf_chunks.insert(t.sf_chunks.end(), {n->slot, (int32_t)n->tokens.size()});
+        t.sf_offsets.push_back((int32_t)(t.sf_chunks.size() / 2));
+    }
+
+    // Merge lists: runs are nested intervals listed in pre-order, so a
+    // position's covering runs come out in root-to-leaf order.
+    t.merge_offsets.assign(1, 0);
+    const int32_t U = (int32_t)(t.cf_runs.size() / 4);
+    for (int32_t pos = 0; pos < b; ++pos) {
+        for (int32_t u = 0; u < U; ++u)
+            if (t.cf_runs[4 * u + 2] <= pos && pos < t.cf_runs[4 * u + 3]) t.merge_runs.push_back(u);
+        t.merge_offsets.push_back((int32_t)t.merge_runs.size());
+    }
+
+    for (int32_t i = 0; i < b; ++i)
+        for (Node* n : p.seqs.at(seq_ids[i]).path) { n->mark = 0; n->row = -1; }
+    return CA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Work plan.
+// Cost model, in "chunk-head tiles" (one chunk of one head, K and V): a
+// sequence-first tile costs 1 (HBM-bound); a chunk-first tile for m queries
+// costs 1 + kCfComputePer16 * ceil(m / 16) (tensor-core work grows with m).
+// ---------------------------------------------------------------------------
+namespace {
+constexpr double kCfComputePer16 = 0.25;
+constexpr int32_t kMaxCfQueries = 64;
+}  // namespace
+
+void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
+    const int32_t H = p.cfg.n_heads, D = p.cfg.head_dim, c = p.cfg.chunk, b = t.b;
+    const int32_t R = (int32_t)(t.cf_rows.size() / 4), U = (int32_t)(t.cf_runs.size() / 4);
+    plan = Plan();
+
+    // Chunk list: chunk-first rows first (index = row), then sf chunks.
+    plan.chunks.resize(R + t.sf_chunks.size() / 2);
+    for (int32_t r = 0; r < R; ++r) plan.chunks[r] = {t.cf_rows[4 * r], t.cf_rows[4 * r + 1]};
+    for (size_t i = 0; i < t.sf_chunks.size() / 2; ++i)
+        plan.chunks[R + i] = {t.sf_chunks[2 * i], t.sf_chunks[2 * i + 1]};
+
+    // Totals for the per-CTA budget.
+    double sf_total = (double)(t.sf_chunks.size() / 2) * H;
+    double cf_total = 0;
+    for (int32_t u = 0; u < U; ++u) {
+        const int32_t nrows = t.cf_runs[4 * u + 1], m = t.cf_runs[4 * u + 3] - t.cf_runs[4 * u + 2];
+        cf_total += (double)nrows * H * (1.0 + kCfComputePer16 * ((m + 15) / 16));
+    }
+    const int32_t tiles_ceiling = (int32_t)std::max(1.0, sf_total + cf_total);
+    grid = std::max(1, std::min(grid, tiles_ceiling));
+    plan.grid = grid;
+    const double avg = (sf_total + cf_total) / grid;
+
+    // Chunk-first units: pieces per run.
+    std::vector<int32_t> pieces(U, 0);
+    struct CfUnit { Unit u; double cost; };
+    std::vector<CfUnit> cf;
+    for (int32_t u = 0; u < U; ++u) {
+        const int32_t row0 = t.cf_runs[4 * u], nrows = t.cf_runs[4 * u + 1];
+        const int32_t lo = t.cf_runs[4 * u + 2], hi = t.cf_runs[4 * u + 3], m = hi - lo;
+        const int32_t ngroups = (m + kMaxCfQueries - 1) / kMaxCfQueries;
+        const int32_t mg = (m + ngroups - 1) / ngroups;
+        const double row_cost = 1.0 + kCfComputePer16 * ((mg + 15) / 16);
+        // Enough rows per piece that partial traffic (2 x mg x (D+2) floats)
+        // stays under 1/8 of the piece's KV bytes; few enough that one piece
+        // does not outweigh a CTA's share.
+        const int32_t rmin = std::max(1, (int32_t)((16.0 * mg * (D + 2)) / ((double)c * D) + 0.999));
+        const int32_t rpar = std::max(1, (int32_t)(avg / row_cost));
+        const int32_t per = std::max(rmin, rpar);
+        const int32_t np = std::max(1, (nrows + per - 1) / per);
+        pieces[u] = np;
+        for (int32_t g = 0; g < ngroups; ++g) {
+            const int32_t qa = lo + (int32_t)((int64_t)m * g / ngroups);
+            const int32_t qb = lo + (int32_t)((int64_t)m * (g + 1) / ngroups);
+            for (int32_t k = 0; k < np; ++k) {
+                const int32_t ra = row0 + (int32_t)((int64_t)nrows * k / np);
+                const int32_t rb = row0 + (int32_t)((int64_t)nrows * (k + 1) / np);
+                for (int32_t h = 0; h < H; ++h) {
+                    Unit x{UNIT_CF, h, qa, qb, ra, rb, k, 0};
+                    cf.push_back({x, (rb - ra) * (1.0 + kCfComputePer16 * ((qb - qa + 15) / 16))});
+                }
+            }
+        }
+    }
+    // Partial index base of a run for its positions: the pieces of the runs
+    // before it on the same path (its ancestors), which are exactly the runs
+    // preceding it in any covered position's merge list.
+    std::vector<int32_t> run_base(U, 0);
+    std::vector<int32_t> nk1(b, 0);
+    for (int32_t pos = 0; pos < b; ++pos) {
+        int32_t acc = 0;
+        for (int32_t k = t.merge_offsets[pos]; k < t.merge_offsets[pos + 1]; ++k) {
+            const int32_t u = t.merge_runs[k];
+            run_base[u] = acc;       // identical for every position the run covers
+            acc += pieces[u];
+        }
+        nk1[pos] = acc;
+    }
+    // The base depends on the unit's run: recover it from the row range.
+    {
+        std::vector<int32_t> run_of_row(R);
+        for (int32_t u = 0; u < U; ++u)
+            for (int32_t r = t.cf_runs[4 * u]; r < t.cf_runs[4 * u] + t.cf_runs[4 * u + 1]; ++r)
+                run_of_row[r] = u;
+        for (auto& x : cf) x.u.part = run_base[run_of_row[x.u.c_begin]] + x.u.part;
+    }
+
+    // LPT: biggest chunk-first units first, each onto the least-loaded CTA.
+    std::vector<std::vector<Unit>> per_cta(grid);
+    std::vector<double> load(grid, 0.0);
+    std::stable_sort(cf.begin(), cf.end(), [](const CfUnit& a, const CfUnit& b2) { return a.cost > b2.cost; });
+    {
+        using E = std::pair<double, int32_t>;
+        std::priority_queue<E, std::vector<E>, std::greater<E>> q;
+        for (int32_t k = 0; k < grid; ++k) q.push({0.0, k});
+        for (const auto& x : cf) {
+            E e = q.top();
+            q.pop();
+            per_cta[e.second].push_back(x.u);
+            e.first += x.cost;
+            load[e.second] = e.first;
+            q.push(e);
+        }
+    }
+
+    // Sequence-first pieces: walk the (position, head) list and fill each
+    // CTA up to the average, cumulative-rounded so all tiles are placed.
+    std::vector<int32_t> npart((size_t)b * H, 0);
+    for (int32_t pos = 0; pos < b; ++pos)
+        for (int32_t h = 0; h < H; ++h) npart[(size_t)pos * H + h] = nk1[pos];
+    {
+        std::vector<double> quota(grid);
+        double qsum = 0;
+        for (int32_t k = 0; k < grid; ++k) { quota[k] = std::max(0.0, avg - load[k]); qsum += quota[k]; }
+        const double scale = qsum > 0 ? sf_total / qsum : 0.0;
+        int64_t placed = 0;
+        double cum = 0;
+        int32_t pos = 0, h = 0, done = 0;   // cursor: chunks of (pos, h) already placed
+        auto seg_len = [&](int32_t ps) { return t.sf_offsets[ps + 1] - t.sf_offsets[ps]; };
+        // skip positions without sf chunks
+        while (pos < b && seg_len(pos) == 0) ++pos;
+        for (int32_t k = 0; k < grid && pos < b; ++k) {
+            cum += quota[k] * scale;
+            int64_t target = (k == grid - 1) ? (int64_t)sf_total : (int64_t)(cum + 0.5);
+            int64_t room = target - placed;
+            while (room > 0 && pos < b) {
+                const int32_t len = seg_len(pos);
+                const int32_t take = (int32_t)std::min<int64_t>(room, len - done);
+                const int32_t base = R + t.sf_offsets[pos];
+                int32_t& np = npart[(size_t)pos * H + h];
+                per_cta[k].push_back(Unit{UNIT_SF, h, pos, pos + 1, base + done, base + done + take, np, 0});
+                np += 1;
+                done += take;
+                placed += take;
+                room -= take;
+                if (done == len) {
+                    done = 0;
+                    if (++h == H) {
+                        h = 0;
+                        ++pos;
+                        while (pos < b && seg_len(pos) == 0) ++pos;
+                    }
+                }
+            }
+        }
+    }
+
+    plan.pbase.assign((size_t)b * H + 1, 0);
+    for (size_t i = 0; i < (size_t)b * H; ++i) plan.pbase[i + 1] = plan.pbase[i] + npart[i];
+    plan.n_partials = plan.pbase.back();
+    plan.cta_begin.assign(grid + 1, 0);
+    for (int32_t k = 0; k < grid; ++k) {
+        plan.cta_begin[k + 1] = plan.cta_begin[k] + (int32_t)per_cta[k].size();
+        plan.units.insert(plan.units.end(), per_cta[k].begin(), per_cta[k].end());
+    }
+}
+
+namespace {
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+}  // namespace
+
+void layout_plan(const Plan& plan, int32_t b, PlanLayout& lay, std::vector<unsigned char>& blob,
+                 const Tables& t) {
+    size_t off = 0;
+    lay.chunks = off;    off = align256(off + plan.chunks.size() * sizeof(ChunkRef));
+    lay.units = off;     off = align256(off + plan.units.size() * sizeof(Unit));
+    lay.cta_begin = off; off = align256(off + plan.cta_begin.size() * sizeof(int32_t));
+    lay.seq_perm = off;  off = align256(off + (size_t)b * sizeof(int32_t));
+    lay.pbase = off;     off = align256(off + plan.pbase.size() * sizeof(int32_t));
+    lay.status = off;    off = align256(off + sizeof(int32_t));
+    lay.total = off;
+    blob.assign(off, 0);
+    std::memcpy(blob.data() + lay.chunks, plan.chunks.data(), plan.chunks.size() * sizeof(ChunkRef));
+    std::memcpy(blob.data() + lay.units, plan.units.data(), plan.units.size() * sizeof(Unit));
+    std::memcpy(blob.data() + lay.cta_begin, plan.cta_begin.data(), plan.cta_begin.size() * sizeof(int32_t));
+    std::memcpy(blob.data() + lay.seq_perm, t.seq_perm.data(), (size_t)b * sizeof(int32_t));
+    std::memcpy(blob.data() + lay.pbase, plan.pbase.data(), plan.pbase.size() * sizeof(int32_t));
+}
+
+void layout_ws(const Plan& plan, const Pool& p, int32_t b, WsLayout& ws) {
+    const size_t H = p.cfg.n_heads, D = p.cfg.head_dim;
+    size_t off = 0;
+    ws.counters = off; off = align256(off + (size_t)b * H * sizeof(int32_t));
+    ws.part_o = off;   off = align256(off + (size_t)plan.n_partials * D * sizeof(float));
+    ws.part_ms = off;  off = align256(off + (size_t)plan.n_partials * 2 * sizeof(float));
+    ws.total = off;
+    ws.q_stage = off;  off = align256(off + (size_t)b * H * D * 2);
+    ws.out_stage = off; off = align256(off + (size_t)b * H * D * 2);
+    ws.total_host = off;
+}
+
+}  // namespace ca

@@ -10,3 +10,6 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+
+
+from tests.libfixture import lib  # noqa: E402,F401  (session fixture)

@@ -1,0 +1,182 @@
+"""The C library's host side against the oracle, on CPU (host-only pools: no
+GPU is touched).  Tables, slots, shared-token counts and pool statistics must
+match bit for bit [ChunkAttention (arXiv 2402.15220v4 summary) §3.1-§3.3]."""
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle.pakv import OracleTrie
+from oracle.schedule import build_schedule
+from tests.treegen import random_segment_sequences
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+TABLES = ["seq_perm", "cf_rows", "cf_runs", "sf_offsets", "sf_chunks", "merge_offsets", "merge_runs"]
+
+
+def header_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(ca_\w+)\s*\(", src, flags=re.M))
+    return names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from prefix_shared_decode_gb300 import capi
+    declared = header_functions()
+    assert declared == set(capi.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert lib.ca_error_string(-5) == b"schedule is older than the pool"
+
+
+def make_pools(c, cap, no_sharing=False, H=2, D=64):
+    from prefix_shared_decode_gb300 import Pool
+    return (Pool(1, H, D, c, cap, no_sharing=no_sharing, host_only=True),
+            OracleTrie(c, cap, no_sharing=no_sharing))
+
+
+def assert_tables_equal(sched, want):
+    got = sched.tables()
+    for name in TABLES:
+        np.testing.assert_array_equal(got[name], want[name].reshape(got[name].shape), err_msg=name)
+
+
+def test_golden_fixture_through_the_c_api(lib):
+    # The fixture uses c = 2; the library supports c in {16, 32, 64}.  Expand
+    # every fixture token to 16 tokens and use c = 32: chunk boundaries and
+    # sharing are preserved, token counts scale by 16.
+    from prefix_shared_decode_gb300 import Pool
+    X = 16
+    g_all = json.load(open(os.path.join(ROOT, "tests", "golden", "schedule_tiny_tree.json")))
+    for g in g_all["scenarios"]:
+        pool = Pool(1, 2, 64, g["chunk"] * X, g["capacity"], host_only=True)
+        expand = lambda toks: [t * X + j for t in toks for j in range(X)]
+        for op in g["ops"]:
+            if op["op"] == "insert":
+                assert pool.insert(op["seq_id"], expand(op["tokens"])) == op["n_shared"] * X
+                assert pool.seq_slots(op["seq_id"]) == op["slots"]
+            elif op["op"] == "remove":
+                pool.remove(op["seq_id"])
+            elif op["op"] == "stats":
+                st = pool.stats()
+                assert st["live_slots"] == op["live_slots"]
+                assert st["refcount_sum"] == op["refcount_sum"]
+            elif op["op"] == "schedule":
+                t = pool.schedule(op["seq_ids"]).tables()
+                for name in TABLES:
+                    want = np.array(op[name], dtype=np.int32).reshape(t[name].shape)
+                    if name in ("cf_rows", "sf_chunks") and want.size:
+                        want[:, 1] *= X
+                    np.testing.assert_array_equal(t[name], want, err_msg=name)
+
+
+@pytest.mark.parametrize("seed", range(16))
+@pytest.mark.parametrize("c", [16, 32])
+def test_random_trees_bit_exact_with_oracle(lib, seed, c):
+    seqs = random_segment_sequences(seed, 12, c)
+    pool, ref = make_pools(c, 400)
+    for i, toks in enumerate(seqs):
+        assert pool.match_prefix(toks) == ref.match_prefix(toks)
+        assert pool.insert(100 + i, toks) == ref.insert(100 + i, toks)
+        assert pool.seq_slots(100 + i) == ref.slots(100 + i)
+    rng = np.random.default_rng(seed)
+    for step in range(3):
+        live = sorted(ref.paths)
+        batch = [int(x) for x in rng.permutation(live)[: max(1, len(live) - step)]]
+        assert_tables_equal(pool.schedule(batch), build_schedule(ref, batch))
+        # churn: remove two, insert two new ones reusing stems of the removed
+        for sid in [int(x) for x in rng.choice(live, size=min(2, len(live) - 1), replace=False)]:
+            pool.remove(sid)
+            ref.remove(sid)
+        for j in range(2):
+            toks = random_segment_sequences(seed * 10 + step * 2 + j, 1, c)[0]
+            sid = 1000 + step * 2 + j
+            assert pool.insert(sid, toks) == ref.insert(sid, toks)
+            assert pool.seq_slots(sid) == ref.slots(sid)
+        st = pool.stats()
+        assert st["live_slots"] == ref.live_slots()
+        assert st["refcount_sum"] == ref.refcount_sum()
+        assert st["generation"] == ref.generation
+
+
+def test_no_sharing_pool_matches_oracle(lib):
+    seqs = random_segment_sequences(3, 10, 16)
+    pool, ref = make_pools(16, 500, no_sharing=True)
+    for i, toks in enumerate(seqs):
+        assert pool.insert(i, toks) == ref.insert(i, toks) == 0
+        assert pool.seq_slots(i) == ref.slots(i)
+    assert_tables_equal(pool.schedule(range(10)), build_schedule(ref, range(10)))
+    assert pool.schedule(range(10)).counts()["cf_rows"] == 0
+
+
+def test_no_tpp_schedule_makes_everything_sequence_first(lib):
+    from prefix_shared_decode_gb300 import Pool
+    pool = Pool(1, 2, 64, 16, 64, host_only=True)
+    prefix = list(range(48))
+    for i in range(4):
+        pool.insert(i, prefix + [1000 + 100 * i + j for j in range(5)])
+    t = pool.schedule([0, 1, 2, 3], no_tpp=True).tables()
+    assert len(t["cf_rows"]) == 0 and len(t["merge_runs"]) == 0
+    for p in range(4):
+        s = t["seq_perm"][p]
+        chunks = t["sf_chunks"][t["sf_offsets"][p]:t["sf_offsets"][p + 1]]
+        assert list(chunks[:, 0]) == pool.seq_slots(s)
+        assert chunks[:, 1].sum() == 53
+
+
+def test_errors_and_rollback(lib):
+    from prefix_shared_decode_gb300 import CAError, Pool
+    pool = Pool(1, 2, 64, 16, 5, host_only=True)
+    pool.insert(1, list(range(40)))                     # 3 slots
+    before = pool.stats()
+    with pytest.raises(CAError) as e:
+        pool.insert(2, list(range(16)) + list(range(100, 150)))   # shares 1, needs 4
+    assert e.value.name == "CA_ERR_OOM"
+    assert pool.stats() == before
+    for fn, name in [(lambda: pool.insert(1, [5]), "CA_ERR_EXISTS"),
+                     (lambda: pool.insert(3, []), "CA_ERR_INVALID"),
+                     (lambda: pool.remove(9), "CA_ERR_NOT_FOUND"),
+                     (lambda: pool.schedule([1, 1]), "CA_ERR_INVALID"),
+                     (lambda: pool.schedule([7]), "CA_ERR_NOT_FOUND"),
+                     (lambda: pool.schedule([]), "CA_ERR_INVALID")]:
+        with pytest.raises(CAError) as e:
+            fn()
+        assert e.value.name == name
+    with pytest.raises(CAError) as e:
+        Pool(1, 2, 96, 16, 5, host_only=True)
+    assert e.value.name == "CA_ERR_UNSUPPORTED"
+
+
+def test_schedule_is_cached_until_the_tree_changes(lib):
+    from prefix_shared_decode_gb300 import Pool
+    pool = Pool(1, 2, 64, 16, 64, host_only=True)
+    pool.insert(1, list(range(40)))
+    pool.insert(2, list(range(40)) + [7])
+    s = pool.schedule([1, 2])
+    h = s.handle.value
+    t0 = s.tables()
+    assert pool.schedule([1, 2], reuse=s).handle.value == h
+    pool.insert(3, [9] * 20)                            # tree changed: rebuilt in place
+    s2 = pool.schedule([1, 2, 3], reuse=s)
+    assert s2.handle.value == h and s2.counts()["b"] == 3
+    np.testing.assert_array_equal(pool.schedule([1, 2], reuse=s).tables()["cf_rows"], t0["cf_rows"])
+
+
+def test_remove_all_frees_everything(lib):
+    seqs = random_segment_sequences(5, 15, 16)
+    pool, ref = make_pools(16, 600)
+    for i, toks in enumerate(seqs):
+        pool.insert(i, toks)
+    for i in np.random.default_rng(5).permutation(15):
+        pool.remove(int(i))
+    st = pool.stats()
+    assert st["live_slots"] == 0 and st["free_slots"] == 600 and st["refcount_sum"] == 0
+    # the allocator restarts from slot 0
+    pool.insert(99, list(range(33)))
+    assert pool.seq_slots(99) == [0, 1, 2]

@@ -29,3 +29,32 @@ def lcp_chunks(a, b, c):
     while (k + 1) * c <= min(len(a), len(b)) and a[k * c:(k + 1) * c] == b[k * c:(k + 1) * c]:
         k += 1
     return k
+
+
+def random_segment_sequences(seed: int, n_seqs: int, chunk: int, n_segments: int = 8):
+    """Sequences that walk a random tree of token segments, plus random
+    private tails.  Segment lengths mix whole chunks with ragged lengths, so
+    branch points fall both on and inside chunk boundaries; an empty tail
+    makes identical sequences that end at the same node."""
+    rng = np.random.default_rng(seed)
+    parent, length = [-1], [0]
+    for s in range(1, n_segments + 1):
+        parent.append(int(rng.integers(0, s)))
+        length.append(int(rng.choice([chunk, 2 * chunk, 3 * chunk, chunk // 2, chunk + 3,
+                                      2 * chunk - 1])))
+    out = []
+    for i in range(n_seqs):
+        s = int(rng.integers(0, n_segments + 1))
+        path = []
+        while s > 0:
+            path.append(s)
+            s = parent[s]
+        toks = []
+        for seg in reversed(path):
+            toks += [seg * 1000 + j for j in range(length[seg])]
+        tail = int(rng.integers(0, 2 * chunk + 1))
+        toks += [500_000 + i * 1000 + j for j in range(tail)]
+        if not toks:
+            toks = [900_000 + i]
+        out.append(toks)
+    return out
