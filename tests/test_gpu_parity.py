@@ -1,0 +1,262 @@
+"""GPU parity of the two-phase decode attention kernel with the fp64 oracle.
+
+Bar: max |out - oracle| <= 2e-3 and mean |out - oracle| <= 2e-4 on fp16
+outputs computed with fp32 accumulation; tables and slots bit-exact.  Small
+cases compare every output with the oracle's trie-based decode attention;
+the full-size workloads compare sampled sequences (all heads) with the plain
+definition over that sequence's K/V [ChunkAttention explainer blog,
+Two-Phase Partition; ChunkAttention (arXiv 2402.15220v4 summary) §3.2]."""
+import numpy as np
+import pytest
+
+import workloads
+from oracle import attention as A
+from oracle.pakv import OracleTrie
+from oracle.schedule import build_schedule
+from tests.treegen import random_segment_sequences
+from workloads.device import capacity_for, insert_sequence
+
+pytestmark = pytest.mark.gpu
+TOL_MAX, TOL_MEAN = 2e-3, 2e-4
+
+
+@pytest.fixture(scope="module")
+def torch_cuda(lib):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch
+
+
+def assert_close(got, want, what=""):
+    err = np.abs(got.astype(np.float64) - want)
+    assert np.isfinite(got).all(), what
+    assert err.max() <= TOL_MAX, f"{what}: max err {err.max():.3g}"
+    assert err.mean() <= TOL_MEAN, f"{what}: mean err {err.mean():.3g}"
+
+
+def load(torch, wl, no_sharing=False, capacity=None):
+    from prefix_shared_decode_gb300 import Pool
+    pool = Pool(wl.n_layers, wl.n_heads, wl.head_dim, wl.chunk, capacity or capacity_for(wl),
+                no_sharing=no_sharing)
+    staging = {}
+    for sid in wl.seq_ids():
+        insert_sequence(pool, wl, sid, staging=staging)
+    return pool
+
+
+def run(torch, pool, batch, q, no_tpp=False, layer=0, scale=None):
+    from prefix_shared_decode_gb300 import decode_attention
+    sched = pool.schedule(batch, no_tpp=no_tpp)
+    out = decode_attention(pool, sched, torch.from_numpy(q).cuda(), layer=layer, scale=scale)
+    assert sched.device_status() == 0
+    return out.cpu().numpy(), sched
+
+
+def oracle_trie(wl):
+    trie = OracleTrie(wl.chunk, 100_000)
+    for sid in wl.seq_ids():
+        k, v = wl.kv_rows(sid)
+        trie.insert(sid, wl.tokens(sid), k, v)
+    return trie
+
+
+def test_tiny_workload_every_output(torch_cuda):
+    wl = workloads.make("tiny")
+    pool = load(torch_cuda, wl)
+    batch = wl.seq_ids()
+    q = wl.queries(0)
+    trie = oracle_trie(wl)
+    want = A.decode_attention(trie, batch, 0, q, wl.scale)
+    for no_tpp in (False, True):
+        got, sched = run(torch_cuda, pool, batch, q, no_tpp=no_tpp)
+        assert_close(got, want, f"tiny no_tpp={no_tpp}")
+    # the tables the kernel ran on are the oracle's, bit for bit
+    t = pool.schedule(batch).tables()
+    ref = build_schedule(trie, batch)
+    for name in ["seq_perm", "cf_rows", "cf_runs", "sf_offsets", "sf_chunks", "merge_offsets", "merge_runs"]:
+        np.testing.assert_array_equal(t[name], ref[name].reshape(t[name].shape), err_msg=name)
+    # sharing off (flat paged layout) gives the same attention
+    flat = load(torch_cuda, wl, no_sharing=True)
+    got, _ = run(torch_cuda, flat, batch, q)
+    assert_close(got, want, "tiny no_sharing")
+
+
+@pytest.mark.parametrize("c,D", [(16, 64), (32, 128), (64, 128), (64, 64), (16, 128), (32, 64)])
+@pytest.mark.parametrize("seed", range(3))
+def test_random_trees_every_output(torch_cuda, c, D, seed):
+    from prefix_shared_decode_gb300 import Pool
+    torch = torch_cuda
+    H = 4
+    rng = np.random.default_rng(seed)
+    seqs = random_segment_sequences(seed, 12, c, n_segments=10)
+    pool = Pool(2, H, D, c, 600)
+    trie = OracleTrie(c, 600)
+    for i, toks in enumerate(seqs):
+        k = rng.standard_normal((2, len(toks), H, D), dtype=np.float32).astype(np.float16)
+        v = rng.standard_normal((2, len(toks), H, D), dtype=np.float32).astype(np.float16)
+        trie.insert(i, toks, k, v)
+        pool.insert(i, toks, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+    batch = [int(x) for x in rng.permutation(12)[:10]]
+    q = rng.standard_normal((10, H, D), dtype=np.float32).astype(np.float16)
+    for layer in (0, 1):
+        want = A.decode_attention(trie, batch, layer, q, 1 / np.sqrt(D))
+        got, _ = run(torch, pool, batch, q, layer=layer)
+        assert_close(got, want, f"c={c} D={D} layer={layer}")
+
+
+def test_edge_cases(torch_cuda):
+    """One-token contexts, exactly one chunk, one chunk plus one token,
+    identical sequences (no sequence-first work at all), a batch of one."""
+    from prefix_shared_decode_gb300 import Pool
+    torch = torch_cuda
+    c, H, D = 64, 2, 128
+    rng = np.random.default_rng(11)
+    cases = {0: [1], 1: list(range(64)), 2: list(range(65)), 3: list(range(128)),
+             4: list(range(128)), 5: list(range(64)) + [777], 6: [5, 6, 7]}
+    pool = Pool(1, H, D, c, 64)
+    trie = OracleTrie(c, 64)
+    for sid, toks in cases.items():
+        k = rng.standard_normal((1, len(toks), H, D), dtype=np.float32).astype(np.float16)
+        v = rng.standard_normal((1, len(toks), H, D), dtype=np.float32).astype(np.float16)
+        trie.insert(sid, toks, k, v)
+        pool.insert(sid, toks, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+    for batch in ([0], [3, 4], list(cases), [6, 2, 1]):
+        q = rng.standard_normal((len(batch), H, D), dtype=np.float32).astype(np.float16)
+        want = A.decode_attention(trie, batch, 0, q, 0.1)
+        got, _ = run(torch, pool, batch, q, scale=0.1)
+        assert_close(got, want, f"batch {batch}")
+    # a one-token context returns that token's value exactly (up to fp16)
+    q = rng.standard_normal((1, H, D), dtype=np.float32).astype(np.float16)
+    got, _ = run(torch, pool, [0], q)
+    np.testing.assert_array_equal(got[0], trie.paths[0][0].v[0][0])
+
+
+def test_more_than_64_sharers(torch_cuda):
+    """A shared run with 70 sequences is split into query groups of <= 64."""
+    from prefix_shared_decode_gb300 import Pool
+    torch = torch_cuda
+    c, H, D, b = 64, 2, 128, 70
+    rng = np.random.default_rng(12)
+    pool = Pool(1, H, D, c, 400)
+    trie = OracleTrie(c, 400)
+    pk = rng.standard_normal((1, 300, H, D), dtype=np.float32).astype(np.float16)
+    pv = rng.standard_normal((1, 300, H, D), dtype=np.float32).astype(np.float16)
+    for i in range(b):
+        n_own = 1 + (i * 7) % 90
+        k = np.concatenate([pk, rng.standard_normal((1, n_own, H, D), dtype=np.float32).astype(np.float16)], 1)
+        v = np.concatenate([pv, rng.standard_normal((1, n_own, H, D), dtype=np.float32).astype(np.float16)], 1)
+        toks = list(range(300)) + [10_000 * (i + 1) + j for j in range(n_own)]
+        trie.insert(i, toks, k, v)
+        pool.insert(i, toks, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+    batch = list(range(b))[::-1]
+    q = rng.standard_normal((b, H, D), dtype=np.float32).astype(np.float16)
+    got, _ = run(torch, pool, batch, q)
+    assert_close(got, A.decode_attention(trie, batch, 0, q, 1 / np.sqrt(D)), "70 sharers")
+
+
+def test_kv_scatter_round_trip(torch_cuda):
+    """Rows copied into the pool sit in kv[slot][layer][K|V][head][row][:]."""
+    from prefix_shared_decode_gb300 import Pool
+    torch = torch_cuda
+    c, H, D, L = 32, 3, 64, 2
+    rng = np.random.default_rng(13)
+    pool = Pool(L, H, D, c, 32)
+    toks = list(range(70))
+    k = rng.standard_normal((L, 70, H, D), dtype=np.float32).astype(np.float16)
+    v = rng.standard_normal((L, 70, H, D), dtype=np.float32).astype(np.float16)
+    pool.insert(1, toks, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+    torch.cuda.synchronize()
+    kv = pool.kv_view().cpu().numpy()          # [slots, L, 2, H, c, D]
+    for i, slot in enumerate(pool.seq_slots(1)):
+        n = min(c, 70 - i * c)
+        for l in range(L):
+            np.testing.assert_array_equal(kv[slot, l, 0, :, :n], k[l, i * c:i * c + n].transpose(1, 0, 2))
+            np.testing.assert_array_equal(kv[slot, l, 1, :, :n], v[l, i * c:i * c + n].transpose(1, 0, 2))
+    # a second insert sharing the first chunk copies only its own rows
+    k2, v2 = -k, -v
+    assert pool.insert(2, toks[:32] + [999] * 5, torch.from_numpy(np.ascontiguousarray(k2[:, :37])).cuda(),
+                       torch.from_numpy(np.ascontiguousarray(v2[:, :37])).cuda()) == 32
+    torch.cuda.synchronize()
+    kv = pool.kv_view().cpu().numpy()
+    s0, s1 = pool.seq_slots(2)
+    np.testing.assert_array_equal(kv[s0, 0, 0, :, :32], k[0, :32].transpose(1, 0, 2))
+    np.testing.assert_array_equal(kv[s1, 0, 0, :, :5], k2[0, 32:37].transpose(1, 0, 2))
+
+
+def test_host_io_entry_and_repeat_calls(torch_cuda):
+    from prefix_shared_decode_gb300 import decode_attention, decode_attention_host
+    torch = torch_cuda
+    wl = workloads.make("tiny")
+    pool = load(torch, wl)
+    sched = pool.schedule(wl.seq_ids())
+    q = torch.from_numpy(wl.queries(3)).cuda()
+    a = decode_attention(pool, sched, q).cpu()
+    b = decode_attention(pool, sched, q).cpu()
+    assert torch.equal(a, b)                           # counters reset, deterministic merge
+    qh = q.cpu().pin_memory()
+    oh = torch.empty_like(qh).pin_memory()
+    decode_attention_host(pool, sched, qh, oh)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, a)
+    assert sched.device_status() == 0
+
+
+def test_stale_schedule_is_rejected(torch_cuda):
+    from prefix_shared_decode_gb300 import CAError, decode_attention
+    torch = torch_cuda
+    wl = workloads.make("tiny")
+    pool = load(torch, wl)
+    sched = pool.schedule(wl.seq_ids())
+    pool.remove(wl.seq_ids()[0])
+    with pytest.raises(CAError) as e:
+        decode_attention(pool, sched, torch.from_numpy(wl.queries(0)).cuda())
+    assert e.value.name == "CA_ERR_STALE"
+
+
+SAMPLE = 4
+
+
+@pytest.mark.parametrize("name", ["llama7b_p1024", "sweep_s2048_b32", "sweep_s2048_b64",
+                                  "sweep_s4096_b32", "sweep_s4096_b64", "no_sharing"])
+def test_full_size_workloads_sampled(torch_cuda, name):
+    """The benchmark's launch configuration at full size; every output is
+    finite and SAMPLE sequences (all heads) match the oracle."""
+    wl = workloads.make(name)
+    pool = load(torch_cuda, wl)
+    batch = wl.seq_ids()
+    q = wl.queries(0)
+    got, sched = run(torch_cuda, pool, batch, q)
+    assert np.isfinite(got).all()
+    rng = np.random.default_rng(0)
+    for i in sorted(rng.choice(len(batch), size=SAMPLE, replace=False)):
+        k, v = wl.kv_rows(batch[i])
+        want = A.softmax_attention(q[i], k[0], v[0], wl.scale)
+        assert_close(got[i], want, f"{name} seq {batch[i]}")
+
+
+def test_multi_tenant_with_churn_sampled(torch_cuda):
+    from prefix_shared_decode_gb300 import decode_attention
+    torch = torch_cuda
+    wl = workloads.make("multi_tenant")
+    pool = load(torch, wl)
+    staging = {}
+    sched = None
+    rng = np.random.default_rng(1)
+    for step in range(3):
+        if step:
+            removed, inserted = wl.churn_step()
+            for sid in removed:
+                pool.remove(sid)
+            for sid in inserted:
+                insert_sequence(pool, wl, sid, staging=staging)
+        batch = wl.seq_ids()
+        sched = pool.schedule(batch, reuse=sched)
+        q = wl.queries(step)
+        got = decode_attention(pool, sched, torch.from_numpy(q).cuda()).cpu().numpy()
+        assert sched.device_status() == 0
+        assert np.isfinite(got).all()
+        for i in sorted(rng.choice(len(batch), size=SAMPLE, replace=False)):
+            k, v = wl.kv_rows(batch[i])
+            assert_close(got[i], A.softmax_attention(q[i], k[0], v[0], wl.scale),
+                         f"multi_tenant step {step} seq {batch[i]}")
