@@ -233,6 +233,9 @@ def run_ours(args):
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, z in kev:        # torch creates the CUDA event on first record; the library re-records it
+        a.record(stream)
+        z.record(stream)
     clocks = ClockSampler(dev)
     clocks.start()
     time.sleep(0.3)

@@ -210,6 +210,8 @@ class Schedule:
     def set_profile_events(self, begin=None, end=None) -> None:
         bp = begin.cuda_event if begin is not None else None
         ep = end.cuda_event if end is not None else None
+        if begin is not None and not (bp and ep):
+            raise ValueError("record the events once before handing them to the library")
         check(capi.lib().ca_sched_set_profile_events(self._h, bp, ep), "ca_sched_set_profile_events")
 
 
