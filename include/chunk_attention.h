@@ -183,7 +183,7 @@ int ca_export_plan(const ca_sched* sched, int32_t counts[4], int32_t* units,
                    int32_t* cta_begin, int32_t* pbase, int32_t* chunks);
 
 /* Bytes of caller-owned device workspace ca_decode_attention needs for this
- * schedule (partial results and merge counters). */
+ * schedule (the partial results of the two phases). */
 int ca_workspace_bytes(const ca_sched* sched, size_t* bytes_out);
 
 /* ---- decode attention -----------------------------------------------------
@@ -194,9 +194,10 @@ int ca_workspace_bytes(const ca_sched* sched, size_t* bytes_out);
  *   out_dev  fp16 [b][n_heads][head_dim], written
  *   layer    0 <= layer < n_layers
  *   ws_dev   >= ca_workspace_bytes(sched) bytes, 256-byte aligned, caller
- *            owned.  It must be zero-filled before its first use; every
- *            completed call leaves it ready for the next one (any schedule).
- *            Calls sharing one workspace must not overlap on the GPU.
+ *            owned; its contents need no initialisation.  Calls sharing one
+ *            workspace must not overlap on the GPU.
+ * Two kernels run on `stream`: the two-phase kernel and a merge kernel
+ * launched as its programmatic dependent (one warp per sequence and head).
  * Errors: CA_ERR_STALE if the pool changed after the schedule was built;
  * CA_ERR_INVALID for a host-only pool, bad layer, NULL or misaligned pointers
  * or a small workspace; CA_ERR_CUDA if a launch fails.  Kernel-side faults

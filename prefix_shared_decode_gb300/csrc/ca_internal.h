@@ -42,7 +42,7 @@ struct Unit {
     int32_t c_begin;   // chunk range in the ChunkRef list
     int32_t c_end;
     int32_t part;      // partial index within each covered (position, head)
-    int32_t pad;
+    int32_t qrow;      // UNIT_SF: row of q / out of its position (seq_perm[q_lo])
 };
 
 // Offsets (in bytes) of the arrays inside the device plan blob.
@@ -60,7 +60,6 @@ struct AttnParams {
     int32_t* status;             // device status word (CA_ERR_* or 0)
     const uint16_t* q;           // fp16 [b][H][D]
     uint16_t* out;               // fp16 [b][H][D]
-    int32_t* counters;           // [b*H] merge arrival counters (zero between calls)
     float* part_o;               // [P][D] unnormalised partial outputs
     float2* part_ms;             // [P] (running max in log2 units, sum of exp2)
     int32_t n_layers, n_heads, layer, capacity;
@@ -70,7 +69,7 @@ struct AttnParams {
 
 // Workspace layout for a schedule.
 struct WsLayout {
-    size_t counters, part_o, part_ms, total;        // device-resident inputs
+    size_t part_o, part_ms, total;                  // device-resident inputs
     size_t q_stage, out_stage, total_host;          // + staging for host I/O
 };
 

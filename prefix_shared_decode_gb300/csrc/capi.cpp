@@ -295,7 +295,6 @@ static int decode_launch(const ca_pool* pool, const ca_sched* s, int32_t layer, 
     a.status = reinterpret_cast<int32_t*>(dev + s->layout.status);
     a.q = static_cast<const uint16_t*>(q);
     a.out = static_cast<uint16_t*>(out);
-    a.counters = reinterpret_cast<int32_t*>(ws + s->ws.counters);
     a.part_o = reinterpret_cast<float*>(ws + s->ws.part_o);
     a.part_ms = reinterpret_cast<float2*>(ws + s->ws.part_ms);
     a.n_layers = pool->cfg.n_layers;

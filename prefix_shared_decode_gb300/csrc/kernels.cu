@@ -18,9 +18,10 @@
 //  * a producer warp streams every chunk-head tile (c x D fp16, contiguous in
 //    the pool) into a ring of shared-memory stages with 2-D TMA loads,
 //    128-byte swizzled, completing on mbarriers; four consumer warps compute;
-//  * partials are merged by whichever unit finishes last for a (sequence,
-//    head), found with one atomic arrival counter per pair (the GPU-atomics
-//    merge of the paper's §3.3), so the whole step is one kernel launch;
+//  * every unit stores its partials with plain stores (no fences, atomics or
+//    waits between units); a small merge kernel, launched as a programmatic
+//    dependent of the main kernel so that its launch overlaps the main
+//    kernel's tail, combines the partials of each (sequence, head);
 //  * every wait is bounded (~1 s) and reports CA_ERR_TIMEOUT instead of
 //    hanging.
 #include <cuda.h>
@@ -75,7 +76,7 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 // Wait for an mbarrier phase; false after about a second (never hangs).
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t spin = 0; spin < (1u << 28); ++spin) {
@@ -141,35 +142,50 @@ __device__ __forceinline__ uint32_t swz(int r, int k, int rows) {
 }
 
 // ---------------------------------------------------------------------------
-// Merge of all partials of one (position, head): the explainer's output
-// combination, m* = max m_j, out = sum 2^{m_j-m*} o_j / sum 2^{m_j-m*} s_j
-// (m in log2 units).  One warp; lane owns D/32 dims.
+// Merge kernel: all partials of one (position, head) combined by the
+// explainer's output-combination rule, m* = max m_j,
+// out = sum 2^{m_j-m*} o_j / sum 2^{m_j-m*} s_j (m in log2 units).  One warp
+// per pair; lane j of a round of 32 holds partial j's (m, s); lane L owns
+// D/32 output dims.  Launched as a programmatic dependent of the main kernel:
+// `griddepcontrol.wait` returns once the main grid has completed and its
+// stores are visible.
 // ---------------------------------------------------------------------------
 template <int D>
-__device__ void merge_final(const AttnParams& p, int pos, int h, int lane) {
+__global__ void __launch_bounds__(128) merge_partials_kernel(const AttnParams p, int n_pairs) {
     constexpr int DPL = D / 32;
-    const int i = pos * p.n_heads + h;
-    const int a = p.pbase[i], z = p.pbase[i + 1];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int gw = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (gw >= n_pairs) return;
+    const int a = p.pbase[gw], n = p.pbase[gw + 1] - a;
     float M = -INFINITY;
-    for (int j = a; j < z; ++j) M = fmaxf(M, __ldcg(&p.part_ms[j]).x);
-    float acc[DPL];
+    for (int j = lane; j < n; j += 32) M = fmaxf(M, __ldcg(&p.part_ms[a + j]).x);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
+    float acc[DPL], S = 0.f;
 #pragma unroll
     for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
-    float S = 0.f;
-    for (int j = a; j < z; ++j) {
-        const float2 ms = __ldcg(&p.part_ms[j]);
+    for (int j0 = 0; j0 < n; j0 += 32) {
+        float2 ms = make_float2(-INFINITY, 0.f);
+        if (j0 + lane < n) ms = __ldcg(&p.part_ms[a + j0 + lane]);
         const float w = (ms.x == -INFINITY) ? 0.f : ex2(ms.x - M);
         S += w * ms.y;
-        const float* po = p.part_o + (size_t)j * D + lane * DPL;
-        if constexpr (DPL == 4) {
-            const float4 o = __ldcg(reinterpret_cast<const float4*>(po));
-            acc[0] += w * o.x; acc[1] += w * o.y; acc[2] += w * o.z; acc[3] += w * o.w;
-        } else {
-            const float2 o = __ldcg(reinterpret_cast<const float2*>(po));
-            acc[0] += w * o.x; acc[1] += w * o.y;
+        const int cnt = min(32, n - j0);
+        for (int j = 0; j < cnt; ++j) {
+            const float wj = __shfl_sync(kFull, w, j);
+            const float* po = p.part_o + (size_t)(a + j0 + j) * D + lane * DPL;
+            if constexpr (DPL == 4) {
+                const float4 o = __ldcg(reinterpret_cast<const float4*>(po));
+                acc[0] += wj * o.x; acc[1] += wj * o.y; acc[2] += wj * o.z; acc[3] += wj * o.w;
+            } else {
+                const float2 o = __ldcg(reinterpret_cast<const float2*>(po));
+                acc[0] += wj * o.x; acc[1] += wj * o.y;
+            }
         }
     }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) S += __shfl_xor_sync(kFull, S, off);
     const float inv = 1.f / S;
+    const int pos = gw / p.n_heads, h = gw % p.n_heads;
     uint16_t* dst = p.out + ((size_t)p.seq_perm[pos] * p.n_heads + h) * D + lane * DPL;
     if constexpr (DPL == 4) {
         uint2 v;
@@ -179,21 +195,6 @@ __device__ void merge_final(const AttnParams& p, int pos, int h, int lane) {
     } else {
         *reinterpret_cast<uint32_t*>(dst) = pack_half2(acc[0] * inv, acc[1] * inv);
     }
-}
-
-// Publish one partial and, if it was the last one of its (position, head),
-// produce the output.  Called by one lane per (position, head); the partial's
-// data must already be written and fenced by the writing lanes.
-__device__ __forceinline__ bool arrive_is_last(const AttnParams& p, int pos, int h) {
-    const int i = pos * p.n_heads + h;
-    const int need = p.pbase[i + 1] - p.pbase[i];
-    const int old = atomicAdd(&p.counters[i], 1);
-    if (old == need - 1) {
-        __threadfence();
-        p.counters[i] = 0;      // ready for the next call
-        return true;
-    }
-    return false;
 }
 
 // ---------------------------------------------------------------------------
@@ -285,7 +286,7 @@ __device__ __forceinline__ void sf_chunk(const uint8_t* kt, const uint8_t* vt, i
 // ---------------------------------------------------------------------------
 template <int C, int D, int NT>
 __device__ __forceinline__ void cf_chunk(uint32_t kt, uint32_t vt, int ntok, int tok0,
-                                         const uint32_t (&qa)[D / 16][4], float scale_log2,
+                                         uint32_t qrow_addr_base, float scale_log2,
                                          float (&m)[2], float (&s)[2], float (&o)[D / 8][4],
                                          int lane) {
     float sacc[NT / 8][4];
@@ -294,14 +295,21 @@ __device__ __forceinline__ void cf_chunk(uint32_t kt, uint32_t vt, int ntok, int
     // S = Q K^T over the D dims, 16 at a time.
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
+        // A fragment of the query block for dims [16 kk, 16 kk + 16), read from
+        // the swizzled Q tile (row rb*16 + lane%16, 16-byte chunk 2kk + lane/16).
+        uint32_t qa[4];
+        {
+            const int qr = (lane & 15), qc = 2 * kk + (lane >> 4);
+            ldsm_x4(qrow_addr_base + swz(qr, qc, kQRows), qa[0], qa[1], qa[2], qa[3]);
+        }
 #pragma unroll
         for (int np = 0; np < NT / 16; ++np) {
             const int tok = tok0 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
             const int kc = 2 * kk + ((lane >> 3) & 1);
             uint32_t b0, b1, b2, b3;
             ldsm_x4(kt + swz(tok, kc, C), b0, b1, b2, b3);
-            mma16816(sacc[2 * np], qa[kk], b0, b1);
-            mma16816(sacc[2 * np + 1], qa[kk], b2, b3);
+            mma16816(sacc[2 * np], qa, b0, b1);
+            mma16816(sacc[2 * np + 1], qa, b2, b3);
         }
     }
     // Online softmax per row (log2 units); columns past ntok are masked.
@@ -373,7 +381,7 @@ struct Smem {
 // The persistent two-phase kernel.
 // ---------------------------------------------------------------------------
 template <int C, int D>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __maxnreg__(200)
 two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnParams p) {
     using SM = Smem<C, D>;
     constexpr int DPL = D / 32;
@@ -387,6 +395,8 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // The merge kernel may be scheduled now; it waits for this grid itself.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if ((smem_u32(smem) & 1023u) != 0 || S < 1 || S > kMaxStages) {   // uniform across the CTA
         if (threadIdx.x == 0) set_status(p.status, CA_ERR_INVALID);
         return;
@@ -410,9 +420,20 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
         const uint64_t pol = policy_evict_first();
         int it = 0;
         bool ok = true;
+        // The plan was uploaded before any kernel that precedes this one in
+        // the stream, so it may be read before the dependency wait; the pool
+        // and the queries only after it.
+        Unit Un = (u_begin < u_end) ? p.units[u_begin] : Unit{};
+        // chunk references run one ahead of the copies they describe
+        ChunkRef chn = (u_begin < u_end) ? p.chunks[Un.c_begin] : ChunkRef{0, 0};
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         for (int u = u_begin; u < u_end && ok; ++u) {
-            const Unit U = p.units[u];
+            const Unit U = Un;
+            if (u + 1 < u_end) Un = p.units[u + 1];
             for (int c = U.c_begin; c < U.c_end; ++c, ++it) {
+                const ChunkRef ch = chn;
+                if (c + 1 < U.c_end) chn = p.chunks[c + 1];
+                else if (u + 1 < u_end) chn = p.chunks[Un.c_begin];
                 const int st = it % S;
                 const uint32_t ph = (uint32_t)(it / S) & 1u;
                 if (!mbar_wait(empty0 + 8 * st, ph ^ 1u)) {
@@ -420,7 +441,6 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     ok = false;
                     break;
                 }
-                const ChunkRef ch = p.chunks[c];
                 const uint32_t fb = full0 + 8 * st;
                 if (ch.slot < 0 || ch.slot >= p.capacity || U.head < 0 || U.head >= H) {
                     set_status(p.status, CA_ERR_DEVICE_BOUNDS);
@@ -450,24 +470,36 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
     // ------------------------------ consumers --------------------------------
     const int w = warp;
     int it = 0;
+    // Descriptors run two units ahead and a sequence-first unit's query row
+    // one unit ahead, so no unit starts on a dependent global load.
+    auto load_q = [&](const Unit& X) -> uint2 {
+        const uint16_t* qp = p.q + ((size_t)X.qrow * H + X.head) * D + lane * DPL;
+        if constexpr (DPL == 4) return *reinterpret_cast<const uint2*>(qp);
+        else return make_uint2(*reinterpret_cast<const uint32_t*>(qp), 0u);
+    };
+    Unit U0{}, U1{};
+    uint2 qn = make_uint2(0u, 0u);
+    if (u_begin < u_end) U0 = p.units[u_begin];
+    if (u_begin + 1 < u_end) U1 = p.units[u_begin + 1];
+    asm volatile("griddepcontrol.wait;" ::: "memory");     // q and the pool after this
+    if (u_begin < u_end && U0.kind == UNIT_SF) qn = load_q(U0);
     for (int u = u_begin; u < u_end; ++u) {
-        const Unit U = p.units[u];
+        const Unit U = U0;
+        const uint2 qraw = qn;
+        U0 = U1;
+        if (u + 2 < u_end) U1 = p.units[u + 2];
+        if (u + 1 < u_end && U0.kind == UNIT_SF) qn = load_q(U0);
         const int h = U.head;
         consumer_sync();   // previous unit (and its exchange reads) finished
         if (U.kind == UNIT_SF) {
             const int pos = U.q_lo;
             float q[DPL], o[DPL], m = -INFINITY, s = 0.f;
             {
-                const uint16_t* qp = p.q + ((size_t)p.seq_perm[pos] * H + h) * D + lane * DPL;
+                const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&qraw.x));
+                q[0] = a.x; q[1] = a.y;
                 if constexpr (DPL == 4) {
-                    const uint2 raw = *reinterpret_cast<const uint2*>(qp);
-                    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-                    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-                    q[0] = a.x; q[1] = a.y; q[2] = b.x; q[3] = b.y;
-                } else {
-                    const uint32_t raw = *reinterpret_cast<const uint32_t*>(qp);
-                    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw));
-                    q[0] = a.x; q[1] = a.y;
+                    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&qraw.y));
+                    q[2] = b.x; q[3] = b.y;
                 }
 #pragma unroll
                 for (int d = 0; d < DPL; ++d) { q[d] *= p.scale_log2; o[d] = 0.f; }
@@ -511,15 +543,12 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 }
                 const int pid = p.pbase[pos * H + h] + U.part;
                 float* dst = p.part_o + (size_t)pid * D + lane * DPL;
-#pragma unroll
-                for (int d = 0; d < DPL; ++d) dst[d] = acc[d];
+                if constexpr (DPL == 4) {
+                    *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                } else {
+                    *reinterpret_cast<float2*>(dst) = make_float2(acc[0], acc[1]);
+                }
                 if (lane == 0) p.part_ms[pid] = make_float2(M, sum);
-                __threadfence();
-                __syncwarp();
-                int last = 0;
-                if (lane == 0) last = arrive_is_last(p, pos, h);
-                last = __shfl_sync(kFull, last, 0);
-                if (last) merge_final<D>(p, pos, h, lane);
             }
         } else {
             // ---------------------------- chunk-first ----------------------------
@@ -540,17 +569,12 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 *reinterpret_cast<uint4*>(qreg + swz(r, k, kQRows)) = v;
             }
             consumer_sync();
-            uint32_t qa[D / 16][4];
             float o[D / 8][4], m[2] = {-INFINITY, -INFINITY}, s[2] = {0.f, 0.f};
 #pragma unroll
             for (int dt = 0; dt < D / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
-            if (active) {
-                const uint32_t qbase = smem_u32(qreg);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    ldsm_x4(qbase + swz(rb * 16 + (lane & 15), 2 * kk + (lane >> 4), kQRows),
-                            qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-            }
+            // Row block rb starts at a multiple of 8 rows, so its swizzle
+            // pattern is the tile's shifted by rb * 16 rows of 128 bytes.
+            const uint32_t qblock = smem_u32(qreg) + rb * 16 * 128;
             const int NTw = C / T;
             for (int c = U.c_begin; c < U.c_end; ++c, ++it) {
                 const int st = it % S;
@@ -563,11 +587,11 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     const uint32_t kt = smem_u32(stages + (size_t)st * SM::kStage);
                     const uint32_t vt = kt + SM::kTile;
                     if (NTw == 16) {
-                        cf_chunk<C, D, 16>(kt, vt, ntok, tp * 16, qa, p.scale_log2, m, s, o, lane);
+                        cf_chunk<C, D, 16>(kt, vt, ntok, tp * 16, qblock, p.scale_log2, m, s, o, lane);
                     } else if constexpr (C >= 32) {
                         // 32 tokens at a time keeps the score tile in registers
                         for (int t0 = tp * NTw; t0 < (tp + 1) * NTw; t0 += 32)
-                            cf_chunk<C, D, 32>(kt, vt, ntok, t0, qa, p.scale_log2, m, s, o, lane);
+                            cf_chunk<C, D, 32>(kt, vt, ntok, t0, qblock, p.scale_log2, m, s, o, lane);
                     }
                 }
                 __syncwarp();
@@ -625,7 +649,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 }
             }
             // Warps with tp == 0 now hold their row block: write one partial
-            // per valid row, then count arrivals and merge where last.
+            // per valid row.
             if (active && tp == 0) {
                 const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll
@@ -641,17 +665,6 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                                 make_float2(o[dt][2 * r], o[dt][2 * r + 1]);
                         if (t4 == 0) p.part_ms[pid] = make_float2(m[r], s[r]);
                     }
-                }
-                __threadfence();
-                __syncwarp();
-                int last = 0;
-                const int row = rb * 16 + lane;
-                if (lane < 16 && row < m_rows) last = arrive_is_last(p, U.q_lo + row, h);
-                unsigned todo = __ballot_sync(kFull, last);
-                while (todo) {
-                    const int l = __ffs(todo) - 1;
-                    todo &= todo - 1;
-                    merge_final<D>(p, U.q_lo + rb * 16 + l, h, lane);
                 }
             }
         }
@@ -816,9 +829,36 @@ int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void*
     const CUtensorMap* map = reinterpret_cast<const CUtensorMap*>(p.tmap);
     void* args[] = {const_cast<CUtensorMap*>(map), &a};
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // Both kernels are programmatic dependents of whatever precedes them in
+    // the stream: their launch overlaps the previous kernel's tail and each
+    // waits (griddepcontrol.wait) before touching data that kernel may write.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t mc = {};
+    mc.gridDim = dim3((unsigned)s.plan.grid);
+    mc.blockDim = dim3(dev::kThreads);
+    mc.dynamicSmemBytes = bytes;
+    mc.stream = cs;
+    mc.attrs = attr;
+    mc.numAttrs = 1;
     if (s.ev_begin) cudaEventRecord(static_cast<cudaEvent_t>(s.ev_begin), cs);
-    cudaError_t e = cudaLaunchKernel(fn, dim3(s.plan.grid), dim3(dev::kThreads), args, bytes, cs);
+    cudaError_t e = cudaLaunchKernelExC(&mc, fn, args);
     if (s.ev_end) cudaEventRecord(static_cast<cudaEvent_t>(s.ev_end), cs);
+    if (e != cudaSuccess) return CA_ERR_CUDA;
+    // Merge: one warp per (position, head).
+    const int n_pairs = s.t.b * p.cfg.n_heads;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)((n_pairs + 3) / 4));
+    lc.blockDim = dim3(128);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = cs;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    if (p.cfg.head_dim == 128)
+        e = cudaLaunchKernelEx(&lc, dev::merge_partials_kernel<128>, a, n_pairs);
+    else
+        e = cudaLaunchKernelEx(&lc, dev::merge_partials_kernel<64>, a, n_pairs);
     return e == cudaSuccess ? CA_OK : CA_ERR_CUDA;
 }
 

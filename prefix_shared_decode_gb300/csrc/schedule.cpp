@@ -123,10 +123,11 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
 // Work plan.
 // Cost model, in "chunk-head tiles" (one chunk of one head, K and V): a
 // sequence-first tile costs 1 (HBM-bound); a chunk-first tile for m queries
-// costs 1 + kCfComputePer16 * ceil(m / 16) (tensor-core work grows with m).
+// costs 1 + kCfComputePer16 * ceil(m / 16) (tensor-core work grows with m;
+// the coefficient is fitted to measured per-chunk unit times on GB300).
 // ---------------------------------------------------------------------------
 namespace {
-constexpr double kCfComputePer16 = 0.25;
+constexpr double kCfComputePer16 = 0.2;
 constexpr int32_t kMaxCfQueries = 64;
 }  // namespace
 
@@ -250,7 +251,8 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
                 const int32_t take = (int32_t)std::min<int64_t>(room, len - done);
                 const int32_t base = R + t.sf_offsets[pos];
                 int32_t& np = npart[(size_t)pos * H + h];
-                per_cta[k].push_back(Unit{UNIT_SF, h, pos, pos + 1, base + done, base + done + take, np, 0});
+                per_cta[k].push_back(Unit{UNIT_SF, h, pos, pos + 1, base + done, base + done + take, np,
+                                          t.seq_perm[pos]});
                 np += 1;
                 done += take;
                 placed += take;
@@ -302,7 +304,6 @@ void layout_plan(const Plan& plan, int32_t b, PlanLayout& lay, std::vector<unsig
 void layout_ws(const Plan& plan, const Pool& p, int32_t b, WsLayout& ws) {
     const size_t H = p.cfg.n_heads, D = p.cfg.head_dim;
     size_t off = 0;
-    ws.counters = off; off = align256(off + (size_t)b * H * sizeof(int32_t));
     ws.part_o = off;   off = align256(off + (size_t)plan.n_partials * D * sizeof(float));
     ws.part_ms = off;  off = align256(off + (size_t)plan.n_partials * 2 * sizeof(float));
     ws.total = off;

@@ -202,6 +202,18 @@ def test_host_io_entry_and_repeat_calls(torch_cuda):
     assert sched.device_status() == 0
 
 
+def test_two_ctas_per_sm(torch_cuda):
+    """The persistent grid holds two CTAs per SM (registers and shared memory
+    of the largest instantiation fit twice)."""
+    from prefix_shared_decode_gb300 import Pool
+    pool = Pool(1, 32, 128, 64, 64)
+    toks = list(range(64 * 40))
+    k = torch_cuda.zeros((1, len(toks), 32, 128), dtype=torch_cuda.float16, device="cuda")
+    pool.insert(0, toks, k, k)
+    sms = torch_cuda.cuda.get_device_properties(0).multi_processor_count
+    assert pool.schedule([0]).plan()["grid"] == min(2 * sms, 40 * 32)
+
+
 def test_stale_schedule_is_rejected(torch_cuda):
     from prefix_shared_decode_gb300 import CAError, decode_attention
     torch = torch_cuda
