@@ -381,7 +381,7 @@ struct Smem {
 // The persistent two-phase kernel.
 // ---------------------------------------------------------------------------
 template <int C, int D>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 2)
 two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnParams p) {
     using SM = Smem<C, D>;
     constexpr int DPL = D / 32;
