@@ -51,6 +51,8 @@ extern "C" {
 #define CA_ERR_DEVICE_BOUNDS -7  /* a kernel saw a table index out of range    */
 #define CA_ERR_TIMEOUT       -8  /* a kernel wait gave up after ~1 s           */
 #define CA_ERR_UNSUPPORTED   -9  /* shape the kernels are not built for        */
+#define CA_ERR_SCRATCH_LIMIT -10  /* schedule needs more than the library's own
+                                     scratch buffer (CA_STATIC_WS_BYTES) holds  */
 
 /* ---- pool flags -------------------------------------------------------- */
 /* Never match prefixes: every sequence owns a private chain of chunks.  This
@@ -216,6 +218,29 @@ int ca_decode_attention_host(const ca_pool* pool, const ca_sched* sched,
                              int32_t layer, const void* q_host, void* out_host,
                              float scale, void* ws_dev, size_t ws_bytes,
                              void* stream);
+
+/* ca_decode_attention for callers that cannot allocate device memory at the
+ * point of the call (a component inside a server that has already reserved
+ * the whole device memory budget for its own pool, a latency-critical path
+ * where cudaMalloc / cudaFree would synchronise the device, a plugin whose
+ * host forbids allocation in its callbacks).  There is no workspace
+ * argument: the partial results go to a fixed buffer the library holds in
+ * device memory, CA_STATIC_WS_BYTES bytes per GPU that loads the library,
+ * kept until the process exits.  The call allocates nothing; the caller
+ * still passes q_dev and out_dev as for ca_decode_attention.
+ *   - The first call on a device looks up the buffer's device address
+ *     (cudaGetSymbolAddress); make that first call outside any stream
+ *     capture.  The pool's device must be current.
+ *   - Every call shares the one buffer: calls that overlap on the GPU
+ *     (other streams, other host threads) race and corrupt each other's
+ *     results.  Nothing in the buffer needs clearing between calls.
+ *   - A schedule whose ca_workspace_bytes() exceeds CA_STATIC_WS_BYTES is
+ *     rejected with CA_ERR_SCRATCH_LIMIT; other errors as ca_decode_attention.
+ * The pages describe no such call; it exists for callers of this library. */
+#define CA_STATIC_WS_BYTES (16u << 20)
+int ca_decode_attention_static_ws(const ca_pool* pool, const ca_sched* sched,
+                                  int32_t layer, const void* q_dev, void* out_dev,
+                                  float scale, void* stream);
 
 /* Synchronise `stream` and read the schedule's device status word: CA_OK,
  * CA_ERR_DEVICE_BOUNDS or CA_ERR_TIMEOUT; the word is then cleared. */

@@ -17,7 +17,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libchunk_attention.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CU_SOURCES = ["kernels.cu"]
+CU_SOURCES = ["kernels.cu", "static_ws.cu"]
 CPP_SOURCES = ["pool.cpp", "schedule.cpp", "capi.cpp"]
 
 

@@ -14,8 +14,9 @@ CA_OK = 0
 ERRORS = {
     -1: "CA_ERR_INVALID", -2: "CA_ERR_OOM", -3: "CA_ERR_NOT_FOUND", -4: "CA_ERR_EXISTS",
     -5: "CA_ERR_STALE", -6: "CA_ERR_CUDA", -7: "CA_ERR_DEVICE_BOUNDS", -8: "CA_ERR_TIMEOUT",
-    -9: "CA_ERR_UNSUPPORTED",
+    -9: "CA_ERR_UNSUPPORTED", -10: "CA_ERR_SCRATCH_LIMIT",
 }
+CA_STATIC_WS_BYTES = 16 << 20
 CA_NO_SHARING = 1
 CA_SCHED_NO_TPP = 1
 
@@ -24,7 +25,8 @@ EXPORTS = [
     "ca_pool_bytes", "ca_pool_create", "ca_pool_destroy", "ca_match_prefix", "ca_insert_tokens",
     "ca_remove_seq", "ca_pool_stats", "ca_seq_slots", "ca_build_schedule", "ca_sched_destroy",
     "ca_sched_counts", "ca_export_tables", "ca_export_plan", "ca_workspace_bytes", "ca_decode_attention",
-    "ca_workspace_bytes_host", "ca_decode_attention_host", "ca_sched_device_status",
+    "ca_workspace_bytes_host", "ca_decode_attention_host", "ca_decode_attention_static_ws",
+    "ca_sched_device_status",
     "ca_sched_set_profile_events", "ca_error_string",
 ]
 
@@ -79,6 +81,7 @@ def lib() -> C.CDLL:
         "ca_workspace_bytes_host": [vp, P(sz)],
         "ca_decode_attention": [vp, vp, i32, vp, vp, C.c_float, vp, sz, vp],
         "ca_decode_attention_host": [vp, vp, i32, vp, vp, C.c_float, vp, sz, vp],
+        "ca_decode_attention_static_ws": [vp, vp, i32, vp, vp, C.c_float, vp],
         "ca_sched_device_status": [vp, vp],
         "ca_sched_set_profile_events": [vp, vp, vp],
         "ca_error_string": [C.c_int],

@@ -360,6 +360,7 @@ const char* ca_error_string(int status) {
         case CA_ERR_DEVICE_BOUNDS: return "kernel saw a table index out of range";
         case CA_ERR_TIMEOUT: return "kernel wait timed out";
         case CA_ERR_UNSUPPORTED: return "shape not supported";
+        case CA_ERR_SCRATCH_LIMIT: return "schedule needs more scratch than the static buffer holds";
         default: return "unknown status";
     }
 }

@@ -1,0 +1,88 @@
+// ca_decode_attention_static_ws: decode attention for callers that cannot
+// allocate device memory at the point of the call.
+//
+// ca_decode_attention needs a caller-provided device workspace for the
+// partial results of the two phases.  Some callers cannot allocate one: a
+// component running inside a server that has already reserved the whole
+// device memory budget for its own pool, code on a latency-critical path
+// where cudaMalloc / cudaFree would synchronise the device, or a plugin whose
+// host forbids allocation inside its callbacks.  This entry point takes the
+// partials from a fixed buffer that the library itself holds in device
+// memory, so the call allocates nothing.
+//
+// The buffer is a file-scope __device__ array of CA_STATIC_WS_BYTES bytes.
+// Every GPU that loads the library keeps it until the process exits.  All
+// calls share it and it keeps whatever the last call left there: the kernels
+// write every partial before reading it, so nothing has to be cleared, but
+// two calls that overlap on the GPU (different streams, or different host
+// threads) would overwrite each other's partials.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "ca_internal.h"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_ws[CA_STATIC_WS_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_lock;
+void* g_ws_ptr[kMaxDevices] = {};
+
+// Device address of g_static_ws on `device` (which must be current).  Looked
+// up once per device: in host code the array's name is only a host-side
+// stand-in, not a device address.
+int static_ws_address(int device, void** out) {
+    if (device < 0 || device >= kMaxDevices) return CA_ERR_INVALID;
+    std::lock_guard<std::mutex> guard(g_lock);
+    if (!g_ws_ptr[device]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_ws) != cudaSuccess || !ptr) return CA_ERR_CUDA;
+        g_ws_ptr[device] = ptr;
+    }
+    *out = g_ws_ptr[device];
+    return CA_OK;
+}
+
+}  // namespace
+
+extern "C" int ca_decode_attention_static_ws(const ca_pool* pool_, const ca_sched* sched_,
+                                             int32_t layer, const void* q_dev, void* out_dev,
+                                             float scale, void* stream) {
+    const ca::Pool* pool = reinterpret_cast<const ca::Pool*>(pool_);
+    const ca::Sched* s = reinterpret_cast<const ca::Sched*>(sched_);
+    if (!pool || !s || !pool->kv || s->pool != pool || !s->dev) return CA_ERR_INVALID;
+    if (s->generation != pool->generation) return CA_ERR_STALE;
+    if (layer < 0 || layer >= pool->cfg.n_layers) return CA_ERR_INVALID;
+    if (!q_dev || !out_dev || (reinterpret_cast<uintptr_t>(q_dev) & 15) ||
+        (reinterpret_cast<uintptr_t>(out_dev) & 15))
+        return CA_ERR_INVALID;
+    if (s->ws.total > (size_t)CA_STATIC_WS_BYTES) return CA_ERR_SCRATCH_LIMIT;
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) return CA_ERR_CUDA;
+    if (device != pool->device) return CA_ERR_INVALID;
+    void* ws = nullptr;
+    int st = static_ws_address(device, &ws);
+    if (st) return st;
+
+    unsigned char* dev = static_cast<unsigned char*>(s->dev);
+    unsigned char* w = static_cast<unsigned char*>(ws);
+    ca::AttnParams a{};
+    a.chunks = reinterpret_cast<const ca::ChunkRef*>(dev + s->layout.chunks);
+    a.units = reinterpret_cast<const ca::Unit*>(dev + s->layout.units);
+    a.cta_begin = reinterpret_cast<const int32_t*>(dev + s->layout.cta_begin);
+    a.seq_perm = reinterpret_cast<const int32_t*>(dev + s->layout.seq_perm);
+    a.pbase = reinterpret_cast<const int32_t*>(dev + s->layout.pbase);
+    a.status = reinterpret_cast<int32_t*>(dev + s->layout.status);
+    a.q = static_cast<const uint16_t*>(q_dev);
+    a.out = static_cast<uint16_t*>(out_dev);
+    a.part_o = reinterpret_cast<float*>(w + s->ws.part_o);
+    a.part_ms = reinterpret_cast<float2*>(w + s->ws.part_ms);
+    a.n_layers = pool->cfg.n_layers;
+    a.n_heads = pool->cfg.n_heads;
+    a.layer = layer;
+    a.capacity = pool->cfg.capacity_slots;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    return ca::launch_attention(*pool, *s, a, stream);
+}
