@@ -84,8 +84,10 @@ struct Node {
     // full shareable chunks only, keyed by their token tuple
     std::unordered_map<std::string, Node*> match;
     int32_t refcount = 0;
-    int32_t mark = 0;              // scratch for schedule building
+    int32_t mark = 0;              // scratch for schedule building: batch holders
     int32_t row = -1;              // scratch: chunk-first row while building
+    int32_t end_begin = 0;         // scratch: batch sequences ending here, as a
+    int32_t end_count = 0;         //   range of the sorted (node, seq_id) list
 };
 
 struct Sequence {

@@ -27,27 +27,41 @@ namespace ca {
 
 int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flags, Tables& t) {
     if (b < 1 || !seq_ids) return CA_ERR_INVALID;
+    for (int32_t i = 0; i < b; ++i)
+        if (!p.seqs.count(seq_ids[i])) return CA_ERR_NOT_FOUND;
     {
-        std::unordered_set<int64_t> seen;
-        for (int32_t i = 0; i < b; ++i) {
-            if (!p.seqs.count(seq_ids[i])) return CA_ERR_NOT_FOUND;
-            if (!seen.insert(seq_ids[i]).second) return CA_ERR_INVALID;
-        }
+        std::vector<int64_t> sorted(seq_ids, seq_ids + b);
+        std::sort(sorted.begin(), sorted.end());
+        if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end()) return CA_ERR_INVALID;
     }
     const bool tpp = !(flags & CA_SCHED_NO_TPP);
-    // Batch holders per node (Node::mark) and sequences ending at each node.
-    std::unordered_map<const Node*, std::vector<int64_t>> ending;
+    // Batch holders per node (Node::mark), and the sequences ending at each
+    // node as one range of a (node, seq_id)-sorted list.
+    std::vector<const Sequence*> seq_of(b);
+    std::vector<std::pair<const Node*, int64_t>> ends(b);
     for (int32_t i = 0; i < b; ++i) {
         const Sequence& s = p.seqs.at(seq_ids[i]);
+        seq_of[i] = &s;
         for (Node* n : s.path) n->mark += 1;
-        ending[s.path.back()].push_back(seq_ids[i]);
+        ends[i] = {s.path.back(), seq_ids[i]};
     }
-    for (auto& kv : ending) std::sort(kv.second.begin(), kv.second.end());
+    std::sort(ends.begin(), ends.end());
+    for (int32_t i = 0; i < b;) {
+        int32_t j = i;
+        while (j < b && ends[j].first == ends[i].first) ++j;
+        Node* n = const_cast<Node*>(ends[i].first);
+        n->end_begin = i;
+        n->end_count = j - i;
+        i = j;
+    }
 
     std::vector<int64_t> order;
     order.reserve(b);
     t = Tables();
     t.b = b;
+    t.seq_perm.reserve(b);
+    t.sf_offsets.reserve(b + 1);
+    t.merge_offsets.reserve(b + 1);
     std::vector<const Node*> row_node;
     struct Frame { const Node* node; size_t next; };
     std::vector<Frame> stack;
@@ -62,8 +76,7 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
                 t.cf_rows.insert(t.cf_rows.end(),
                                  {node->slot, (int32_t)node->tokens.size(), (int32_t)order.size(), -1});
             }
-            auto e = ending.find(node);
-            if (e != ending.end()) order.insert(order.end(), e->second.begin(), e->second.end());
+            for (int32_t k = 0; k < node->end_count; ++k) order.push_back(ends[node->end_begin + k].second);
         }
         size_t ci = f.next;
         while (ci < node->children.size() && node->children[ci]->mark == 0) ++ci;
@@ -77,11 +90,16 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
     }
 
     // seq_perm: DFS position -> caller row.
-    std::unordered_map<int64_t, int32_t> caller;
-    caller.reserve(b);
-    for (int32_t i = 0; i < b; ++i) caller[seq_ids[i]] = i;
+    std::vector<std::pair<int64_t, int32_t>> caller(b);
+    for (int32_t i = 0; i < b; ++i) caller[i] = {seq_ids[i], i};
+    std::sort(caller.begin(), caller.end());
     t.seq_perm.resize(b);
-    for (int32_t pos = 0; pos < b; ++pos) t.seq_perm[pos] = caller[order[pos]];
+    std::vector<const Sequence*> seq_at(b);
+    for (int32_t pos = 0; pos < b; ++pos) {
+        const int32_t i = std::lower_bound(caller.begin(), caller.end(), std::make_pair(order[pos], INT32_MIN))->second;
+        t.seq_perm[pos] = i;
+        seq_at[pos] = seq_of[i];
+    }
 
     // Runs.
     const int32_t R = (int32_t)row_node.size();
@@ -99,7 +117,7 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
     // Sequence-first lists.
     t.sf_offsets.assign(1, 0);
     for (int32_t pos = 0; pos < b; ++pos) {
-        for (const Node* n : p.seqs.at(order[pos]).path)
+        for (const Node* n : seq_at[pos]->path)
             if (!tpp || n->mark == 1) t.sf_chunks.insert(t.sf_chunks.end(), {n->slot, (int32_t)n->tokens.size()});
         t.sf_offsets.push_back((int32_t)(t.sf_chunks.size() / 2));
     }
@@ -114,8 +132,11 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
         t.merge_offsets.push_back((int32_t)t.merge_runs.size());
     }
 
-    for (int32_t i = 0; i < b; ++i)
-        for (Node* n : p.seqs.at(seq_ids[i]).path) { n->mark = 0; n->row = -1; }
+    for (int32_t i = 0; i < b; ++i) {
+        for (Node* n : seq_of[i]->path) { n->mark = 0; n->row = -1; }
+        Node* e = seq_of[i]->path.back();
+        e->end_begin = e->end_count = 0;
+    }
     return CA_OK;
 }
 
@@ -158,6 +179,7 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
     std::vector<int32_t> pieces(U, 0);
     struct CfUnit { Unit u; double cost; };
     std::vector<CfUnit> cf;
+    cf.reserve((size_t)U * H * 4);
     for (int32_t u = 0; u < U; ++u) {
         const int32_t row0 = t.cf_runs[4 * u], nrows = t.cf_runs[4 * u + 1];
         const int32_t lo = t.cf_runs[4 * u + 2], hi = t.cf_runs[4 * u + 3], m = hi - lo;
@@ -209,7 +231,9 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
     }
 
     // LPT: biggest chunk-first units first, each onto the least-loaded CTA.
-    std::vector<std::vector<Unit>> per_cta(grid);
+    // Units are collected flat with their CTA and counting-sorted at the end.
+    std::vector<std::pair<int32_t, Unit>> tagged;
+    tagged.reserve(cf.size() + (size_t)b * H + grid);
     std::vector<double> load(grid, 0.0);
     std::stable_sort(cf.begin(), cf.end(), [](const CfUnit& a, const CfUnit& b2) { return a.cost > b2.cost; });
     {
@@ -219,7 +243,7 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
         for (const auto& x : cf) {
             E e = q.top();
             q.pop();
-            per_cta[e.second].push_back(x.u);
+            tagged.emplace_back(e.second, x.u);
             e.first += x.cost;
             load[e.second] = e.first;
             q.push(e);
@@ -251,8 +275,8 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
                 const int32_t take = (int32_t)std::min<int64_t>(room, len - done);
                 const int32_t base = R + t.sf_offsets[pos];
                 int32_t& np = npart[(size_t)pos * H + h];
-                per_cta[k].push_back(Unit{UNIT_SF, h, pos, pos + 1, base + done, base + done + take, np,
-                                          t.seq_perm[pos]});
+                tagged.emplace_back(k, Unit{UNIT_SF, h, pos, pos + 1, base + done, base + done + take, np,
+                                            t.seq_perm[pos]});
                 np += 1;
                 done += take;
                 placed += take;
@@ -272,10 +296,15 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
     plan.pbase.assign((size_t)b * H + 1, 0);
     for (size_t i = 0; i < (size_t)b * H; ++i) plan.pbase[i + 1] = plan.pbase[i] + npart[i];
     plan.n_partials = plan.pbase.back();
+    // Counting sort by CTA, stable: each CTA keeps its chunk-first units
+    // first, then its sequence-first pieces in list order.
     plan.cta_begin.assign(grid + 1, 0);
-    for (int32_t k = 0; k < grid; ++k) {
-        plan.cta_begin[k + 1] = plan.cta_begin[k] + (int32_t)per_cta[k].size();
-        plan.units.insert(plan.units.end(), per_cta[k].begin(), per_cta[k].end());
+    for (const auto& x : tagged) plan.cta_begin[x.first + 1] += 1;
+    for (int32_t k = 0; k < grid; ++k) plan.cta_begin[k + 1] += plan.cta_begin[k];
+    plan.units.resize(tagged.size());
+    {
+        std::vector<int32_t> fill(plan.cta_begin.begin(), plan.cta_begin.end() - 1);
+        for (const auto& x : tagged) plan.units[fill[x.first]++] = x.second;
     }
 }
 
