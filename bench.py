@@ -209,6 +209,7 @@ def run_ours(args):
 
     churn = wl.churn > 0
     churn_host_us = []
+    host_split = {"remove": [], "insert": [], "schedule": []}
     if churn:
         # Draw every step's churn (ids, tokens) before timing.  Inserted rows
         # come from device-resident N(0,1) fp16 blocks, so the timed step does
@@ -231,11 +232,18 @@ def run_ours(args):
             removed, inserted, live = plan_churn[i]
             for sid in removed:
                 pool.remove(sid)
+            t1 = time.perf_counter()
             for sid, toks in inserted:
                 pool.insert(sid, toks, kblk[:, :len(toks)], vblk[:, :len(toks)])
+            t2 = time.perf_counter()
             batch = live
-            churn_host_us.append((time.perf_counter() - th) * 1e6)
         sched = pool.schedule(batch, reuse=sched)
+        if churn:
+            t3 = time.perf_counter()
+            host_split["remove"].append((t1 - th) * 1e6)
+            host_split["insert"].append((t2 - t1) * 1e6)
+            host_split["schedule"].append((t3 - t2) * 1e6)
+            churn_host_us.append((t3 - th) * 1e6)
         if sched.workspace_bytes() > ws.numel():
             ws = torch.zeros(2 * sched.workspace_bytes(), dtype=torch.uint8, device=dev)
         decode_attention(pool, sched, qs[i % 4], out=out, scale=wl.scale, workspace=ws)
@@ -386,6 +394,7 @@ def run_ours(args):
     if churn:
         res["config"]["churn_per_step"] = wl.churn
         res["churn_host_us"] = round(statistics.median(churn_host_us), 1)
+        res["churn_host_split_us"] = {k: round(statistics.median(v), 1) for k, v in host_split.items()}
     if context:
         res["context"] = context
         res["context"]["speedup_vs_paged_flat"] = round(context["paged_flat_us"] / us, 2)

@@ -153,10 +153,18 @@ __device__ __forceinline__ uint32_t swz(int r, int k, int rows) {
 template <int D>
 __global__ void __launch_bounds__(128) merge_partials_kernel(const AttnParams p, int n_pairs) {
     constexpr int DPL = D / 32;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    constexpr int KB = 4;                          // partials whose loads are in flight together
     const int gw = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    // Plan entries may be read before the dependency wait; partials only after.
+    int a = 0, n = 0, row = 0;
+    if (gw < n_pairs) {
+        a = p.pbase[gw];
+        n = p.pbase[gw + 1] - a;
+        row = p.seq_perm[gw / p.n_heads];
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (gw >= n_pairs) return;
-    const int a = p.pbase[gw], n = p.pbase[gw + 1] - a;
+    // Every lane loads (m, s) of partials lane, lane + 32, ...: max, then weights.
     float M = -INFINITY;
     for (int j = lane; j < n; j += 32) M = fmaxf(M, __ldcg(&p.part_ms[a + j]).x);
 #pragma unroll
@@ -170,23 +178,34 @@ __global__ void __launch_bounds__(128) merge_partials_kernel(const AttnParams p,
         const float w = (ms.x == -INFINITY) ? 0.f : ex2(ms.x - M);
         S += w * ms.y;
         const int cnt = min(32, n - j0);
-        for (int j = 0; j < cnt; ++j) {
-            const float wj = __shfl_sync(kFull, w, j);
-            const float* po = p.part_o + (size_t)(a + j0 + j) * D + lane * DPL;
-            if constexpr (DPL == 4) {
-                const float4 o = __ldcg(reinterpret_cast<const float4*>(po));
-                acc[0] += wj * o.x; acc[1] += wj * o.y; acc[2] += wj * o.z; acc[3] += wj * o.w;
-            } else {
-                const float2 o = __ldcg(reinterpret_cast<const float2*>(po));
-                acc[0] += wj * o.x; acc[1] += wj * o.y;
+        for (int j = 0; j < cnt; j += KB) {
+            // KB partial rows loaded at once (rows past cnt repeat the last
+            // valid one with weight 0), then accumulated.
+            float o[KB][DPL];
+            float wk[KB];
+#pragma unroll
+            for (int k = 0; k < KB; ++k) {
+                const int jj = min(j + k, cnt - 1);
+                wk[k] = (j + k < cnt) ? __shfl_sync(kFull, w, jj) : 0.f;
+                const float* po = p.part_o + (size_t)(a + j0 + jj) * D + lane * DPL;
+                if constexpr (DPL == 4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
+                    o[k][0] = v.x; o[k][1] = v.y; o[k][2] = v.z; o[k][3] = v.w;
+                } else {
+                    const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
+                    o[k][0] = v.x; o[k][1] = v.y;
+                }
             }
+#pragma unroll
+            for (int k = 0; k < KB; ++k)
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) acc[d] += wk[k] * o[k][d];
         }
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) S += __shfl_xor_sync(kFull, S, off);
     const float inv = 1.f / S;
-    const int pos = gw / p.n_heads, h = gw % p.n_heads;
-    uint16_t* dst = p.out + ((size_t)p.seq_perm[pos] * p.n_heads + h) * D + lane * DPL;
+    uint16_t* dst = p.out + ((size_t)row * p.n_heads + gw % p.n_heads) * D + lane * DPL;
     if constexpr (DPL == 4) {
         uint2 v;
         v.x = pack_half2(acc[0] * inv, acc[1] * inv);
@@ -675,7 +694,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
 // KV scatter for inserts: rows [first, n) of k/v [L][n][H][D] into the pool
 // chunk slots listed per chunk.  16-byte vectors, grid-stride.
 // ---------------------------------------------------------------------------
-constexpr int kScatterMaxChunks = 1024;
+constexpr int kScatterMaxChunks = 64;     // chunks per launch (keeps the parameter block small)
 struct ScatterArgs {
     const uint4* k;
     const uint4* v;
