@@ -212,15 +212,19 @@ def run_ours(args):
     host_split = {"remove": [], "insert": [], "schedule": []}
     if churn:
         # Draw every step's churn (ids, tokens) before timing.  Inserted rows
-        # come from device-resident N(0,1) fp16 blocks, so the timed step does
+        # come from device-resident N(0,1) fp16 blocks (one packed buffer per
+        # step, as a batched prefill would leave them), so the timed step does
         # only what a serving step does: remove, insert (trie + KV scatter),
         # reschedule, attend.  (Churn parity with the real generator is a GPU
         # test.)
         plan_churn = []
         for i in range(args.warmup + args.steps):
             removed, inserted = wl.churn_step()
-            plan_churn.append((removed, [(sid, wl.tokens(sid)) for sid in inserted], wl.seq_ids()))
-        nmax = max(len(t) for _, ins, _ in plan_churn for _, t in ins)
+            toks = [wl.tokens(sid) for sid in inserted]
+            plan_churn.append((np.array(removed, dtype=np.int64), np.array(inserted, dtype=np.int64),
+                               np.concatenate(toks), np.array([len(t) for t in toks], dtype=np.int32),
+                               wl.seq_ids()))
+        nmax = max(int(p[3].sum()) for p in plan_churn)
         g = torch.Generator(device=dev).manual_seed(wl.seed)
         kblk = torch.randn((L, nmax, H, D), generator=g, device=dev).half()
         vblk = torch.randn((L, nmax, H, D), generator=g, device=dev).half()
@@ -229,12 +233,11 @@ def run_ours(args):
         nonlocal sched, batch, ws
         if churn:
             th = time.perf_counter()
-            removed, inserted, live = plan_churn[i]
-            for sid in removed:
-                pool.remove(sid)
+            removed, inserted, toks, lens, live = plan_churn[i]
+            pool.remove_batch(removed)
             t1 = time.perf_counter()
-            for sid, toks in inserted:
-                pool.insert(sid, toks, kblk[:, :len(toks)], vblk[:, :len(toks)])
+            rows = int(lens.sum())
+            pool.insert_batch(inserted, toks, kblk[:, :rows], vblk[:, :rows], lengths=lens)
             t2 = time.perf_counter()
             batch = live
         sched = pool.schedule(batch, reuse=sched)

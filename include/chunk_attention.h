@@ -129,10 +129,30 @@ int ca_insert_tokens(ca_pool* pool, int64_t seq_id, const int32_t* tokens,
                      int32_t n, const void* k_dev, const void* v_dev,
                      void* stream, int32_t* n_shared_out);
 
+/* Insert several sequences at once (sequences joining in one iteration
+ * [CA §2.2]).  Equivalent to ca_insert_tokens for seq_ids[0], seq_ids[1], ...
+ * in order (a later sequence may share chunks an earlier one created), but
+ * with one call and one KV copy launch per 128 new chunks.
+ *   tokens   int32, the n_seqs token lists concatenated; lengths[i] >= 1
+ *   k_dev / v_dev  fp16 [n_layers][sum(lengths)][n_heads][head_dim]: the
+ *            rows of sequence i start at row lengths[0] + ... + lengths[i-1]
+ *            (a packed prefill output); rows of matched tokens are not read
+ *   n_shared_out   int32[n_seqs] or NULL
+ * All or nothing: on any error (CA_ERR_EXISTS, CA_ERR_OOM, CA_ERR_INVALID,
+ * CA_ERR_CUDA) the pool is left exactly as before the call. */
+int ca_insert_batch(ca_pool* pool, int32_t n_seqs, const int64_t* seq_ids,
+                    const int32_t* tokens, const int32_t* lengths,
+                    const void* k_dev, const void* v_dev, void* stream,
+                    int32_t* n_shared_out);
+
 /* Remove a finished sequence [CA §3.1: completed sequences remove their
  * path].  Every chunk on its path loses one reference; chunks left with none
  * return their slot to the free list [CA-blog, 動的プレフィックス検出]. */
 int ca_remove_seq(ca_pool* pool, int64_t seq_id);
+
+/* Remove n_seqs sequences; CA_ERR_NOT_FOUND (nothing removed) if any id is
+ * unknown, CA_ERR_INVALID if an id repeats. */
+int ca_remove_batch(ca_pool* pool, int32_t n_seqs, const int64_t* seq_ids);
 
 int ca_pool_stats(const ca_pool* pool, ca_stats* out);
 

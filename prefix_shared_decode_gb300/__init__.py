@@ -107,8 +107,39 @@ class Pool:
                                           C.byref(shared)), "ca_insert_tokens")
         return shared.value
 
+    def insert_batch(self, seq_ids, token_lists, k=None, v=None, stream=None, lengths=None) -> list[int]:
+        """Insert several sequences in one call; k, v are fp16 device tensors
+        [L, sum(lengths), H, D] holding the sequences' rows back to back (None
+        for a host-only pool).  All or nothing.  Returns the shared tokens.
+        ``token_lists`` is a list of token arrays, or (with ``lengths``) the
+        already concatenated tokens."""
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        if lengths is None:
+            lens = np.ascontiguousarray(np.array([len(t) for t in token_lists], dtype=np.int32))
+            tok = np.ascontiguousarray(np.concatenate([np.asarray(t, dtype=np.int32) for t in token_lists]))
+        else:
+            lens = np.ascontiguousarray(np.asarray(lengths, dtype=np.int32))
+            tok = np.ascontiguousarray(np.asarray(token_lists, dtype=np.int32))
+        kp = vp = None
+        if k is not None:
+            assert k.is_contiguous() and v.is_contiguous()
+            assert tuple(k.shape) == (self.n_layers, int(lens.sum()), self.n_heads, self.head_dim)
+            kp, vp = k.data_ptr(), v.data_ptr()
+        shared = np.zeros(len(ids), dtype=np.int32)
+        P32 = C.POINTER(C.c_int32)
+        check(capi.lib().ca_insert_batch(self._h, len(ids), ids.ctypes.data_as(C.POINTER(C.c_int64)),
+                                         tok.ctypes.data_as(P32), lens.ctypes.data_as(P32), kp, vp,
+                                         None if self.host_only else _stream_ptr(stream),
+                                         shared.ctypes.data_as(P32)), "ca_insert_batch")
+        return shared.tolist()
+
     def remove(self, seq_id: int) -> None:
         check(capi.lib().ca_remove_seq(self._h, int(seq_id)), "ca_remove_seq")
+
+    def remove_batch(self, seq_ids) -> None:
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        check(capi.lib().ca_remove_batch(self._h, len(ids), ids.ctypes.data_as(C.POINTER(C.c_int64))),
+              "ca_remove_batch")
 
     def stats(self) -> dict:
         s = capi.Stats()

@@ -78,11 +78,16 @@ struct WsLayout {
 // ---------------------------------------------------------------------------
 struct Node {
     int32_t slot = -1;
-    std::vector<int32_t> tokens;   // the chunk's token ids (ntok = size)
+    int32_t ntok = 0;              // tokens in the chunk (c, or fewer for a tail)
+    uint64_t hash = 0;             // full chunks: 64-bit hash of the token tuple
+    bool matchable = false;        // full chunk a later insert may match
     Node* parent = nullptr;
-    std::vector<Node*> children;   // insertion order
-    // full shareable chunks only, keyed by their token tuple
-    std::unordered_map<std::string, Node*> match;
+    std::vector<Node*> children;   // insertion order (capacity kept when reused)
+    // Hash index over the matchable children, built only once a node has many
+    // children (a linear scan of the stored hashes is cheaper below that).
+    // Should two different sibling tuples ever share a hash, the index keeps
+    // the first: sharing is lost for the other, results stay exact.
+    std::unique_ptr<std::unordered_map<uint64_t, Node*>> index;
     int32_t refcount = 0;
     int32_t mark = 0;              // scratch for schedule building: batch holders
     int32_t row = -1;              // scratch: chunk-first row while building
@@ -102,8 +107,9 @@ struct Pool {
     int device = -1;
     int num_sms = 0;
     alignas(64) unsigned char tmap[128];  // CUtensorMap over the pool
-    std::unique_ptr<Node> root;
-    std::vector<std::unique_ptr<Node>> nodes_by_slot;  // owner, indexed by slot
+    Node root;
+    std::vector<Node> nodes;       // one per slot, reused; live iff refcount > 0
+    std::vector<int32_t> tokens;   // [slot][c] token ids of each live chunk
     std::vector<int32_t> heap;     // min-heap of free slots
     std::unordered_map<int64_t, Sequence> seqs;
     int64_t generation = 0;
@@ -160,8 +166,13 @@ void layout_ws(const Plan& plan, const Pool& p, int32_t b, WsLayout& ws);
 int kernel_smem_bytes(int chunk, int head_dim, int* n_stages, size_t* bytes);
 int kernel_ctas_per_sm(int chunk, int head_dim, int* ctas);
 int make_tensor_map(Pool& p);
-int launch_scatter(const Pool& p, const void* k, const void* v, int32_t n,
-                   const std::vector<std::pair<int32_t, int32_t>>& new_chunks, void* stream);
+// One new chunk to fill: rows [src_row, src_row + n_rows) of a packed
+// [L][total_rows][H][D] source go to rows [0, n_rows) of `slot`.
+struct ScatterChunk {
+    int32_t src_row, n_rows, slot;
+};
+int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_rows,
+                   const std::vector<ScatterChunk>& chunks, void* stream);
 int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void* stream);
 
 }  // namespace ca

@@ -72,8 +72,8 @@ int ca_pool_create(const ca_pool_config* cfg, void* kv_dev, size_t kv_bytes, ca_
         p->cfg = *cfg;
         p->kv = kv_dev;
         p->kv_bytes = kv_bytes;
-        p->root.reset(new Node());
-        p->nodes_by_slot.resize(cfg->capacity_slots);
+        p->nodes.resize(cfg->capacity_slots);
+        p->tokens.assign((size_t)cfg->capacity_slots * cfg->chunk, 0);
         p->heap.resize(cfg->capacity_slots);
         for (int32_t i = 0; i < cfg->capacity_slots; ++i) p->heap[i] = i;   // sorted = min-heap
         if (kv_dev) {
@@ -107,28 +107,45 @@ int ca_match_prefix(const ca_pool* pool, const int32_t* tokens, int32_t n, int32
 
 int ca_insert_tokens(ca_pool* pool, int64_t seq_id, const int32_t* tokens, int32_t n,
                      const void* k_dev, const void* v_dev, void* stream, int32_t* n_shared_out) {
-    if (!pool || n <= 0 || !tokens) return CA_ERR_INVALID;
+    return ca_insert_batch(pool, 1, &seq_id, tokens, &n, k_dev, v_dev, stream, n_shared_out);
+}
+
+int ca_insert_batch(ca_pool* pool, int32_t n_seqs, const int64_t* seq_ids, const int32_t* tokens,
+                    const int32_t* lengths, const void* k_dev, const void* v_dev, void* stream,
+                    int32_t* n_shared_out) {
+    if (!pool || n_seqs < 1 || !seq_ids || !tokens || !lengths) return CA_ERR_INVALID;
+    int64_t total = 0;
+    for (int32_t i = 0; i < n_seqs; ++i) {
+        if (lengths[i] < 1) return CA_ERR_INVALID;
+        total += lengths[i];
+    }
+    if (total > INT32_MAX) return CA_ERR_INVALID;
     if (pool->kv) {
         if (!k_dev || !v_dev || !aligned(k_dev, 16) || !aligned(v_dev, 16)) return CA_ERR_INVALID;
     } else if (k_dev || v_dev) {
         return CA_ERR_INVALID;
     }
     return guard([&] {
-        std::vector<std::pair<int32_t, int32_t>> fresh;
-        int32_t shared = 0;
         const int64_t gen = pool->generation;
-        int st = pool_insert(*pool, seq_id, tokens, n, &fresh, &shared);
-        if (st) return st;
-        if (pool->kv) {
-            st = launch_scatter(*pool, k_dev, v_dev, n, fresh, stream);
-            if (st) {                       // undo: the pool must be unchanged
-                pool_remove(*pool, seq_id);
-                pool->generation = gen;
-                return st;
-            }
+        std::vector<std::pair<int32_t, int32_t>> fresh;
+        std::vector<ScatterChunk> copies;
+        int32_t row0 = 0, i = 0, st = CA_OK;
+        for (; i < n_seqs; ++i) {
+            fresh.clear();
+            int32_t shared = 0;
+            st = pool_insert(*pool, seq_ids[i], tokens + row0, lengths[i], &fresh, &shared);
+            if (st) break;
+            for (const auto& f : fresh)
+                copies.push_back({row0 + f.first, std::min(pool->cfg.chunk, lengths[i] - f.first), f.second});
+            if (n_shared_out) n_shared_out[i] = shared;
+            row0 += lengths[i];
         }
-        if (n_shared_out) *n_shared_out = shared;
-        return CA_OK;
+        if (!st && pool->kv) st = launch_scatter(*pool, k_dev, v_dev, (int32_t)total, copies, stream);
+        if (st) {                              // undo: the pool must be unchanged
+            for (int32_t j = (i < n_seqs ? i : n_seqs) - 1; j >= 0; --j) pool_remove(*pool, seq_ids[j]);
+            pool->generation = gen;
+        }
+        return st;
     });
 }
 
@@ -137,14 +154,26 @@ int ca_remove_seq(ca_pool* pool, int64_t seq_id) {
     return guard([&] { return pool_remove(*pool, seq_id); });
 }
 
+int ca_remove_batch(ca_pool* pool, int32_t n_seqs, const int64_t* seq_ids) {
+    if (!pool || n_seqs < 0 || (n_seqs > 0 && !seq_ids)) return CA_ERR_INVALID;
+    return guard([&] {
+        for (int32_t i = 0; i < n_seqs; ++i)
+            if (!pool->seqs.count(seq_ids[i])) return CA_ERR_NOT_FOUND;
+        std::vector<int64_t> sorted(seq_ids, seq_ids + n_seqs);
+        std::sort(sorted.begin(), sorted.end());
+        if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end()) return CA_ERR_INVALID;
+        for (int32_t i = 0; i < n_seqs; ++i) pool_remove(*pool, seq_ids[i]);
+        return CA_OK;
+    });
+}
+
 int ca_pool_stats(const ca_pool* pool, ca_stats* out) {
     if (!pool || !out) return CA_ERR_INVALID;
     return guard([&] {
         ca_stats s{};
         s.free_slots = (int64_t)pool->heap.size();
         s.live_slots = pool->cfg.capacity_slots - s.free_slots;
-        for (const auto& n : pool->nodes_by_slot)
-            if (n) s.refcount_sum += n->refcount;
+        for (const auto& n : pool->nodes) s.refcount_sum += n.refcount;
         s.live_seqs = (int64_t)pool->seqs.size();
         s.generation = pool->generation;
         *out = s;

@@ -28,6 +28,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 
@@ -691,36 +692,33 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
 }
 
 // ---------------------------------------------------------------------------
-// KV scatter for inserts: rows [first, n) of k/v [L][n][H][D] into the pool
-// chunk slots listed per chunk.  16-byte vectors, grid-stride.
+// KV scatter for inserts: each listed chunk copies rows [src_row, src_row +
+// n_rows) of k/v [L][total_rows][H][D] into rows [0, n_rows) of its slot's
+// K and V tiles.  One CTA per (chunk, layer); 16-byte vectors.
 // ---------------------------------------------------------------------------
-constexpr int kScatterMaxChunks = 64;     // chunks per launch (keeps the parameter block small)
+constexpr int kScatterMaxChunks = 128;    // chunks per launch (small parameter block)
 struct ScatterArgs {
     const uint4* k;
     const uint4* v;
     uint4* pool;
-    int32_t n, first_tok, n_tok, chunk, n_layers, n_heads, vec_per_row, first_chunk;
-    int32_t slots[kScatterMaxChunks];
+    int32_t total_rows, chunk, n_layers, n_heads, vec_per_row, n_chunks;
+    ScatterChunk ch[kScatterMaxChunks];
 };
 
-__global__ void kv_scatter_kernel(const __grid_constant__ ScatterArgs a) {
-    const long long total = (long long)a.n_layers * a.n_tok * a.n_heads * a.vec_per_row;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int vec = (int)(i % a.vec_per_row);
-        long long r = i / a.vec_per_row;
-        const int h = (int)(r % a.n_heads);
-        r /= a.n_heads;
-        const int t = a.first_tok + (int)(r % a.n_tok);
-        const int l = (int)(r / a.n_tok);
-        const int slot = a.slots[t / a.chunk - a.first_chunk];
-        const long long src = (((long long)l * a.n + t) * a.n_heads + h) * a.vec_per_row + vec;
-        const long long tile =
-            (((long long)slot * a.n_layers + l) * 2 * a.n_heads + h) * a.chunk + (t % a.chunk);
-        const long long dk = tile * a.vec_per_row + vec;
-        const long long dv = dk + (long long)a.n_heads * a.chunk * a.vec_per_row;
-        a.pool[dk] = a.k[src];
-        a.pool[dv] = a.v[src];
+__global__ void __launch_bounds__(256) kv_scatter_kernel(const __grid_constant__ ScatterArgs a) {
+    // one CTA per (chunk, layer, head): a c x D tile of K and one of V
+    const int h = blockIdx.x % a.n_heads;
+    const int rest = blockIdx.x / a.n_heads;
+    const int ci = rest % a.n_chunks, l = rest / a.n_chunks;
+    const ScatterChunk c = a.ch[ci];
+    const int total = c.n_rows * a.vec_per_row;
+    const long long tile = ((((long long)c.slot * a.n_layers + l) * 2 * a.n_heads + h) * a.chunk) * a.vec_per_row;
+    const long long vtile = tile + (long long)a.n_heads * a.chunk * a.vec_per_row;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const int r = i / a.vec_per_row, vec = i % a.vec_per_row;
+        const long long src = (((long long)l * a.total_rows + c.src_row + r) * a.n_heads + h) * a.vec_per_row + vec;
+        a.pool[tile + i] = a.k[src];
+        a.pool[vtile + i] = a.v[src];
     }
 }
 
@@ -805,34 +803,25 @@ int make_tensor_map(Pool& p) {
     return r == CUDA_SUCCESS ? CA_OK : CA_ERR_CUDA;
 }
 
-int launch_scatter(const Pool& p, const void* k, const void* v, int32_t n,
-                   const std::vector<std::pair<int32_t, int32_t>>& new_chunks, void* stream) {
-    if (new_chunks.empty()) return CA_OK;
+int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_rows,
+                   const std::vector<ScatterChunk>& chunks, void* stream) {
     const ca_pool_config& c = p.cfg;
-    size_t i = 0;
-    while (i < new_chunks.size()) {
-        const size_t cnt = std::min<size_t>(dev::kScatterMaxChunks, new_chunks.size() - i);
+    for (size_t i = 0; i < chunks.size(); i += dev::kScatterMaxChunks) {
+        const size_t cnt = std::min<size_t>(dev::kScatterMaxChunks, chunks.size() - i);
         dev::ScatterArgs a;
-        std::memset(&a, 0, sizeof(a));
         a.k = static_cast<const uint4*>(k);
         a.v = static_cast<const uint4*>(v);
         a.pool = static_cast<uint4*>(p.kv);
-        a.n = n;
+        a.total_rows = total_rows;
         a.chunk = c.chunk;
         a.n_layers = c.n_layers;
         a.n_heads = c.n_heads;
         a.vec_per_row = c.head_dim / 8;
-        a.first_tok = new_chunks[i].first;
-        const int32_t end_tok = (i + cnt < new_chunks.size()) ? new_chunks[i + cnt].first : n;
-        a.n_tok = end_tok - a.first_tok;
-        a.first_chunk = new_chunks[i].first / c.chunk;
-        for (size_t j = 0; j < cnt; ++j) a.slots[j] = new_chunks[i + j].second;
-        const long long total = (long long)c.n_layers * a.n_tok * c.n_heads * a.vec_per_row;
-        long long blocks = (total + 255) / 256;
-        if (blocks > 4096) blocks = 4096;
-        dev::kv_scatter_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+        a.n_chunks = (int32_t)cnt;
+        std::copy(chunks.begin() + i, chunks.begin() + i + cnt, a.ch);
+        const unsigned blocks = (unsigned)(cnt * c.n_layers * c.n_heads);
+        dev::kv_scatter_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
         if (cudaGetLastError() != cudaSuccess) return CA_ERR_CUDA;
-        i += cnt;
     }
     return CA_OK;
 }

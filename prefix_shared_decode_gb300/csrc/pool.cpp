@@ -15,15 +15,60 @@
 //  * children keep insertion order (the schedule walks them in that order).
 #include <algorithm>
 #include <functional>
-#include <string>
 
 #include "ca_internal.h"
 
 namespace ca {
 namespace {
 
-std::string chunk_key(const int32_t* tokens, int32_t c) {
-    return std::string(reinterpret_cast<const char*>(tokens), sizeof(int32_t) * (size_t)c);
+// 64-bit hash of a chunk's token tuple (multiply-xorshift per token).
+uint64_t chunk_hash(const int32_t* tokens, int32_t c) {
+    uint64_t h = 0x6a09e667f3bcc909ull ^ (uint64_t)c;
+    for (int32_t i = 0; i < c; ++i) {
+        h ^= (uint64_t)(uint32_t)tokens[i];
+        h *= 0x9e3779b97f4a7c15ull;
+        h ^= h >> 31;
+    }
+    return h;
+}
+
+constexpr size_t kIndexAbove = 32;   // children before a node gets a hash index
+
+const int32_t* chunk_tokens(const Pool& p, const Node* n) {
+    return p.tokens.data() + (size_t)n->slot * p.cfg.chunk;
+}
+
+Node* find_child(const Pool& p, const Node* node, const int32_t* tokens, int32_t c, uint64_t h) {
+    if (node->index) {
+        auto it = node->index->find(h);
+        if (it == node->index->end()) return nullptr;
+        Node* ch = it->second;
+        return std::equal(tokens, tokens + c, chunk_tokens(p, ch)) ? ch : nullptr;
+    }
+    for (Node* ch : node->children)
+        if (ch->matchable && ch->hash == h && std::equal(tokens, tokens + c, chunk_tokens(p, ch)))
+            return ch;
+    return nullptr;
+}
+
+void add_child(Node* node, Node* ch) {
+    node->children.push_back(ch);
+    if (node->index) {
+        if (ch->matchable) node->index->emplace(ch->hash, ch);
+    } else if (node->children.size() > kIndexAbove) {
+        node->index.reset(new std::unordered_map<uint64_t, Node*>());
+        for (Node* x : node->children)
+            if (x->matchable) node->index->emplace(x->hash, x);
+    }
+}
+
+void drop_child(Node* node, Node* ch) {
+    auto& v = node->children;
+    v.erase(std::find(v.begin(), v.end(), ch));
+    if (node->index && ch->matchable) {
+        auto it = node->index->find(ch->hash);
+        if (it != node->index->end() && it->second == ch) node->index->erase(it);
+    }
 }
 
 int32_t heap_pop(std::vector<int32_t>& h) {
@@ -38,26 +83,26 @@ void heap_push(std::vector<int32_t>& h, int32_t s) {
     std::push_heap(h.begin(), h.end(), std::greater<int32_t>());
 }
 
-int32_t count_matched(const Pool& p, const int32_t* tokens, int32_t n, const Node** last) {
+// Walk the matched full-chunk prefix; returns the matched nodes.
+void walk_matched(const Pool& p, const int32_t* tokens, int32_t n, std::vector<Node*>& out) {
+    out.clear();
+    if (p.cfg.flags & CA_NO_SHARING) return;
     const int32_t c = p.cfg.chunk;
-    const Node* node = p.root.get();
-    int32_t matched = 0;
-    if (!(p.cfg.flags & CA_NO_SHARING)) {
-        for (int32_t i = 0; i < n / c; ++i) {
-            auto it = node->match.find(chunk_key(tokens + (size_t)i * c, c));
-            if (it == node->match.end()) break;
-            node = it->second;
-            ++matched;
-        }
+    const Node* node = &p.root;
+    for (int32_t i = 0; i < n / c; ++i) {
+        Node* ch = find_child(p, node, tokens + (size_t)i * c, c, chunk_hash(tokens + (size_t)i * c, c));
+        if (!ch) break;
+        out.push_back(ch);
+        node = ch;
     }
-    if (last) *last = node;
-    return matched;
 }
 
 }  // namespace
 
 int32_t pool_match(const Pool& p, const int32_t* tokens, int32_t n) {
-    return count_matched(p, tokens, n, nullptr) * p.cfg.chunk;
+    std::vector<Node*> path;
+    walk_matched(p, tokens, n, path);
+    return (int32_t)path.size() * p.cfg.chunk;
 }
 
 int pool_insert(Pool& p, int64_t seq_id, const int32_t* tokens, int32_t n,
@@ -66,34 +111,34 @@ int pool_insert(Pool& p, int64_t seq_id, const int32_t* tokens, int32_t n,
     if (p.seqs.count(seq_id)) return CA_ERR_EXISTS;
     const int32_t c = p.cfg.chunk;
     const int32_t pieces = (n + c - 1) / c;
-    const Node* last = nullptr;
-    const int32_t matched = count_matched(p, tokens, n, &last);
+    Sequence seq;
+    seq.length = n;
+    walk_matched(p, tokens, n, seq.path);
+    const int32_t matched = (int32_t)seq.path.size();
     const int32_t n_new = pieces - matched;
     if ((size_t)n_new > p.heap.size()) return CA_ERR_OOM;
 
-    Sequence seq;
-    seq.length = n;
     seq.path.reserve(pieces);
-    Node* node = p.root.get();
-    for (int32_t i = 0; i < pieces; ++i) {
+    for (Node* m : seq.path) m->refcount += 1;
+    Node* node = matched ? seq.path.back() : &p.root;
+    const bool share = !(p.cfg.flags & CA_NO_SHARING);
+    for (int32_t i = matched; i < pieces; ++i) {
         const int32_t a = i * c, len = std::min(c, n - a);
-        if (i < matched) {
-            node = node->match.find(chunk_key(tokens + a, c))->second;
-        } else {
-            const int32_t slot = heap_pop(p.heap);
-            std::unique_ptr<Node> ch(new Node());
-            ch->slot = slot;
-            ch->tokens.assign(tokens + a, tokens + a + len);
-            ch->parent = node;
-            node->children.push_back(ch.get());
-            if (len == c && !(p.cfg.flags & CA_NO_SHARING))
-                node->match.emplace(chunk_key(tokens + a, c), ch.get());
-            node = ch.get();
-            p.nodes_by_slot[slot] = std::move(ch);
-            if (new_chunks) new_chunks->emplace_back(a, slot);
-        }
-        node->refcount += 1;
+        const int32_t slot = heap_pop(p.heap);
+        Node* ch = &p.nodes[slot];
+        ch->slot = slot;
+        ch->ntok = len;
+        std::copy(tokens + a, tokens + a + len, p.tokens.begin() + (size_t)slot * c);
+        ch->matchable = share && len == c;
+        ch->hash = ch->matchable ? chunk_hash(tokens + a, c) : 0;
+        ch->parent = node;
+        ch->children.clear();
+        ch->index.reset();
+        ch->refcount = 1;
+        add_child(node, ch);
+        node = ch;
         seq.path.push_back(node);
+        if (new_chunks) new_chunks->emplace_back(a, slot);
     }
     p.seqs.emplace(seq_id, std::move(seq));
     p.generation += 1;
@@ -115,17 +160,14 @@ int pool_remove(Pool& p, int64_t seq_id) {
     }
     if (first_free < path.size()) {
         Node* top = path[first_free];
-        Node* parent = top->parent;
-        auto& ch = parent->children;
-        ch.erase(std::find(ch.begin(), ch.end(), top));
-        if (top->tokens.size() == (size_t)p.cfg.chunk) {
-            auto m = parent->match.find(chunk_key(top->tokens.data(), p.cfg.chunk));
-            if (m != parent->match.end() && m->second == top) parent->match.erase(m);
-        }
+        drop_child(top->parent, top);
         for (size_t i = first_free; i < path.size(); ++i) {
-            const int32_t slot = path[i]->slot;
-            heap_push(p.heap, slot);
-            p.nodes_by_slot[slot].reset();
+            Node* x = path[i];
+            heap_push(p.heap, x->slot);
+            x->children.clear();
+            x->index.reset();
+            x->parent = nullptr;
+            x->matchable = false;
         }
     }
     p.generation += 1;

@@ -65,16 +65,16 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
     std::vector<const Node*> row_node;
     struct Frame { const Node* node; size_t next; };
     std::vector<Frame> stack;
-    stack.push_back({p.root.get(), 0});
+    stack.push_back({&p.root, 0});
     while (!stack.empty()) {
         Frame& f = stack.back();
         const Node* node = f.node;
-        if (f.next == 0 && node != p.root.get()) {
+        if (f.next == 0 && node != &p.root) {
             if (tpp && node->mark >= 2) {
                 const_cast<Node*>(node)->row = (int32_t)row_node.size();
                 row_node.push_back(node);
                 t.cf_rows.insert(t.cf_rows.end(),
-                                 {node->slot, (int32_t)node->tokens.size(), (int32_t)order.size(), -1});
+                                 {node->slot, node->ntok, (int32_t)order.size(), -1});
             }
             for (int32_t k = 0; k < node->end_count; ++k) order.push_back(ends[node->end_begin + k].second);
         }
@@ -118,7 +118,7 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
     t.sf_offsets.assign(1, 0);
     for (int32_t pos = 0; pos < b; ++pos) {
         for (const Node* n : seq_at[pos]->path)
-            if (!tpp || n->mark == 1) t.sf_chunks.insert(t.sf_chunks.end(), {n->slot, (int32_t)n->tokens.size()});
+            if (!tpp || n->mark == 1) t.sf_chunks.insert(t.sf_chunks.end(), {n->slot, n->ntok});
         t.sf_offsets.push_back((int32_t)(t.sf_chunks.size() / 2));
     }
 

@@ -180,3 +180,46 @@ def test_remove_all_frees_everything(lib):
     # the allocator restarts from slot 0
     pool.insert(99, list(range(33)))
     assert pool.seq_slots(99) == [0, 1, 2]
+
+
+def test_insert_batch_equals_sequential_inserts(lib):
+    from prefix_shared_decode_gb300 import Pool
+    seqs = random_segment_sequences(21, 12, 16)
+    one, many = Pool(1, 2, 64, 16, 400, host_only=True), Pool(1, 2, 64, 16, 400, host_only=True)
+    want = [one.insert(100 + i, t) for i, t in enumerate(seqs)]
+    got = many.insert_batch([100 + i for i in range(12)], seqs)
+    assert got == want
+    for i in range(12):
+        assert many.seq_slots(100 + i) == one.seq_slots(100 + i)
+    assert many.stats() == one.stats()
+    many.remove_batch([100, 105, 107])
+    for s in (100, 105, 107):
+        one.remove(s)
+    assert many.stats() == one.stats()
+
+
+def test_insert_batch_is_all_or_nothing(lib):
+    from prefix_shared_decode_gb300 import CAError, Pool
+    pool = Pool(1, 2, 64, 16, 10, host_only=True)
+    pool.insert(1, list(range(40)))                       # 3 slots
+    before = pool.stats()
+    slots1 = pool.seq_slots(1)
+    # second entry collides with an existing id
+    with pytest.raises(CAError) as e:
+        pool.insert_batch([2, 1], [list(range(20)), [7]])
+    assert e.value.name == "CA_ERR_EXISTS"
+    assert pool.stats() == before and pool.seq_slots(1) == slots1
+    # the third entry runs out of slots after two succeeded
+    with pytest.raises(CAError) as e:
+        pool.insert_batch([3, 4, 5], [list(range(16)) + [500] * 20, [900] * 40, [901] * 100])
+    assert e.value.name == "CA_ERR_OOM"
+    assert pool.stats() == before
+    with pytest.raises(CAError) as e:
+        pool.remove_batch([1, 42])
+    assert e.value.name == "CA_ERR_NOT_FOUND"
+    assert pool.stats() == before
+    with pytest.raises(CAError) as e:
+        pool.remove_batch([1, 1])
+    assert e.value.name == "CA_ERR_INVALID"
+    # a later sequence of the batch shares chunks an earlier one created
+    assert pool.insert_batch([6, 7], [[3] * 33, [3] * 40]) == [0, 32]

@@ -184,6 +184,31 @@ def test_kv_scatter_round_trip(torch_cuda):
     np.testing.assert_array_equal(kv[s1, 0, 0, :, :5], k2[0, 32:37].transpose(1, 0, 2))
 
 
+def test_insert_batch_packed_rows(torch_cuda):
+    """ca_insert_batch copies each sequence's rows out of one packed K/V
+    buffer; attention over the result matches the oracle."""
+    from prefix_shared_decode_gb300 import Pool
+    torch = torch_cuda
+    c, H, D, L = 32, 4, 128, 2
+    rng = np.random.default_rng(14)
+    seqs = random_segment_sequences(14, 9, c, n_segments=6)
+    total = sum(len(t) for t in seqs)
+    k = rng.standard_normal((L, total, H, D), dtype=np.float32).astype(np.float16)
+    v = rng.standard_normal((L, total, H, D), dtype=np.float32).astype(np.float16)
+    pool = Pool(L, H, D, c, 300)
+    trie = OracleTrie(c, 300)
+    shared = pool.insert_batch(list(range(9)), seqs, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+    row = 0
+    for i, t in enumerate(seqs):
+        assert trie.insert(i, t, k[:, row:row + len(t)], v[:, row:row + len(t)]) == shared[i]
+        row += len(t)
+    batch = [8, 3, 0, 5, 1]
+    q = rng.standard_normal((5, H, D), dtype=np.float32).astype(np.float16)
+    for layer in (0, 1):
+        got, _ = run(torch, pool, batch, q, layer=layer)
+        assert_close(got, A.decode_attention(trie, batch, layer, q, 1 / np.sqrt(D)), f"layer {layer}")
+
+
 def test_host_io_entry_and_repeat_calls(torch_cuda):
     from prefix_shared_decode_gb300 import decode_attention, decode_attention_host
     torch = torch_cuda
