@@ -194,12 +194,17 @@ int ca_export_tables(const ca_sched* sched, int32_t* seq_perm, int32_t* cf_rows,
 /* The kernel work plan derived from the tables (inspection and tests).
  * counts[0..3] = n_units, grid (CTAs), n_pbase (= b * n_heads + 1),
  * n_chunks.  Any array may be NULL.  Layouts (int32):
- *   units[n_units][8]  (kind 0 = chunk-first / 1 = sequence-first, head,
- *                       pos_lo, pos_hi, chunk_begin, chunk_end, part, 0)
+ *   units[n_units][12] (kind, head, pos_lo, pos_hi, begin, end, part, qrow,
+ *                       n_per_head, base, part_next, 0).  Chunk-first (kind 0):
+ *                       chunks [begin, end) of the list for one head and
+ *                       positions [pos_lo, pos_hi).  Sequence-first (kind 1):
+ *                       position pos_lo's (head, chunk) pairs with linear
+ *                       index h * n_per_head + j in [begin, end), chunk j at
+ *                       list index base + j; its first head uses partial
+ *                       index `part`, later heads `part_next`.
  *   cta_begin[grid+1]  unit range of each CTA
  *   pbase[n_pbase]     partial ids of (position p, head h) are
- *                      [pbase[p*H+h], pbase[p*H+h+1]); a unit writes id
- *                      pbase[p*H+h] + part for each position it covers
+ *                      [pbase[p*H+h], pbase[p*H+h+1])
  *   chunks[n_chunks][2] (slot, ntok) list the units index into */
 int ca_export_plan(const ca_sched* sched, int32_t counts[4], int32_t* units,
                    int32_t* cta_begin, int32_t* pbase, int32_t* chunks);

@@ -212,7 +212,7 @@ class Schedule:
         L = capi.lib()
         check(L.ca_export_plan(self._h, cnt, None, None, None, None), "ca_export_plan")
         n_units, grid, n_pbase, n_chunks = list(cnt)
-        out = {"units": np.zeros((n_units, 8), np.int32), "cta_begin": np.zeros(grid + 1, np.int32),
+        out = {"units": np.zeros((n_units, 12), np.int32), "cta_begin": np.zeros(grid + 1, np.int32),
                "pbase": np.zeros(n_pbase, np.int32), "chunks": np.zeros((n_chunks, 2), np.int32)}
         ptr = lambda a: a.ctypes.data_as(C.POINTER(C.c_int32))
         check(L.ca_export_plan(self._h, cnt, ptr(out["units"]), ptr(out["cta_begin"]),

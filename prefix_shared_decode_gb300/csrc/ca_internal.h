@@ -18,14 +18,18 @@ namespace ca {
 // ---------------------------------------------------------------------------
 // Work plan read by the attention kernel (uploaded to the device as one blob).
 //
-// A unit is one stretch of chunks that one CTA streams for one head:
+// A unit is one stretch of chunk-heads that one CTA streams:
 //  * UNIT_CF (chunk-first): rows [c_begin, c_end) of one run of chunks shared
-//    by batch positions [q_lo, q_hi) (at most 64 of them), all against the
-//    batched queries of those positions [ChunkAttention §3.2: the queries of
-//    the sequences that share a chunk form a matrix for tensor-core matmul].
-//  * UNIT_SF (sequence-first): some of position q_lo's own chunks.
-// Every unit leaves one partial triple (o, m, s) per covered position; the
-// partials of (position p, head h) occupy ids [pbase[p*H+h], pbase[p*H+h+1]).
+//    by batch positions [q_lo, q_hi) (at most 64 of them), for one head,
+//    against the batched queries of those positions [ChunkAttention §3.2:
+//    the queries of the sequences that share a chunk form a matrix for
+//    tensor-core matmul].
+//  * UNIT_SF (sequence-first): a contiguous range [c_begin, c_end) of position
+//    q_lo's own (head, chunk) pairs in the order h * n_per_head + j, i.e. the
+//    tail of one head's chunks, whole heads, and the start of another.
+// Every unit leaves one partial triple (o, m, s) per covered (position,
+// head); the partials of (position p, head h) occupy ids
+// [pbase[p*H+h], pbase[p*H+h+1]).
 // ---------------------------------------------------------------------------
 enum : int32_t { UNIT_CF = 0, UNIT_SF = 1 };
 
@@ -36,14 +40,19 @@ struct ChunkRef {      // one chunk the kernel reads
 
 struct Unit {
     int32_t kind;      // UNIT_CF or UNIT_SF
-    int32_t head;
+    int32_t head;      // CF: the head; SF: first head (c_begin / n_per_head)
     int32_t q_lo;      // first batch position
     int32_t q_hi;      // one past the last batch position
-    int32_t c_begin;   // chunk range in the ChunkRef list
+    int32_t c_begin;   // CF: chunk rows in the ChunkRef list; SF: linear (head, chunk) range
     int32_t c_end;
-    int32_t part;      // partial index within each covered (position, head)
-    int32_t qrow;      // UNIT_SF: row of q / out of its position (seq_perm[q_lo])
+    int32_t part;      // partial index within the first covered (position, head)
+    int32_t qrow;      // SF: row of q / out of its position (seq_perm[q_lo])
+    int32_t n_per_head;  // SF: chunks of the position per head
+    int32_t base;      // SF: ChunkRef index of the position's first chunk
+    int32_t part_next; // SF: partial index within the (position, head)s after the first
+    int32_t pad;
 };
+constexpr int kUnitInts = (int)(sizeof(Unit) / sizeof(int32_t));
 
 // Offsets (in bytes) of the arrays inside the device plan blob.
 struct PlanLayout {
@@ -128,6 +137,8 @@ struct Plan {
     std::vector<int32_t> pbase;
     int32_t grid = 0;
     int64_t n_partials = 0;
+    // scratch kept across rebuilds so that a rebuild allocates nothing new
+    std::vector<std::pair<int32_t, Unit>> tagged;
 };
 
 struct Sched {
@@ -136,6 +147,7 @@ struct Sched {
     uint32_t flags = 0;
     std::vector<int64_t> seq_ids;
     Tables t;
+    Tables t_next;                     // rebuilt into, then swapped with t
     Plan plan;
     PlanLayout layout{};
     WsLayout ws{};

@@ -199,18 +199,17 @@ int ca_build_schedule(ca_pool* pool, const int64_t* seq_ids, int32_t b, uint32_t
         if (s && s->pool == pool && s->generation == pool->generation && s->flags == flags &&
             (int32_t)s->seq_ids.size() == b && std::equal(seq_ids, seq_ids + b, s->seq_ids.begin()))
             return CA_OK;                   // context unchanged since the tree last changed
-        Tables t;
-        int st = build_tables(*pool, seq_ids, b, flags, t);
-        if (st) return st;
         std::unique_ptr<ca_sched> fresh;
         if (!s) {
             fresh.reset(new ca_sched());
             s = fresh.get();
         }
+        int st = build_tables(*pool, seq_ids, b, flags, s->t_next);
+        if (st) return st;                  // s (if reused) keeps its previous tables
+        std::swap(s->t, s->t_next);
         s->pool = pool;
         s->flags = flags;
         s->seq_ids.assign(seq_ids, seq_ids + b);
-        s->t = std::move(t);
         build_plan(*pool, s->t, pool->kv ? pool->num_sms : kHostOnlyGrid, s->plan);
         layout_plan(s->plan, b, s->layout, s->blob, s->t);
         layout_ws(s->plan, *pool, b, s->ws);
@@ -279,7 +278,7 @@ int ca_export_plan(const ca_sched* s, int32_t counts[4], int32_t* units, int32_t
     counts[1] = s->plan.grid;
     counts[2] = (int32_t)s->plan.pbase.size();
     counts[3] = (int32_t)s->plan.chunks.size();
-    static_assert(sizeof(Unit) == 8 * sizeof(int32_t), "Unit is 8 int32");
+    static_assert(sizeof(Unit) == 12 * sizeof(int32_t), "Unit is 12 int32");
     static_assert(sizeof(ChunkRef) == 2 * sizeof(int32_t), "ChunkRef is 2 int32");
     if (units && !s->plan.units.empty())
         std::memcpy(units, s->plan.units.data(), s->plan.units.size() * sizeof(Unit));

@@ -443,17 +443,26 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
         // The plan was uploaded before any kernel that precedes this one in
         // the stream, so it may be read before the dependency wait; the pool
         // and the queries only after it.
+        auto first_chunk = [&](const Unit& X) {
+            return X.kind == UNIT_SF ? X.base + X.c_begin % X.n_per_head : X.c_begin;
+        };
         Unit Un = (u_begin < u_end) ? p.units[u_begin] : Unit{};
         // chunk references run one ahead of the copies they describe
-        ChunkRef chn = (u_begin < u_end) ? p.chunks[Un.c_begin] : ChunkRef{0, 0};
+        ChunkRef chn = (u_begin < u_end) ? p.chunks[first_chunk(Un)] : ChunkRef{0, 0};
         asm volatile("griddepcontrol.wait;" ::: "memory");
         for (int u = u_begin; u < u_end && ok; ++u) {
             const Unit U = Un;
             if (u + 1 < u_end) Un = p.units[u + 1];
-            for (int c = U.c_begin; c < U.c_end; ++c, ++it) {
+            const bool sf = U.kind == UNIT_SF;
+            const int n = sf ? U.n_per_head : 1;
+            int h = sf ? U.c_begin / n : U.head;
+            int j = sf ? U.c_begin - h * n : 0;
+            for (int L = U.c_begin; L < U.c_end; ++L, ++it) {
                 const ChunkRef ch = chn;
-                if (c + 1 < U.c_end) chn = p.chunks[c + 1];
-                else if (u + 1 < u_end) chn = p.chunks[Un.c_begin];
+                const int head = h;
+                if (sf && ++j == n) { j = 0; ++h; }
+                if (L + 1 < U.c_end) chn = p.chunks[sf ? U.base + j : L + 1];
+                else if (u + 1 < u_end) chn = p.chunks[first_chunk(Un)];
                 const int st = it % S;
                 const uint32_t ph = (uint32_t)(it / S) & 1u;
                 if (!mbar_wait(empty0 + 8 * st, ph ^ 1u)) {
@@ -462,14 +471,14 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     break;
                 }
                 const uint32_t fb = full0 + 8 * st;
-                if (ch.slot < 0 || ch.slot >= p.capacity || U.head < 0 || U.head >= H) {
+                if (ch.slot < 0 || ch.slot >= p.capacity || head < 0 || head >= H) {
                     set_status(p.status, CA_ERR_DEVICE_BOUNDS);
                     mbar_arrive(fb);          // release the consumers without data
                     continue;
                 }
                 mbar_expect_tx(fb, SM::kStage);
                 const uint32_t dst = smem_u32(stages + (size_t)st * SM::kStage);
-                const int rowK = (((ch.slot * p.n_layers + p.layer) * 2 + 0) * H + U.head) * C;
+                const int rowK = (((ch.slot * p.n_layers + p.layer) * 2 + 0) * H + head) * C;
                 const int rowV = rowK + H * C;
 #pragma unroll
                 for (int bx = 0; bx < BOXES; ++bx) {
@@ -490,89 +499,116 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
     // ------------------------------ consumers --------------------------------
     const int w = warp;
     int it = 0;
-    // Descriptors run two units ahead and a sequence-first unit's query row
-    // one unit ahead, so no unit starts on a dependent global load.
-    auto load_q = [&](const Unit& X) -> uint2 {
-        const uint16_t* qp = p.q + ((size_t)X.qrow * H + X.head) * D + lane * DPL;
+    // Unit descriptors are held lane-distributed (lane i keeps field i) and
+    // run two units ahead; query rows of sequence-first heads are fetched one
+    // head ahead, so no unit or head starts on a dependent global load.
+    enum { F_KIND = 0, F_HEAD, F_QLO, F_QHI, F_CB, F_CE, F_PART, F_QROW, F_N, F_BASE, F_PNEXT };
+    auto load_desc = [&](int u) -> int32_t {
+        return lane < kUnitInts ? reinterpret_cast<const int32_t*>(p.units + u)[lane] : 0;
+    };
+    auto fld = [&](int32_t d, int i) -> int32_t { return __shfl_sync(kFull, d, i); };
+    auto load_q = [&](int qrow, int head) -> uint2 {
+        const uint16_t* qp = p.q + ((size_t)qrow * H + head) * D + lane * DPL;
         if constexpr (DPL == 4) return *reinterpret_cast<const uint2*>(qp);
         else return make_uint2(*reinterpret_cast<const uint32_t*>(qp), 0u);
     };
-    Unit U0{}, U1{};
-    uint2 qn = make_uint2(0u, 0u);
-    if (u_begin < u_end) U0 = p.units[u_begin];
-    if (u_begin + 1 < u_end) U1 = p.units[u_begin + 1];
+    uint2 qn = make_uint2(0u, 0u);        // prefetched query row ...
+    int qn_row = -1, qn_head = -1;        // ... and which (row, head) it is
+    auto prefetch_q = [&](int qrow, int head) {
+        qn = load_q(qrow, head);
+        qn_row = qrow;
+        qn_head = head;
+    };
+    auto take_q = [&](int qrow, int head) -> uint2 {
+        return (qrow == qn_row && head == qn_head) ? qn : load_q(qrow, head);
+    };
+    int32_t d0 = 0, d1 = 0;
+    if (u_begin < u_end) d0 = load_desc(u_begin);
+    if (u_begin + 1 < u_end) d1 = load_desc(u_begin + 1);
     asm volatile("griddepcontrol.wait;" ::: "memory");     // q and the pool after this
-    if (u_begin < u_end && U0.kind == UNIT_SF) qn = load_q(U0);
+    if (u_begin < u_end && fld(d0, F_KIND) == UNIT_SF) prefetch_q(fld(d0, F_QROW), fld(d0, F_HEAD));
+    int flush = 0;                        // sequence-first partials written (exchange parity)
     for (int u = u_begin; u < u_end; ++u) {
-        const Unit U = U0;
-        const uint2 qraw = qn;
-        U0 = U1;
-        if (u + 2 < u_end) U1 = p.units[u + 2];
-        if (u + 1 < u_end && U0.kind == UNIT_SF) qn = load_q(U0);
-        const int h = U.head;
+        const int32_t dc = d0;
+        d0 = d1;
+        if (u + 2 < u_end) d1 = load_desc(u + 2);
+        const bool next_sf = (u + 1 < u_end) && fld(d0, F_KIND) == UNIT_SF;
         consumer_sync();   // previous unit (and its exchange reads) finished
-        if (U.kind == UNIT_SF) {
-            const int pos = U.q_lo;
-            float q[DPL], o[DPL], m = -INFINITY, s = 0.f;
-            {
-                const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&qraw.x));
-                q[0] = a.x; q[1] = a.y;
-                if constexpr (DPL == 4) {
-                    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&qraw.y));
-                    q[2] = b.x; q[3] = b.y;
+        if (fld(dc, F_KIND) == UNIT_SF) {
+            const int pos = fld(dc, F_QLO), n = fld(dc, F_N), base = fld(dc, F_BASE);
+            const int qrow = fld(dc, F_QROW), c_end = fld(dc, F_CE), part_next = fld(dc, F_PNEXT);
+            int L = fld(dc, F_CB), h = fld(dc, F_HEAD), part = fld(dc, F_PART);
+            while (L < c_end) {                   // one head's piece at a time
+                const int seg_end = min(c_end, (h + 1) * n);
+                const uint2 qraw = take_q(qrow, h);
+                if (seg_end < c_end) prefetch_q(qrow, h + 1);
+                else if (next_sf) prefetch_q(fld(d0, F_QROW), fld(d0, F_HEAD));
+                float q[DPL], o[DPL], m = -INFINITY, s = 0.f;
+                {
+                    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&qraw.x));
+                    q[0] = a.x; q[1] = a.y;
+                    if constexpr (DPL == 4) {
+                        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&qraw.y));
+                        q[2] = b.x; q[3] = b.y;
+                    }
+#pragma unroll
+                    for (int d = 0; d < DPL; ++d) { q[d] *= p.scale_log2; o[d] = 0.f; }
                 }
-#pragma unroll
-                for (int d = 0; d < DPL; ++d) { q[d] *= p.scale_log2; o[d] = 0.f; }
-            }
-            for (int c = U.c_begin; c < U.c_end; ++c, ++it) {
-                const int st = it % S;
-                if (!mbar_wait(full0 + 8 * st, (uint32_t)(it / S) & 1u)) {
-                    set_status(p.status, CA_ERR_TIMEOUT);
-                    return;
+                for (int j = L - h * n; L < seg_end; ++L, ++j, ++it) {
+                    const int st = it % S;
+                    if (!mbar_wait(full0 + 8 * st, (uint32_t)(it / S) & 1u)) {
+                        set_status(p.status, CA_ERR_TIMEOUT);
+                        return;
+                    }
+                    const int ntok = min(max(p.chunks[base + j].ntok, 0), C);
+                    const uint8_t* kt = stages + (size_t)st * SM::kStage;
+                    sf_chunk<C, D>(kt, kt + SM::kTile, ntok, q, m, s, o, w, lane);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty0 + 8 * st);
                 }
-                const int ntok = min(max(p.chunks[c].ntok, 0), C);
-                const uint8_t* kt = stages + (size_t)st * SM::kStage;
-                sf_chunk<C, D>(kt, kt + SM::kTile, ntok, q, m, s, o, w, lane);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty0 + 8 * st);
-            }
-            // Combine the four warps' states, write the partial.
-            float* xo = reinterpret_cast<float*>(qreg);          // [4][D]
-            xo[w * D + lane * DPL + 0] = o[0];
-            xo[w * D + lane * DPL + 1] = o[1];
-            if constexpr (DPL == 4) {
-                xo[w * D + lane * DPL + 2] = o[2];
-                xo[w * D + lane * DPL + 3] = o[3];
-            }
-            if (lane == 0) { xms[2 * w] = m; xms[2 * w + 1] = s; }
-            consumer_sync();
-            if (w == 0) {
-                float M = -INFINITY;
+                // Combine the four warps' states and write the partial.  The
+                // exchange area alternates between two halves, so the next
+                // head's writes never meet this head's reads.
+                float* xo = reinterpret_cast<float*>(qreg) + (flush & 1) * kConsumerWarps * D;
+                float* xm = xms + (flush & 1) * 2 * kConsumerWarps;
 #pragma unroll
-                for (int v = 0; v < kConsumerWarps; ++v) M = fmaxf(M, xms[2 * v]);
-                float acc[DPL], sum = 0.f;
+                for (int d = 0; d < DPL; ++d) xo[w * D + lane * DPL + d] = o[d];
+                if (lane == 0) { xm[2 * w] = m; xm[2 * w + 1] = s; }
+                consumer_sync();
+                if (w == 0) {
+                    float M = -INFINITY;
 #pragma unroll
-                for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
+                    for (int v = 0; v < kConsumerWarps; ++v) M = fmaxf(M, xm[2 * v]);
+                    float acc[DPL], sum = 0.f;
 #pragma unroll
-                for (int v = 0; v < kConsumerWarps; ++v) {
-                    const float mv = xms[2 * v];
-                    const float wt = (mv == -INFINITY) ? 0.f : ex2(mv - M);
-                    sum += wt * xms[2 * v + 1];
+                    for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
 #pragma unroll
-                    for (int d = 0; d < DPL; ++d) acc[d] += wt * xo[v * D + lane * DPL + d];
+                    for (int v = 0; v < kConsumerWarps; ++v) {
+                        const float mv = xm[2 * v];
+                        const float wt = (mv == -INFINITY) ? 0.f : ex2(mv - M);
+                        sum += wt * xm[2 * v + 1];
+#pragma unroll
+                        for (int d = 0; d < DPL; ++d) acc[d] += wt * xo[v * D + lane * DPL + d];
+                    }
+                    const int pid = p.pbase[pos * H + h] + part;
+                    float* dst = p.part_o + (size_t)pid * D + lane * DPL;
+                    if constexpr (DPL == 4) {
+                        *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                    } else {
+                        *reinterpret_cast<float2*>(dst) = make_float2(acc[0], acc[1]);
+                    }
+                    if (lane == 0) p.part_ms[pid] = make_float2(M, sum);
                 }
-                const int pid = p.pbase[pos * H + h] + U.part;
-                float* dst = p.part_o + (size_t)pid * D + lane * DPL;
-                if constexpr (DPL == 4) {
-                    *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                } else {
-                    *reinterpret_cast<float2*>(dst) = make_float2(acc[0], acc[1]);
-                }
-                if (lane == 0) p.part_ms[pid] = make_float2(M, sum);
+                ++flush;
+                ++h;
+                part = part_next;
             }
         } else {
             // ---------------------------- chunk-first ----------------------------
-            const int m_rows = U.q_hi - U.q_lo;
+            const int h = fld(dc, F_HEAD), q_lo = fld(dc, F_QLO), q_hi = fld(dc, F_QHI);
+            const int c_begin = fld(dc, F_CB), c_end = fld(dc, F_CE), upart = fld(dc, F_PART);
+            if (next_sf) prefetch_q(fld(d0, F_QROW), fld(d0, F_HEAD));
+            const int m_rows = q_hi - q_lo;
             const int rblocks = m_rows <= 16 ? 1 : m_rows <= 32 ? 2 : 4;
             int T = kConsumerWarps / rblocks;            // warps splitting the tokens
             if (T * 16 > C) T = C / 16;
@@ -585,7 +621,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 uint4 v = make_uint4(0, 0, 0, 0);
                 if (r < m_rows)
                     v = *reinterpret_cast<const uint4*>(
-                        p.q + ((size_t)p.seq_perm[U.q_lo + r] * H + h) * D + k * 8);
+                        p.q + ((size_t)p.seq_perm[q_lo + r] * H + h) * D + k * 8);
                 *reinterpret_cast<uint4*>(qreg + swz(r, k, kQRows)) = v;
             }
             consumer_sync();
@@ -596,7 +632,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
             // pattern is the tile's shifted by rb * 16 rows of 128 bytes.
             const uint32_t qblock = smem_u32(qreg) + rb * 16 * 128;
             const int NTw = C / T;
-            for (int c = U.c_begin; c < U.c_end; ++c, ++it) {
+            for (int c = c_begin; c < c_end; ++c, ++it) {
                 const int st = it % S;
                 if (!mbar_wait(full0 + 8 * st, (uint32_t)(it / S) & 1u)) {
                     set_status(p.status, CA_ERR_TIMEOUT);
@@ -676,8 +712,8 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 for (int r = 0; r < 2; ++r) {
                     const int row = rb * 16 + g + 8 * r;
                     if (row < m_rows) {
-                        const int pos = U.q_lo + row;
-                        const int pid = p.pbase[pos * H + h] + U.part;
+                        const int pos = q_lo + row;
+                        const int pid = p.pbase[pos * H + h] + upart;
                         float* dst = p.part_o + (size_t)pid * D;
 #pragma unroll
                         for (int dt = 0; dt < D / 8; ++dt)

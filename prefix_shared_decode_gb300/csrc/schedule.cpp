@@ -18,8 +18,6 @@
 #include <algorithm>
 #include <cstring>
 #include <numeric>
-#include <queue>
-#include <unordered_set>
 
 #include "ca_internal.h"
 
@@ -57,8 +55,10 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
 
     std::vector<int64_t> order;
     order.reserve(b);
-    t = Tables();
     t.b = b;
+    for (auto* v : {&t.seq_perm, &t.cf_rows, &t.cf_runs, &t.sf_offsets, &t.sf_chunks, &t.merge_offsets,
+                    &t.merge_runs})
+        v->clear();
     t.seq_perm.reserve(b);
     t.sf_offsets.reserve(b + 1);
     t.merge_offsets.reserve(b + 1);
@@ -155,7 +155,11 @@ constexpr int32_t kMaxCfQueries = 64;
 void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
     const int32_t H = p.cfg.n_heads, D = p.cfg.head_dim, c = p.cfg.chunk, b = t.b;
     const int32_t R = (int32_t)(t.cf_rows.size() / 4), U = (int32_t)(t.cf_runs.size() / 4);
-    plan = Plan();
+    plan.chunks.clear();
+    plan.units.clear();
+    plan.cta_begin.clear();
+    plan.pbase.clear();
+    plan.n_partials = 0;
 
     // Chunk list: chunk-first rows first (index = row), then sf chunks.
     plan.chunks.resize(R + t.sf_chunks.size() / 2);
@@ -201,7 +205,7 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
                 const int32_t ra = row0 + (int32_t)((int64_t)nrows * k / np);
                 const int32_t rb = row0 + (int32_t)((int64_t)nrows * (k + 1) / np);
                 for (int32_t h = 0; h < H; ++h) {
-                    Unit x{UNIT_CF, h, qa, qb, ra, rb, k, 0};
+                    Unit x{UNIT_CF, h, qa, qb, ra, rb, k, 0, 0, 0, 0, 0};
                     cf.push_back({x, (rb - ra) * (1.0 + kCfComputePer16 * ((qb - qa + 15) / 16))});
                 }
             }
@@ -232,26 +236,43 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
 
     // LPT: biggest chunk-first units first, each onto the least-loaded CTA.
     // Units are collected flat with their CTA and counting-sorted at the end.
-    std::vector<std::pair<int32_t, Unit>> tagged;
-    tagged.reserve(cf.size() + (size_t)b * H + grid);
+    std::vector<std::pair<int32_t, Unit>>& tagged = plan.tagged;
+    tagged.clear();
+    tagged.reserve(cf.size() + (size_t)b + 2 * grid);
     std::vector<double> load(grid, 0.0);
-    std::stable_sort(cf.begin(), cf.end(), [](const CfUnit& a, const CfUnit& b2) { return a.cost > b2.cost; });
     {
-        using E = std::pair<double, int32_t>;
-        std::priority_queue<E, std::vector<E>, std::greater<E>> q;
-        for (int32_t k = 0; k < grid; ++k) q.push({0.0, k});
-        for (const auto& x : cf) {
-            E e = q.top();
-            q.pop();
-            tagged.emplace_back(e.second, x.u);
-            e.first += x.cost;
-            load[e.second] = e.first;
-            q.push(e);
+        // Costs in 1/64 tile units; the heap key packs (load, CTA) into one
+        // integer so that ties go to the lowest CTA index (deterministic).
+        std::vector<int32_t> order(cf.size());
+        std::vector<int64_t> icost(cf.size());
+        for (size_t i = 0; i < cf.size(); ++i) {
+            order[i] = (int32_t)i;
+            icost[i] = (int64_t)(cf[i].cost * 64.0 + 0.5);
+        }
+        std::sort(order.begin(), order.end(), [&](int32_t x, int32_t y) {
+            return icost[x] != icost[y] ? icost[x] > icost[y] : x < y;
+        });
+        std::vector<int64_t> heap(grid);
+        for (int32_t k = 0; k < grid; ++k) heap[k] = k;           // load 0
+        auto greater = [](int64_t x, int64_t y) { return x > y; };
+        std::make_heap(heap.begin(), heap.end(), greater);
+        for (int32_t i : order) {
+            std::pop_heap(heap.begin(), heap.end(), greater);
+            const int64_t top = heap.back();
+            const int32_t k = (int32_t)(top & 0xfffff);
+            const int64_t l = (top >> 20) + icost[i];
+            tagged.emplace_back(k, cf[i].u);
+            load[k] = l / 64.0;
+            heap.back() = (l << 20) | k;
+            std::push_heap(heap.begin(), heap.end(), greater);
         }
     }
 
-    // Sequence-first pieces: walk the (position, head) list and fill each
-    // CTA up to the average, cumulative-rounded so all tiles are placed.
+    // Sequence-first pieces.  Position p's work is its n_p own chunks for each
+    // of the H heads, in the order h * n_p + j; positions are laid end to end
+    // and each CTA takes a contiguous stretch up to its share (cumulative
+    // rounding places every tile), cut into one unit per position it touches.
+    // A head split between two units gets one partial per piece.
     std::vector<int32_t> npart((size_t)b * H, 0);
     for (int32_t pos = 0; pos < b; ++pos)
         for (int32_t h = 0; h < H; ++h) npart[(size_t)pos * H + h] = nk1[pos];
@@ -260,34 +281,35 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
         double qsum = 0;
         for (int32_t k = 0; k < grid; ++k) { quota[k] = std::max(0.0, avg - load[k]); qsum += quota[k]; }
         const double scale = qsum > 0 ? sf_total / qsum : 0.0;
-        int64_t placed = 0;
-        double cum = 0;
-        int32_t pos = 0, h = 0, done = 0;   // cursor: chunks of (pos, h) already placed
         auto seg_len = [&](int32_t ps) { return t.sf_offsets[ps + 1] - t.sf_offsets[ps]; };
-        // skip positions without sf chunks
+        int64_t placed = 0, done = 0;        // done: linear offset reached in `pos`
+        double cum = 0;
+        int32_t pos = 0, head_pieces = 0;    // pieces already placed of the head holding `done`
         while (pos < b && seg_len(pos) == 0) ++pos;
         for (int32_t k = 0; k < grid && pos < b; ++k) {
             cum += quota[k] * scale;
-            int64_t target = (k == grid - 1) ? (int64_t)sf_total : (int64_t)(cum + 0.5);
+            const int64_t target = (k == grid - 1) ? (int64_t)sf_total : (int64_t)(cum + 0.5);
             int64_t room = target - placed;
             while (room > 0 && pos < b) {
-                const int32_t len = seg_len(pos);
-                const int32_t take = (int32_t)std::min<int64_t>(room, len - done);
-                const int32_t base = R + t.sf_offsets[pos];
-                int32_t& np = npart[(size_t)pos * H + h];
-                tagged.emplace_back(k, Unit{UNIT_SF, h, pos, pos + 1, base + done, base + done + take, np,
-                                            t.seq_perm[pos]});
-                np += 1;
-                done += take;
+                const int32_t n = seg_len(pos);
+                const int64_t total = (int64_t)n * H;
+                const int64_t take = std::min<int64_t>(room, total - done);
+                const int64_t a = done, z = done + take;
+                const int32_t h0 = (int32_t)(a / n), hz = (int32_t)((z - 1) / n);
+                const int32_t before = (a % n == 0) ? 0 : head_pieces;
+                tagged.emplace_back(k, Unit{UNIT_SF, h0, pos, pos + 1, (int32_t)a, (int32_t)z,
+                                            nk1[pos] + before, t.seq_perm[pos], n,
+                                            R + t.sf_offsets[pos], nk1[pos], 0});
+                for (int32_t h = h0; h <= hz; ++h) npart[(size_t)pos * H + h] += 1;
+                head_pieces = (z % n == 0) ? 0 : ((z / n == h0) ? before + 1 : 1);
+                done = z;
                 placed += take;
                 room -= take;
-                if (done == len) {
+                if (done == total) {
                     done = 0;
-                    if (++h == H) {
-                        h = 0;
-                        ++pos;
-                        while (pos < b && seg_len(pos) == 0) ++pos;
-                    }
+                    head_pieces = 0;
+                    ++pos;
+                    while (pos < b && seg_len(pos) == 0) ++pos;
                 }
             }
         }

@@ -22,21 +22,29 @@ def simulate(plan, tables, trie, q, scale, H):
     perm, pbase = tables["seq_perm"], plan["pbase"]
     parts = {}
     cover = {}
-    for kind, h, lo, hi, cb, ce, part, _ in plan["units"]:
-        assert 0 <= h < H and lo < hi and cb < ce
-        if kind == 0:
-            assert hi - lo <= 64
-        else:
-            assert hi == lo + 1
-        chunks = plan["chunks"][cb:ce]
+    def emit(pos, h, part, chunks):
         k = np.concatenate([by_slot[s].k[0][:t, h] for s, t in chunks])[:, None, :]
         v = np.concatenate([by_slot[s].v[0][:t, h] for s, t in chunks])[:, None, :]
-        for pos in range(lo, hi):
-            pid = pbase[pos * H + h] + part
-            assert pbase[pos * H + h] <= pid < pbase[pos * H + h + 1]
-            assert pid not in parts
-            parts[pid] = A.partial(q[perm[pos], h][None, :], k, v, scale)
-            cover.setdefault((pos, h), []).extend(int(s) for s, _ in chunks)
+        pid = pbase[pos * H + h] + part
+        assert pbase[pos * H + h] <= pid < pbase[pos * H + h + 1]
+        assert pid not in parts
+        parts[pid] = A.partial(q[perm[pos], h][None, :], k, v, scale)
+        cover.setdefault((pos, h), []).extend(int(s) for s, _ in chunks)
+
+    for kind, h, lo, hi, cb, ce, part, qrow, n, base, part_next, _ in plan["units"]:
+        assert lo < hi and cb < ce
+        if kind == 0:
+            assert 0 <= h < H and hi - lo <= 64
+            for pos in range(lo, hi):
+                emit(pos, h, part, plan["chunks"][cb:ce])
+        else:
+            assert hi == lo + 1 and qrow == perm[lo] and h == cb // n
+            L = cb
+            while L < ce:                      # one head's piece at a time
+                hh, j = divmod(L, n)
+                z = min(ce, (hh + 1) * n)
+                emit(lo, hh, part if hh == h else part_next, plan["chunks"][base + j:base + j + (z - L)])
+                L = z
     assert len(parts) == pbase[-1]
     out = np.empty(q.shape)
     b = len(perm)
@@ -89,6 +97,8 @@ def test_plan_splits_large_runs_and_query_groups(lib):
     sched = pool.schedule(list(range(70)))
     plan = sched.plan()
     cf = plan["units"][plan["units"][:, 0] == 0]
+    sf = plan["units"][plan["units"][:, 0] == 1]
+    assert len(sf) <= 70 + 2 * 304                          # about one unit per position and CTA
     assert cf[:, 3].max() - cf[:, 2].min() == 70
     assert (cf[:, 3] - cf[:, 2]).max() <= 64
     assert len(np.unique(cf[:, 2])) == 2                   # two query groups
