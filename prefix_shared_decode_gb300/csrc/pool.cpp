@@ -21,15 +21,31 @@
 namespace ca {
 namespace {
 
-// 64-bit hash of a chunk's token tuple (multiply-xorshift per token).
+// 64-bit hash of a chunk's token tuple: four independent multiply-xorshift
+// lanes over token pairs (short dependency chains), folded at the end.
 uint64_t chunk_hash(const int32_t* tokens, int32_t c) {
-    uint64_t h = 0x6a09e667f3bcc909ull ^ (uint64_t)c;
-    for (int32_t i = 0; i < c; ++i) {
-        h ^= (uint64_t)(uint32_t)tokens[i];
-        h *= 0x9e3779b97f4a7c15ull;
-        h ^= h >> 31;
+    const uint64_t K = 0x9e3779b97f4a7c15ull;
+    uint64_t h[4] = {0x6a09e667f3bcc909ull ^ (uint64_t)c, 0xbb67ae8584caa73bull,
+                     0x3c6ef372fe94f82bull, 0xa54ff53a5f1d36f1ull};
+    int32_t i = 0;
+    for (; i + 8 <= c; i += 8) {
+        for (int l = 0; l < 4; ++l) {
+            const uint64_t w = (uint64_t)(uint32_t)tokens[i + 2 * l] |
+                               ((uint64_t)(uint32_t)tokens[i + 2 * l + 1] << 32);
+            h[l] = (h[l] ^ w) * K;
+            h[l] ^= h[l] >> 29;
+        }
     }
-    return h;
+    for (; i < c; ++i) {
+        h[0] = (h[0] ^ (uint64_t)(uint32_t)tokens[i]) * K;
+        h[0] ^= h[0] >> 29;
+    }
+    uint64_t r = h[0];
+    for (int l = 1; l < 4; ++l) {
+        r = (r ^ h[l]) * K;
+        r ^= r >> 31;
+    }
+    return r;
 }
 
 constexpr size_t kIndexAbove = 32;   // children before a node gets a hash index

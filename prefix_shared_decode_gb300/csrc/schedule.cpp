@@ -33,14 +33,18 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
         if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end()) return CA_ERR_INVALID;
     }
     const bool tpp = !(flags & CA_SCHED_NO_TPP);
-    // Batch holders per node (Node::mark), and the sequences ending at each
-    // node as one range of a (node, seq_id)-sorted list.
+    // Batch holders per node.  When the batch is every live sequence (the
+    // usual decode step) they are the chunks' refcounts; otherwise each
+    // batch path is marked (Node::mark).
+    const bool all_live = (size_t)b == p.seqs.size();
+    auto holders = [all_live](const Node* n) { return all_live ? n->refcount : n->mark; };
     std::vector<const Sequence*> seq_of(b);
     std::vector<std::pair<const Node*, int64_t>> ends(b);
     for (int32_t i = 0; i < b; ++i) {
         const Sequence& s = p.seqs.at(seq_ids[i]);
         seq_of[i] = &s;
-        for (Node* n : s.path) n->mark += 1;
+        if (!all_live)
+            for (Node* n : s.path) n->mark += 1;
         ends[i] = {s.path.back(), seq_ids[i]};
     }
     std::sort(ends.begin(), ends.end());
@@ -70,7 +74,7 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
         Frame& f = stack.back();
         const Node* node = f.node;
         if (f.next == 0 && node != &p.root) {
-            if (tpp && node->mark >= 2) {
+            if (tpp && holders(node) >= 2) {
                 const_cast<Node*>(node)->row = (int32_t)row_node.size();
                 row_node.push_back(node);
                 t.cf_rows.insert(t.cf_rows.end(),
@@ -79,7 +83,7 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
             for (int32_t k = 0; k < node->end_count; ++k) order.push_back(ends[node->end_begin + k].second);
         }
         size_t ci = f.next;
-        while (ci < node->children.size() && node->children[ci]->mark == 0) ++ci;
+        while (ci < node->children.size() && holders(node->children[ci]) == 0) ++ci;
         if (ci < node->children.size()) {
             f.next = ci + 1;
             stack.push_back({node->children[ci], 0});
@@ -117,8 +121,14 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
     // Sequence-first lists.
     t.sf_offsets.assign(1, 0);
     for (int32_t pos = 0; pos < b; ++pos) {
-        for (const Node* n : seq_at[pos]->path)
-            if (!tpp || n->mark == 1) t.sf_chunks.insert(t.sf_chunks.end(), {n->slot, n->ntok});
+        // holders never grow along a path, so the chunks this sequence holds
+        // alone are a suffix of it
+        const auto& path = seq_at[pos]->path;
+        size_t k = path.size();
+        if (!tpp) k = 0;
+        else
+            while (k > 0 && holders(path[k - 1]) == 1) --k;
+        for (; k < path.size(); ++k) t.sf_chunks.insert(t.sf_chunks.end(), {path[k]->slot, path[k]->ntok});
         t.sf_offsets.push_back((int32_t)(t.sf_chunks.size() / 2));
     }
 
@@ -133,10 +143,12 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
     }
 
     for (int32_t i = 0; i < b; ++i) {
-        for (Node* n : seq_of[i]->path) { n->mark = 0; n->row = -1; }
+        if (!all_live)
+            for (Node* n : seq_of[i]->path) n->mark = 0;
         Node* e = seq_of[i]->path.back();
         e->end_begin = e->end_count = 0;
     }
+    for (const Node* n : row_node) const_cast<Node*>(n)->row = -1;
     return CA_OK;
 }
 
