@@ -202,7 +202,9 @@ int ca_export_tables(const ca_sched* sched, int32_t* seq_perm, int32_t* cf_rows,
  *                       index h * n_per_head + j in [begin, end), chunk j at
  *                       list index base + j; its first head uses partial
  *                       index `part`, later heads `part_next`.
- *   cta_begin[grid+1]  unit range of each CTA
+ *   cta_begin[grid+1]  static unit range of each CTA; units from
+ *                      cta_begin[grid] to n_units form the tail queue that
+ *                      CTAs drain dynamically after their static ranges
  *   pbase[n_pbase]     partial ids of (position p, head h) are
  *                      [pbase[p*H+h], pbase[p*H+h+1])
  *   chunks[n_chunks][2] (slot, ntok) list the units index into */
@@ -222,7 +224,8 @@ int ca_workspace_bytes(const ca_sched* sched, size_t* bytes_out);
  *   layer    0 <= layer < n_layers
  *   ws_dev   >= ca_workspace_bytes(sched) bytes, 256-byte aligned, caller
  *            owned; its contents need no initialisation.  Calls sharing one
- *            workspace must not overlap on the GPU.
+ *            workspace or one schedule must not overlap on the GPU (the
+ *            schedule holds the kernels' work-queue counter).
  * Two kernels run on `stream`: the two-phase kernel and a merge kernel
  * launched as its programmatic dependent (one warp per sequence and head).
  * Errors: CA_ERR_STALE if the pool changed after the schedule was built;

@@ -56,7 +56,7 @@ constexpr int kUnitInts = (int)(sizeof(Unit) / sizeof(int32_t));
 
 // Offsets (in bytes) of the arrays inside the device plan blob.
 struct PlanLayout {
-    size_t chunks, units, cta_begin, seq_perm, pbase, status, total;
+    size_t chunks, units, cta_begin, seq_perm, pbase, status, counter, total;
 };
 
 // Parameters of the attention kernel (passed by value).
@@ -67,6 +67,8 @@ struct AttnParams {
     const int32_t* seq_perm;     // [b] position -> row of q / out
     const int32_t* pbase;        // [b*H + 1] partial-id CSR per (position, head)
     int32_t* status;             // device status word (CA_ERR_* or 0)
+    int32_t* dyn_counter;        // next unit of the shared tail queue (0 between calls)
+    int32_t dyn_begin, dyn_end;  // the tail queue: units [dyn_begin, dyn_end)
     const uint16_t* q;           // fp16 [b][H][D]
     uint16_t* out;               // fp16 [b][H][D]
     float* part_o;               // [P][D] unnormalised partial outputs
@@ -132,8 +134,8 @@ struct Tables {
 
 struct Plan {
     std::vector<ChunkRef> chunks;
-    std::vector<Unit> units;
-    std::vector<int32_t> cta_begin;
+    std::vector<Unit> units;       // per-CTA static lists, then the tail queue
+    std::vector<int32_t> cta_begin;  // [grid + 1]; cta_begin[grid] = first queue unit
     std::vector<int32_t> pbase;
     int32_t grid = 0;
     int64_t n_partials = 0;

@@ -321,6 +321,9 @@ static int decode_launch(const ca_pool* pool, const ca_sched* s, int32_t layer, 
     a.seq_perm = reinterpret_cast<const int32_t*>(dev + s->layout.seq_perm);
     a.pbase = reinterpret_cast<const int32_t*>(dev + s->layout.pbase);
     a.status = reinterpret_cast<int32_t*>(dev + s->layout.status);
+    a.dyn_counter = reinterpret_cast<int32_t*>(dev + s->layout.counter);
+    a.dyn_begin = s->plan.cta_begin[s->plan.grid];
+    a.dyn_end = (int32_t)s->plan.units.size();
     a.q = static_cast<const uint16_t*>(q);
     a.out = static_cast<uint16_t*>(out);
     a.part_o = reinterpret_cast<float*>(ws + s->ws.part_o);

@@ -41,6 +41,7 @@ constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kMaxStages = 8;
 constexpr int kQRows = 64;                 // queries per chunk-first unit, max
+constexpr int kRing = 16;                  // unit announcements (producer -> consumers)
 constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(128) merge_partials_kernel(const AttnParams p,
         row = p.seq_perm[gw / p.n_heads];
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.dyn_counter = 0;   // the main grid is done with it
     if (gw >= n_pairs) return;
     // Every lane loads (m, s) of partials lane, lane + 32, ...: max, then weights.
     float M = -INFINITY;
@@ -394,7 +396,10 @@ struct Smem {
     static constexpr int kQBytes = kQRows * D * 2;
     static constexpr int kXmsBytes = 512;
     static constexpr int kBarBytes = 2 * kMaxStages * 8;
-    static size_t bytes(int stages) { return (size_t)stages * kStage + kQBytes + kXmsBytes + kBarBytes; }
+    static constexpr int kRingBytes = kRing * 4;
+    static size_t bytes(int stages) {
+        return (size_t)stages * kStage + kQBytes + kXmsBytes + kBarBytes + kRingBytes;
+    }
 };
 
 // ---------------------------------------------------------------------------
@@ -412,6 +417,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
     uint8_t* qreg = smem + (size_t)S * SM::kStage;
     float* xms = reinterpret_cast<float*>(qreg + SM::kQBytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xms) + SM::kXmsBytes);
+    volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(bars + 2 * kMaxStages);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -440,19 +446,48 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
         const uint64_t pol = policy_evict_first();
         int it = 0;
         bool ok = true;
-        // The plan was uploaded before any kernel that precedes this one in
-        // the stream, so it may be read before the dependency wait; the pool
-        // and the queries only after it.
+        // Work: this CTA's static units [u_begin, u_end), then units claimed
+        // one at a time from the shared tail queue [dyn_begin, dyn_end).
+        // Claims run three units ahead, and each unit's id together with the
+        // next two is announced in the ring before its first chunk is issued
+        // (the chunk's barrier arrival publishes it).  The plan was uploaded
+        // before any kernel that precedes this one in the stream, so it may
+        // be read before the dependency wait; the pool, the queries and the
+        // queue counter (reset by the previous call's merge kernel) only after.
         auto first_chunk = [&](const Unit& X) {
             return X.kind == UNIT_SF ? X.base + X.c_begin % X.n_per_head : X.c_begin;
         };
-        Unit Un = (u_begin < u_end) ? p.units[u_begin] : Unit{};
-        // chunk references run one ahead of the copies they describe
-        ChunkRef chn = (u_begin < u_end) ? p.chunks[first_chunk(Un)] : ChunkRef{0, 0};
+        int s_next = u_begin;
+        auto claim = [&]() -> int {
+            if (s_next < u_end) return s_next++;
+            const int k = atomicAdd(p.dyn_counter, 1);
+            return (p.dyn_begin + k < p.dyn_end) ? p.dyn_begin + k : -1;
+        };
+        int cur = (u_begin < u_end) ? s_next++ : -1;
+        Unit Un = (cur >= 0) ? p.units[cur] : Unit{};
+        ChunkRef chn = (cur >= 0) ? p.chunks[first_chunk(Un)] : ChunkRef{0, 0};
         asm volatile("griddepcontrol.wait;" ::: "memory");
-        for (int u = u_begin; u < u_end && ok; ++u) {
+        if (cur < 0) {
+            cur = claim();
+            if (cur >= 0) {
+                Un = p.units[cur];
+                chn = p.chunks[first_chunk(Un)];
+            }
+        }
+        int nxt = (cur >= 0) ? claim() : -1;
+        int nxt2 = (nxt >= 0) ? claim() : -1;
+        if (cur < 0) {
+            // nothing to do: tell the consumers through the first stage
+            ring[0] = -1;
+            mbar_arrive(full0);
+            return;
+        }
+        for (int seq = 0; cur >= 0 && ok; ++seq) {
             const Unit U = Un;
-            if (u + 1 < u_end) Un = p.units[u + 1];
+            ring[seq % kRing] = cur;
+            ring[(seq + 1) % kRing] = nxt;
+            ring[(seq + 2) % kRing] = nxt2;
+            if (nxt >= 0) Un = p.units[nxt];
             const bool sf = U.kind == UNIT_SF;
             const int n = sf ? U.n_per_head : 1;
             int h = sf ? U.c_begin / n : U.head;
@@ -462,7 +497,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 const int head = h;
                 if (sf && ++j == n) { j = 0; ++h; }
                 if (L + 1 < U.c_end) chn = p.chunks[sf ? U.base + j : L + 1];
-                else if (u + 1 < u_end) chn = p.chunks[first_chunk(Un)];
+                else if (nxt >= 0) chn = p.chunks[first_chunk(Un)];
                 const int st = it % S;
                 const uint32_t ph = (uint32_t)(it / S) & 1u;
                 if (!mbar_wait(empty0 + 8 * st, ph ^ 1u)) {
@@ -486,6 +521,9 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     tma_load_2d(dst + SM::kTile + bx * C * 128, &tmap, bx * 64, rowV, fb, pol);
                 }
             }
+            cur = nxt;
+            nxt = nxt2;
+            nxt2 = (nxt2 >= 0) ? claim() : -1;
         }
         if (!ok) {
             // Give the copies already issued a bounded chance to land before
@@ -522,17 +560,38 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
     auto take_q = [&](int qrow, int head) -> uint2 {
         return (qrow == qn_row && head == qn_head) ? qn : load_q(qrow, head);
     };
-    int32_t d0 = 0, d1 = 0;
-    if (u_begin < u_end) d0 = load_desc(u_begin);
-    if (u_begin + 1 < u_end) d1 = load_desc(u_begin + 1);
+    // Unit ids: the first from the plan (or, for a CTA without static work,
+    // from the producer's announcement with the first stage); every later one
+    // from the ring, where the producer announces each unit's next two.
+    int cur = (u_begin < u_end) ? u_begin : -1;
+    int32_t dc = (cur >= 0) ? load_desc(cur) : 0, dn = 0;
     asm volatile("griddepcontrol.wait;" ::: "memory");     // q and the pool after this
-    if (u_begin < u_end && fld(d0, F_KIND) == UNIT_SF) prefetch_q(fld(d0, F_QROW), fld(d0, F_HEAD));
+    if (cur < 0) {
+        if (!mbar_wait(full0, 0u)) {
+            set_status(p.status, CA_ERR_TIMEOUT);
+            return;
+        }
+        cur = ring[0];
+        if (cur < 0) return;
+        dc = load_desc(cur);
+    }
+    if (fld(dc, F_KIND) == UNIT_SF) prefetch_q(fld(dc, F_QROW), fld(dc, F_HEAD));
+    int nxt = -1;
     int flush = 0;                        // sequence-first partials written (exchange parity)
-    for (int u = u_begin; u < u_end; ++u) {
-        const int32_t dc = d0;
-        d0 = d1;
-        if (u + 2 < u_end) d1 = load_desc(u + 2);
-        const bool next_sf = (u + 1 < u_end) && fld(d0, F_KIND) == UNIT_SF;
+    for (int seq = 0; cur >= 0; ++seq) {
+        // The unit's first stage carries the announcement of the units after it.
+        if (!mbar_wait(full0 + 8 * (it % S), (uint32_t)(it / S) & 1u)) {
+            set_status(p.status, CA_ERR_TIMEOUT);
+            return;
+        }
+        if (seq == 0) {
+            nxt = ring[1 % kRing];
+            if (nxt >= 0) dn = load_desc(nxt);
+        }
+        const int nn = ring[(seq + 2) % kRing];
+        const int32_t dnn = (nn >= 0) ? load_desc(nn) : 0;
+        const int32_t d0 = dn;                // the next unit's descriptor
+        const bool next_sf = nxt >= 0 && fld(d0, F_KIND) == UNIT_SF;
         consumer_sync();   // previous unit (and its exchange reads) finished
         if (fld(dc, F_KIND) == UNIT_SF) {
             const int pos = fld(dc, F_QLO), n = fld(dc, F_N), base = fld(dc, F_BASE);
@@ -724,6 +783,10 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 }
             }
         }
+        cur = nxt;
+        dc = dn;
+        nxt = nn;
+        dn = dnn;
     }
 }
 
@@ -782,7 +845,8 @@ void* pick_kernel(int chunk, int head_dim) {
 }
 size_t smem_for(int chunk, int head_dim, int stages) {
     const size_t stage = (size_t)2 * chunk * head_dim * 2;
-    return (size_t)stages * stage + (size_t)dev::kQRows * head_dim * 2 + 512 + 2 * dev::kMaxStages * 8;
+    return (size_t)stages * stage + (size_t)dev::kQRows * head_dim * 2 + 512 + 2 * dev::kMaxStages * 8 +
+           4 * dev::kRing;
 }
 }  // namespace
 
@@ -903,7 +967,11 @@ int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void*
         e = cudaLaunchKernelEx(&lc, dev::merge_partials_kernel<128>, a, n_pairs);
     else
         e = cudaLaunchKernelEx(&lc, dev::merge_partials_kernel<64>, a, n_pairs);
-    return e == cudaSuccess ? CA_OK : CA_ERR_CUDA;
+    if (e != cudaSuccess) {
+        cudaMemsetAsync(a.dyn_counter, 0, sizeof(int32_t), cs);   // keep the next call's queue clean
+        return CA_ERR_CUDA;
+    }
+    return CA_OK;
 }
 
 }  // namespace ca

@@ -162,6 +162,11 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
 namespace {
 constexpr double kCfComputePer16 = 0.2;
 constexpr int32_t kMaxCfQueries = 64;
+// Share of the sequence-first tiles left to the tail queue that CTAs drain
+// dynamically once their static lists are done (absorbs the run-to-run rate
+// differences between SMs), and the size of a queued unit in chunk-heads.
+constexpr double kTailShare = 0.12;
+constexpr int32_t kTailUnitTiles = 2;
 }  // namespace
 
 void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
@@ -189,7 +194,9 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
     const int32_t tiles_ceiling = (int32_t)std::max(1.0, sf_total + cf_total);
     grid = std::max(1, std::min(grid, tiles_ceiling));
     plan.grid = grid;
-    const double avg = (sf_total + cf_total) / grid;
+    const int64_t tail_tiles = (int64_t)(kTailShare * sf_total);
+    const double sf_static = sf_total - (double)tail_tiles;
+    const double avg = (sf_static + cf_total) / grid;
 
     // Chunk-first units: pieces per run.
     std::vector<int32_t> pieces(U, 0);
@@ -292,7 +299,7 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
         std::vector<double> quota(grid);
         double qsum = 0;
         for (int32_t k = 0; k < grid; ++k) { quota[k] = std::max(0.0, avg - load[k]); qsum += quota[k]; }
-        const double scale = qsum > 0 ? sf_total / qsum : 0.0;
+        const double scale = qsum > 0 ? sf_static / qsum : 0.0;
         auto seg_len = [&](int32_t ps) { return t.sf_offsets[ps + 1] - t.sf_offsets[ps]; };
         int64_t placed = 0, done = 0;        // done: linear offset reached in `pos`
         double cum = 0;
@@ -300,7 +307,7 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
         while (pos < b && seg_len(pos) == 0) ++pos;
         for (int32_t k = 0; k < grid && pos < b; ++k) {
             cum += quota[k] * scale;
-            const int64_t target = (k == grid - 1) ? (int64_t)sf_total : (int64_t)(cum + 0.5);
+            const int64_t target = (k == grid - 1) ? (int64_t)sf_static : (int64_t)(cum + 0.5);
             int64_t room = target - placed;
             while (room > 0 && pos < b) {
                 const int32_t n = seg_len(pos);
@@ -325,21 +332,43 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
                 }
             }
         }
+        // The rest of the list becomes the tail queue: units of at most
+        // kTailUnitTiles chunk-heads that never cross a head boundary.
+        while (pos < b) {
+            const int32_t n = seg_len(pos);
+            const int64_t total = (int64_t)n * H;
+            const int64_t a = done;
+            const int64_t head_end = (a / n + 1) * n;
+            const int64_t z = std::min<int64_t>(a + kTailUnitTiles, head_end);
+            const int32_t h0 = (int32_t)(a / n);
+            const int32_t before = (a % n == 0) ? 0 : head_pieces;
+            tagged.emplace_back(grid, Unit{UNIT_SF, h0, pos, pos + 1, (int32_t)a, (int32_t)z,
+                                           nk1[pos] + before, t.seq_perm[pos], n,
+                                           R + t.sf_offsets[pos], nk1[pos], 0});
+            npart[(size_t)pos * H + h0] += 1;
+            head_pieces = (z % n == 0) ? 0 : before + 1;
+            done = z;
+            if (done == total) {
+                done = 0;
+                head_pieces = 0;
+                ++pos;
+                while (pos < b && seg_len(pos) == 0) ++pos;
+            }
+        }
     }
 
     plan.pbase.assign((size_t)b * H + 1, 0);
     for (size_t i = 0; i < (size_t)b * H; ++i) plan.pbase[i + 1] = plan.pbase[i] + npart[i];
     plan.n_partials = plan.pbase.back();
-    // Counting sort by CTA, stable: each CTA keeps its chunk-first units
-    // first, then its sequence-first pieces in list order.
-    plan.cta_begin.assign(grid + 1, 0);
-    for (const auto& x : tagged) plan.cta_begin[x.first + 1] += 1;
-    for (int32_t k = 0; k < grid; ++k) plan.cta_begin[k + 1] += plan.cta_begin[k];
+    // Counting sort by CTA (bucket `grid` is the tail queue), stable: each
+    // CTA keeps its chunk-first units first, then its sequence-first pieces in
+    // list order.
+    std::vector<int32_t> start(grid + 2, 0);
+    for (const auto& x : tagged) start[x.first + 1] += 1;
+    for (int32_t k = 0; k <= grid; ++k) start[k + 1] += start[k];
+    plan.cta_begin.assign(start.begin(), start.begin() + grid + 1);
     plan.units.resize(tagged.size());
-    {
-        std::vector<int32_t> fill(plan.cta_begin.begin(), plan.cta_begin.end() - 1);
-        for (const auto& x : tagged) plan.units[fill[x.first]++] = x.second;
-    }
+    for (const auto& x : tagged) plan.units[start[x.first]++] = x.second;
 }
 
 namespace {
@@ -355,6 +384,7 @@ void layout_plan(const Plan& plan, int32_t b, PlanLayout& lay, std::vector<unsig
     lay.seq_perm = off;  off = align256(off + (size_t)b * sizeof(int32_t));
     lay.pbase = off;     off = align256(off + plan.pbase.size() * sizeof(int32_t));
     lay.status = off;    off = align256(off + sizeof(int32_t));
+    lay.counter = off;   off = align256(off + sizeof(int32_t));
     lay.total = off;
     blob.assign(off, 0);
     std::memcpy(blob.data() + lay.chunks, plan.chunks.data(), plan.chunks.size() * sizeof(ChunkRef));
