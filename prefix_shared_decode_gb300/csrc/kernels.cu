@@ -447,13 +447,14 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
         int it = 0;
         bool ok = true;
         // Work: this CTA's static units [u_begin, u_end), then units claimed
-        // one at a time from the shared tail queue [dyn_begin, dyn_end).
-        // Claims run three units ahead, and each unit's id together with the
-        // next two is announced in the ring before its first chunk is issued
-        // (the chunk's barrier arrival publishes it).  The plan was uploaded
-        // before any kernel that precedes this one in the stream, so it may
-        // be read before the dependency wait; the pool, the queries and the
-        // queue counter (reset by the previous call's merge kernel) only after.
+        // one at a time from the shared tail queue [dyn_begin, dyn_end).  A
+        // queue unit is claimed only once this CTA has issued all its earlier
+        // work (at most one claim ahead), so slow CTAs do not hoard the tail.
+        // Each unit's id is written to the ring before its first chunk is
+        // issued (that chunk's barrier arrival publishes it); after the last
+        // unit a stage carries the id -1.  The plan may be read before the
+        // dependency wait; the pool, the queries and the queue counter (reset
+        // by the previous call's merge kernel) only after it.
         auto first_chunk = [&](const Unit& X) {
             return X.kind == UNIT_SF ? X.base + X.c_begin % X.n_per_head : X.c_begin;
         };
@@ -474,25 +475,27 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 chn = p.chunks[first_chunk(Un)];
             }
         }
-        int nxt = (cur >= 0) ? claim() : -1;
-        int nxt2 = (nxt >= 0) ? claim() : -1;
-        if (cur < 0) {
-            // nothing to do: tell the consumers through the first stage
-            ring[0] = -1;
-            mbar_arrive(full0);
-            return;
-        }
-        for (int seq = 0; cur >= 0 && ok; ++seq) {
+        int seq = 0;
+        for (; cur >= 0 && ok; ++seq) {
             const Unit U = Un;
             ring[seq % kRing] = cur;
-            ring[(seq + 1) % kRing] = nxt;
-            ring[(seq + 2) % kRing] = nxt2;
-            if (nxt >= 0) Un = p.units[nxt];
+            // The next unit (the next static one, or in the tail phase a
+            // claim) is taken when three chunks of this one remain: late
+            // enough not to hold queue work long, early enough to hide the
+            // claim and descriptor latency.
+            int nxt = -1;
+            bool have_next = false;
+            const int claim_at = max(U.c_begin, U.c_end - 3);
             const bool sf = U.kind == UNIT_SF;
             const int n = sf ? U.n_per_head : 1;
             int h = sf ? U.c_begin / n : U.head;
             int j = sf ? U.c_begin - h * n : 0;
             for (int L = U.c_begin; L < U.c_end; ++L, ++it) {
+                if (!have_next && L >= claim_at) {
+                    nxt = claim();
+                    if (nxt >= 0) Un = p.units[nxt];
+                    have_next = true;
+                }
                 const ChunkRef ch = chn;
                 const int head = h;
                 if (sf && ++j == n) { j = 0; ++h; }
@@ -521,9 +524,21 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     tma_load_2d(dst + SM::kTile + bx * C * 128, &tmap, bx * 64, rowV, fb, pol);
                 }
             }
+            if (!have_next) {                 // left early on a timeout
+                nxt = -1;
+            }
             cur = nxt;
-            nxt = nxt2;
-            nxt2 = (nxt2 >= 0) ? claim() : -1;
+        }
+        if (ok) {
+            // end of work: one more stage, without data, carries the id -1
+            const int st = it % S;
+            if (mbar_wait(empty0 + 8 * st, ((uint32_t)(it / S) & 1u) ^ 1u)) {
+                ring[seq % kRing] = -1;
+                mbar_arrive(full0 + 8 * st);
+            } else {
+                set_status(p.status, CA_ERR_TIMEOUT);
+                ok = false;
+            }
         }
         if (!ok) {
             // Give the copies already issued a bounded chance to land before
@@ -560,38 +575,29 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
     auto take_q = [&](int qrow, int head) -> uint2 {
         return (qrow == qn_row && head == qn_head) ? qn : load_q(qrow, head);
     };
-    // Unit ids: the first from the plan (or, for a CTA without static work,
-    // from the producer's announcement with the first stage); every later one
-    // from the ring, where the producer announces each unit's next two.
-    int cur = (u_begin < u_end) ? u_begin : -1;
-    int32_t dc = (cur >= 0) ? load_desc(cur) : 0, dn = 0;
+    // Unit ids come from the ring (the producer writes each before the
+    // unit's first chunk; -1 ends the work).  Static ids are known from the
+    // plan, so their descriptors and first query rows are fetched one unit
+    // ahead; a queue unit's descriptor is read when its id arrives.
+    const int n_static = u_end - u_begin;
+    int32_t dn = (n_static > 0) ? load_desc(u_begin) : 0;   // descriptor of unit `seq`
     asm volatile("griddepcontrol.wait;" ::: "memory");     // q and the pool after this
-    if (cur < 0) {
-        if (!mbar_wait(full0, 0u)) {
-            set_status(p.status, CA_ERR_TIMEOUT);
-            return;
-        }
-        cur = ring[0];
-        if (cur < 0) return;
-        dc = load_desc(cur);
-    }
-    if (fld(dc, F_KIND) == UNIT_SF) prefetch_q(fld(dc, F_QROW), fld(dc, F_HEAD));
-    int nxt = -1;
+    if (n_static > 0 && fld(dn, F_KIND) == UNIT_SF) prefetch_q(fld(dn, F_QROW), fld(dn, F_HEAD));
     int flush = 0;                        // sequence-first partials written (exchange parity)
-    for (int seq = 0; cur >= 0; ++seq) {
-        // The unit's first stage carries the announcement of the units after it.
+    for (int seq = 0;; ++seq) {
+        // The unit's first stage (or the closing one) carries its id.
         if (!mbar_wait(full0 + 8 * (it % S), (uint32_t)(it / S) & 1u)) {
             set_status(p.status, CA_ERR_TIMEOUT);
             return;
         }
-        if (seq == 0) {
-            nxt = ring[1 % kRing];
-            if (nxt >= 0) dn = load_desc(nxt);
-        }
-        const int nn = ring[(seq + 2) % kRing];
-        const int32_t dnn = (nn >= 0) ? load_desc(nn) : 0;
-        const int32_t d0 = dn;                // the next unit's descriptor
-        const bool next_sf = nxt >= 0 && fld(d0, F_KIND) == UNIT_SF;
+        const int cur = ring[seq % kRing];
+        if (cur < 0) break;
+        const int32_t dc = (seq < n_static) ? dn : load_desc(cur);
+        // the next unit, when it is static: its descriptor now, its query later
+        const bool next_static = seq + 1 < n_static;
+        if (next_static) dn = load_desc(u_begin + seq + 1);
+        const int32_t d0 = dn;
+        const bool next_sf = next_static && fld(d0, F_KIND) == UNIT_SF;
         consumer_sync();   // previous unit (and its exchange reads) finished
         if (fld(dc, F_KIND) == UNIT_SF) {
             const int pos = fld(dc, F_QLO), n = fld(dc, F_N), base = fld(dc, F_BASE);
@@ -783,10 +789,6 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 }
             }
         }
-        cur = nxt;
-        dc = dn;
-        nxt = nn;
-        dn = dnn;
     }
 }
 
