@@ -166,7 +166,8 @@ constexpr int32_t kMaxCfQueries = 64;
 // dynamically once their static lists are done (absorbs the run-to-run rate
 // differences between SMs), and the size of a queued unit in chunk-heads.
 constexpr double kTailShare = 0.12;
-constexpr int32_t kTailUnitTiles = 2;
+constexpr int32_t kTailUnitsPerCta = 2;     // aim: about this many queue units per CTA
+constexpr int32_t kTailUnitMin = 2, kTailUnitMax = 8;
 }  // namespace
 
 void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
@@ -333,13 +334,16 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
             }
         }
         // The rest of the list becomes the tail queue: units of at most
-        // kTailUnitTiles chunk-heads that never cross a head boundary.
+        // `tail_unit` chunk-heads that never cross a head boundary.
+        const int32_t tail_unit = std::max<int32_t>(
+            kTailUnitMin, std::min<int32_t>(kTailUnitMax, (int32_t)((tail_tiles + kTailUnitsPerCta * grid - 1) /
+                                                                   ((int64_t)kTailUnitsPerCta * grid))));
         while (pos < b) {
             const int32_t n = seg_len(pos);
             const int64_t total = (int64_t)n * H;
             const int64_t a = done;
             const int64_t head_end = (a / n + 1) * n;
-            const int64_t z = std::min<int64_t>(a + kTailUnitTiles, head_end);
+            const int64_t z = std::min<int64_t>(a + tail_unit, head_end);
             const int32_t h0 = (int32_t)(a / n);
             const int32_t before = (a % n == 0) ? 0 : head_pieces;
             tagged.emplace_back(grid, Unit{UNIT_SF, h0, pos, pos + 1, (int32_t)a, (int32_t)z,
