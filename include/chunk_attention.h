@@ -90,10 +90,12 @@ typedef struct {
 } ca_stats;
 
 /* ---- pool ----------------------------------------------------------------
- * Device layout (row-major, fp16):
+ * Device layout: the K/V tiles (row-major, fp16)
  *     kv[slot][layer][K|V][head][c][head_dim]
  * so one chunk of one head is a contiguous c x head_dim tile (16 KiB at
- * c = 64, D = 128) that the kernels fetch whole with TMA.
+ * c = 64, D = 128) that the kernels fetch whole with TMA; then one int32 per
+ * slot holding the chunk's valid-token count (the kernels read it, so a
+ * decode-time append can grow a partial chunk without a new schedule).
  */
 
 /* Bytes of device memory a pool with this shape needs (for kv_dev). */
@@ -144,6 +146,23 @@ int ca_insert_batch(ca_pool* pool, int32_t n_seqs, const int64_t* seq_ids,
                     const int32_t* tokens, const int32_t* lengths,
                     const void* k_dev, const void* v_dev, void* stream,
                     int32_t* n_shared_out);
+
+/* Append decoded tokens to a live sequence [CA §3.1: decoding appends tokens
+ * to leaf chunks or grows new chunks].  The tokens first fill the sequence's
+ * partial last chunk in place, then grow new private chunks (lowest free
+ * slots first); an append never matches existing chunks.  A chunk that
+ * becomes full becomes shareable by later inserts (unless its parent already
+ * holds an equal one).  k_dev / v_dev: fp16 [n_layers][n][n_heads][head_dim]
+ * for the n appended tokens.  Filling the partial chunk does not change the
+ * tree's structure, so schedules stay valid (their exported ntok values are
+ * as of their build; the kernels read current counts from the pool); growing
+ * a chunk bumps the generation (schedules go stale), as the pages' "a full
+ * chunk triggers a context copy" [CA §3.3].  n_new_chunks_out (may be NULL)
+ * receives the number of chunks grown.  Errors: CA_ERR_NOT_FOUND, CA_ERR_OOM,
+ * CA_ERR_INVALID, CA_ERR_CUDA; on error the pool is unchanged. */
+int ca_append_tokens(ca_pool* pool, int64_t seq_id, const int32_t* tokens,
+                     int32_t n, const void* k_dev, const void* v_dev,
+                     void* stream, int32_t* n_new_chunks_out);
 
 /* Remove a finished sequence [CA §3.1: completed sequences remove their
  * path].  Every chunk on its path loses one reference; chunks left with none

@@ -24,6 +24,15 @@ the rest supports):
   R7  a sequence's context is exactly the tokens inserted for it.
   NS  with ``no_sharing`` nothing is ever matched, so every sequence owns a
       private chain of chunks (the flat paged layout used as the control).
+  R13 decode-time append [CA-summary §3.1: decoding appends tokens to leaf
+      chunks or grows new chunks; §3.3: a full chunk triggers a context
+      copy]: the appended tokens first fill the sequence's partial last chunk
+      (always private, R2), then grow new private chunks (lowest slots first);
+      an append never matches existing chunks.  A chunk that becomes full
+      this way becomes matchable for later inserts unless its parent already
+      has a matchable child with the same tokens.  Only growing a new chunk
+      changes the tree's structure (bumps the generation); filling the
+      partial chunk in place does not.
 """
 from __future__ import annotations
 
@@ -152,6 +161,47 @@ class OracleTrie:
         self.lengths[seq_id] = n
         self.generation += 1
         return n_matched * c
+
+    def append(self, seq_id: int, tokens, k=None, v=None) -> int:
+        """Append decoded tokens to a sequence (R13).  ``k``/``v`` are
+        [L, n, H, D] for the appended tokens (or None).  Returns the number of
+        new chunks; on error the trie is unchanged."""
+        if seq_id not in self.paths:
+            raise OracleError("not_found", str(seq_id))
+        tokens = [int(t) for t in tokens]
+        n, c = len(tokens), self.chunk
+        if n <= 0:
+            raise OracleError("invalid", "empty append")
+        path = self.paths[seq_id]
+        last = path[-1]
+        fill = min(c - last.ntok, n)
+        n_new = -(-(n - fill) // c)
+        if n_new > len(self.free):
+            raise OracleError("oom", f"need {n_new} slots, {len(self.free)} free")
+        if fill:
+            last.tokens = last.tokens + tuple(tokens[:fill])
+            if k is not None:
+                last.k = np.concatenate([last.k, k[:, :fill]], axis=1)
+                last.v = np.concatenate([last.v, v[:, :fill]], axis=1)
+            if last.ntok == c and not self.no_sharing:
+                last.parent.match.setdefault(last.tokens, last)
+        node = last
+        for i in range(n_new):
+            a = fill + i * c
+            key = tuple(tokens[a:a + c])
+            slot = heapq.heappop(self.free)
+            child = Node(slot, key, None if k is None else k[:, a:a + len(key)],
+                         None if v is None else v[:, a:a + len(key)], node)
+            node.children.append(child)
+            if len(key) == c and not self.no_sharing:
+                node.match.setdefault(key, child)
+            child.refcount = 1
+            path.append(child)
+            node = child
+        self.lengths[seq_id] += n
+        if n_new:
+            self.generation += 1
+        return n_new
 
     def remove(self, seq_id: int) -> None:
         """Drop a sequence's references; chunks left with none are freed."""

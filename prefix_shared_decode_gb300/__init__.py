@@ -133,6 +133,22 @@ class Pool:
                                          shared.ctypes.data_as(P32)), "ca_insert_batch")
         return shared.tolist()
 
+    def append(self, seq_id: int, tokens, k=None, v=None, stream=None) -> int:
+        """Append decoded tokens to a sequence; k, v are fp16 device tensors
+        [L, n, H, D] for the new tokens (None for a host-only pool).  Returns
+        the number of chunks grown (0: the partial last chunk took them)."""
+        tok = _i32(tokens)
+        kp = vp = None
+        if k is not None:
+            assert k.is_contiguous() and v.is_contiguous()
+            assert tuple(k.shape) == (self.n_layers, len(tok), self.n_heads, self.head_dim)
+            kp, vp = k.data_ptr(), v.data_ptr()
+        grown = C.c_int32()
+        check(capi.lib().ca_append_tokens(self._h, int(seq_id), tok.ctypes.data_as(C.POINTER(C.c_int32)),
+                                          len(tok), kp, vp, None if self.host_only else _stream_ptr(stream),
+                                          C.byref(grown)), "ca_append_tokens")
+        return grown.value
+
     def remove(self, seq_id: int) -> None:
         check(capi.lib().ca_remove_seq(self._h, int(seq_id)), "ca_remove_seq")
 

@@ -23,7 +23,7 @@ CA_SCHED_NO_TPP = 1
 # Every symbol the header declares, in header order.
 EXPORTS = [
     "ca_pool_bytes", "ca_pool_create", "ca_pool_destroy", "ca_match_prefix", "ca_insert_tokens",
-    "ca_insert_batch", "ca_remove_seq", "ca_remove_batch", "ca_pool_stats", "ca_seq_slots", "ca_build_schedule", "ca_sched_destroy",
+    "ca_insert_batch", "ca_append_tokens", "ca_remove_seq", "ca_remove_batch", "ca_pool_stats", "ca_seq_slots", "ca_build_schedule", "ca_sched_destroy",
     "ca_sched_counts", "ca_export_tables", "ca_export_plan", "ca_workspace_bytes", "ca_decode_attention",
     "ca_workspace_bytes_host", "ca_decode_attention_host", "ca_decode_attention_static_ws",
     "ca_sched_device_status",
@@ -70,6 +70,7 @@ def lib() -> C.CDLL:
         "ca_match_prefix": [vp, P(i32), i32, P(i32)],
         "ca_insert_tokens": [vp, i64, P(i32), i32, vp, vp, vp, P(i32)],
         "ca_insert_batch": [vp, i32, P(i64), P(i32), P(i32), vp, vp, vp, P(i32)],
+        "ca_append_tokens": [vp, i64, P(i32), i32, vp, vp, vp, P(i32)],
         "ca_remove_seq": [vp, i64],
         "ca_remove_batch": [vp, i32, P(i64)],
         "ca_pool_stats": [vp, P(Stats)],

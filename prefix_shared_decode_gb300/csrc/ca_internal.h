@@ -66,6 +66,7 @@ struct AttnParams {
     const int32_t* cta_begin;    // [grid + 1] unit ranges per CTA
     const int32_t* seq_perm;     // [b] position -> row of q / out
     const int32_t* pbase;        // [b*H + 1] partial-id CSR per (position, head)
+    const int32_t* slot_ntok;    // [capacity] valid tokens per pool slot (device table)
     int32_t* status;             // device status word (CA_ERR_* or 0)
     int32_t* dyn_counter;        // next unit of the shared tail queue (0 between calls)
     int32_t dyn_begin, dyn_end;  // the tail queue: units [dyn_begin, dyn_end)
@@ -162,7 +163,32 @@ struct Sched {
     void* ev_end = nullptr;
 };
 
+// One chunk to fill: rows [src_row, src_row + n_rows) of a packed
+// [L][total_rows][H][D] source go to rows [dst_row, dst_row + n_rows) of
+// `slot`, whose valid-token count becomes dst_row + n_rows.
+struct ScatterChunk {
+    int32_t src_row, n_rows, slot, dst_row;
+};
+
+// Device bytes of the pool: the K/V tiles, then the per-slot token counts.
+size_t pool_tile_bytes(const ca_pool_config& c);
+size_t pool_total_bytes(const ca_pool_config& c);
+
+// What an append changed, so that a failed copy launch can undo it.
+struct AppendUndo {
+    Node* last = nullptr;
+    int32_t ntok = 0;
+    bool matchable = false;
+    uint64_t hash = 0;
+    size_t path_size = 0;
+    int64_t generation = 0;
+    int32_t length = 0;
+};
+
 // pool.cpp
+int pool_append(Pool& p, int64_t seq_id, const int32_t* tokens, int32_t n,
+                std::vector<ScatterChunk>* copies, AppendUndo* undo);
+void pool_undo_append(Pool& p, int64_t seq_id, const AppendUndo& undo);
 int pool_insert(Pool& p, int64_t seq_id, const int32_t* tokens, int32_t n,
                 std::vector<std::pair<int32_t, int32_t>>* new_chunks,  // (first token, slot)
                 int32_t* n_shared);
@@ -180,11 +206,6 @@ void layout_ws(const Plan& plan, const Pool& p, int32_t b, WsLayout& ws);
 int kernel_smem_bytes(int chunk, int head_dim, int* n_stages, size_t* bytes);
 int kernel_ctas_per_sm(int chunk, int head_dim, int* ctas);
 int make_tensor_map(Pool& p);
-// One new chunk to fill: rows [src_row, src_row + n_rows) of a packed
-// [L][total_rows][H][D] source go to rows [0, n_rows) of `slot`.
-struct ScatterChunk {
-    int32_t src_row, n_rows, slot;
-};
 int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_rows,
                    const std::vector<ScatterChunk>& chunks, void* stream);
 int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void* stream);

@@ -43,9 +43,7 @@ int check_cfg(const ca_pool_config* c) {
     return CA_OK;
 }
 
-size_t pool_bytes(const ca_pool_config& c) {
-    return (size_t)c.capacity_slots * c.n_layers * 2 * c.n_heads * c.chunk * c.head_dim * 2;
-}
+size_t pool_bytes(const ca_pool_config& c) { return pool_total_bytes(c); }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? CA_OK : CA_ERR_CUDA; }
 
@@ -136,7 +134,7 @@ int ca_insert_batch(ca_pool* pool, int32_t n_seqs, const int64_t* seq_ids, const
             st = pool_insert(*pool, seq_ids[i], tokens + row0, lengths[i], &fresh, &shared);
             if (st) break;
             for (const auto& f : fresh)
-                copies.push_back({row0 + f.first, std::min(pool->cfg.chunk, lengths[i] - f.first), f.second});
+                copies.push_back({row0 + f.first, std::min(pool->cfg.chunk, lengths[i] - f.first), f.second, 0});
             if (n_shared_out) n_shared_out[i] = shared;
             row0 += lengths[i];
         }
@@ -146,6 +144,32 @@ int ca_insert_batch(ca_pool* pool, int32_t n_seqs, const int64_t* seq_ids, const
             pool->generation = gen;
         }
         return st;
+    });
+}
+
+int ca_append_tokens(ca_pool* pool, int64_t seq_id, const int32_t* tokens, int32_t n,
+                     const void* k_dev, const void* v_dev, void* stream, int32_t* n_new_chunks_out) {
+    if (!pool || n <= 0 || !tokens) return CA_ERR_INVALID;
+    if (pool->kv) {
+        if (!k_dev || !v_dev || !aligned(k_dev, 16) || !aligned(v_dev, 16)) return CA_ERR_INVALID;
+    } else if (k_dev || v_dev) {
+        return CA_ERR_INVALID;
+    }
+    return guard([&] {
+        std::vector<ScatterChunk> copies;
+        AppendUndo undo;
+        const size_t before = pool->seqs.count(seq_id) ? pool->seqs.at(seq_id).path.size() : 0;
+        int st = pool_append(*pool, seq_id, tokens, n, &copies, &undo);
+        if (st) return st;
+        if (pool->kv) {
+            st = launch_scatter(*pool, k_dev, v_dev, n, copies, stream);
+            if (st) {
+                pool_undo_append(*pool, seq_id, undo);
+                return st;
+            }
+        }
+        if (n_new_chunks_out) *n_new_chunks_out = (int32_t)(pool->seqs.at(seq_id).path.size() - before);
+        return CA_OK;
     });
 }
 
@@ -320,6 +344,8 @@ static int decode_launch(const ca_pool* pool, const ca_sched* s, int32_t layer, 
     a.cta_begin = reinterpret_cast<const int32_t*>(dev + s->layout.cta_begin);
     a.seq_perm = reinterpret_cast<const int32_t*>(dev + s->layout.seq_perm);
     a.pbase = reinterpret_cast<const int32_t*>(dev + s->layout.pbase);
+    a.slot_ntok = reinterpret_cast<const int32_t*>(static_cast<const unsigned char*>(pool->kv) +
+                                                   pool_tile_bytes(pool->cfg));
     a.status = reinterpret_cast<int32_t*>(dev + s->layout.status);
     a.dyn_counter = reinterpret_cast<int32_t*>(dev + s->layout.counter);
     a.dyn_begin = s->plan.cta_begin[s->plan.grid];

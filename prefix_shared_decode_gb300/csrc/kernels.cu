@@ -396,7 +396,7 @@ struct Smem {
     static constexpr int kQBytes = kQRows * D * 2;
     static constexpr int kXmsBytes = 512;
     static constexpr int kBarBytes = 2 * kMaxStages * 8;
-    static constexpr int kRingBytes = kRing * 4;
+    static constexpr int kRingBytes = kRing * 4 + kMaxStages * 4;
     static size_t bytes(int stages) {
         return (size_t)stages * kStage + kQBytes + kXmsBytes + kBarBytes + kRingBytes;
     }
@@ -418,6 +418,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
     float* xms = reinterpret_cast<float*>(qreg + SM::kQBytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xms) + SM::kXmsBytes);
     volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(bars + 2 * kMaxStages);
+    volatile int32_t* stage_ntok = ring + kRing;          // valid tokens of each stage's chunk
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -497,6 +498,11 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     have_next = true;
                 }
                 const ChunkRef ch = chn;
+                // the chunk's token count comes from the pool's device table
+                // (appends grow partial chunks in place); the load is in
+                // flight while the producer waits for the stage
+                const bool slot_ok = ch.slot >= 0 && ch.slot < p.capacity;
+                const int ntok = slot_ok ? p.slot_ntok[ch.slot] : 0;
                 const int head = h;
                 if (sf && ++j == n) { j = 0; ++h; }
                 if (L + 1 < U.c_end) chn = p.chunks[sf ? U.base + j : L + 1];
@@ -509,11 +515,13 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     break;
                 }
                 const uint32_t fb = full0 + 8 * st;
-                if (ch.slot < 0 || ch.slot >= p.capacity || head < 0 || head >= H) {
+                if (!slot_ok || head < 0 || head >= H) {
                     set_status(p.status, CA_ERR_DEVICE_BOUNDS);
+                    stage_ntok[st] = 0;
                     mbar_arrive(fb);          // release the consumers without data
                     continue;
                 }
+                stage_ntok[st] = min(max(ntok, 0), C);
                 mbar_expect_tx(fb, SM::kStage);
                 const uint32_t dst = smem_u32(stages + (size_t)st * SM::kStage);
                 const int rowK = (((ch.slot * p.n_layers + p.layer) * 2 + 0) * H + head) * C;
@@ -625,7 +633,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                         set_status(p.status, CA_ERR_TIMEOUT);
                         return;
                     }
-                    const int ntok = min(max(p.chunks[base + j].ntok, 0), C);
+                    const int ntok = stage_ntok[st];
                     const uint8_t* kt = stages + (size_t)st * SM::kStage;
                     sf_chunk<C, D>(kt, kt + SM::kTile, ntok, q, m, s, o, w, lane);
                     __syncwarp();
@@ -704,7 +712,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     return;
                 }
                 if (active) {
-                    const int ntok = min(max(p.chunks[c].ntok, 0), C);
+                    const int ntok = stage_ntok[st];
                     const uint32_t kt = smem_u32(stages + (size_t)st * SM::kStage);
                     const uint32_t vt = kt + SM::kTile;
                     if (NTw == 16) {
@@ -802,6 +810,7 @@ struct ScatterArgs {
     const uint4* k;
     const uint4* v;
     uint4* pool;
+    int32_t* slot_ntok;
     int32_t total_rows, chunk, n_layers, n_heads, vec_per_row, n_chunks;
     ScatterChunk ch[kScatterMaxChunks];
 };
@@ -813,7 +822,9 @@ __global__ void __launch_bounds__(256) kv_scatter_kernel(const __grid_constant__
     const int ci = rest % a.n_chunks, l = rest / a.n_chunks;
     const ScatterChunk c = a.ch[ci];
     const int total = c.n_rows * a.vec_per_row;
-    const long long tile = ((((long long)c.slot * a.n_layers + l) * 2 * a.n_heads + h) * a.chunk) * a.vec_per_row;
+    if (h == 0 && l == 0 && threadIdx.x == 0) a.slot_ntok[c.slot] = c.dst_row + c.n_rows;
+    const long long tile = ((((long long)c.slot * a.n_layers + l) * 2 * a.n_heads + h) * a.chunk +
+                            c.dst_row) * a.vec_per_row;
     const long long vtile = tile + (long long)a.n_heads * a.chunk * a.vec_per_row;
     for (int i = threadIdx.x; i < total; i += blockDim.x) {
         const int r = i / a.vec_per_row, vec = i % a.vec_per_row;
@@ -848,7 +859,7 @@ void* pick_kernel(int chunk, int head_dim) {
 size_t smem_for(int chunk, int head_dim, int stages) {
     const size_t stage = (size_t)2 * chunk * head_dim * 2;
     return (size_t)stages * stage + (size_t)dev::kQRows * head_dim * 2 + 512 + 2 * dev::kMaxStages * 8 +
-           4 * dev::kRing;
+           4 * dev::kRing + 4 * dev::kMaxStages;
 }
 }  // namespace
 
@@ -914,6 +925,7 @@ int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_ro
         a.k = static_cast<const uint4*>(k);
         a.v = static_cast<const uint4*>(v);
         a.pool = static_cast<uint4*>(p.kv);
+        a.slot_ntok = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(p.kv) + pool_tile_bytes(c));
         a.total_rows = total_rows;
         a.chunk = c.chunk;
         a.n_layers = c.n_layers;

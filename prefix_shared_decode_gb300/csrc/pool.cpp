@@ -162,6 +162,94 @@ int pool_insert(Pool& p, int64_t seq_id, const int32_t* tokens, int32_t n,
     return CA_OK;
 }
 
+size_t pool_tile_bytes(const ca_pool_config& c) {
+    return (size_t)c.capacity_slots * c.n_layers * 2 * c.n_heads * c.chunk * c.head_dim * 2;
+}
+
+size_t pool_total_bytes(const ca_pool_config& c) {
+    return pool_tile_bytes(c) + (((size_t)c.capacity_slots * sizeof(int32_t) + 255) & ~size_t(255));
+}
+
+int pool_append(Pool& p, int64_t seq_id, const int32_t* tokens, int32_t n,
+                std::vector<ScatterChunk>* copies, AppendUndo* undo) {
+    if (n <= 0 || !tokens) return CA_ERR_INVALID;
+    auto it = p.seqs.find(seq_id);
+    if (it == p.seqs.end()) return CA_ERR_NOT_FOUND;
+    Sequence& seq = it->second;
+    const int32_t c = p.cfg.chunk;
+    const bool share = !(p.cfg.flags & CA_NO_SHARING);
+    Node* last = seq.path.back();
+    const int32_t fill = std::min(c - last->ntok, n);
+    const int32_t n_new = (n - fill + c - 1) / c;
+    if ((size_t)n_new > p.heap.size()) return CA_ERR_OOM;
+    if (undo) *undo = AppendUndo{last, last->ntok, last->matchable, last->hash, seq.path.size(),
+                                 p.generation, seq.length};
+    if (fill > 0) {
+        // the partial last chunk is private (never matched), so it grows in place
+        std::copy(tokens, tokens + fill, p.tokens.begin() + (size_t)last->slot * c + last->ntok);
+        if (copies) copies->push_back({0, fill, last->slot, last->ntok});
+        last->ntok += fill;
+        if (last->ntok == c && share) {
+            const int32_t* lt = chunk_tokens(p, last);
+            const uint64_t h = chunk_hash(lt, c);
+            if (!find_child(p, last->parent, lt, c, h)) {
+                last->hash = h;
+                last->matchable = true;
+                if (last->parent->index) last->parent->index->emplace(h, last);
+            }
+        }
+    }
+    Node* node = last;
+    for (int32_t i = 0; i < n_new; ++i) {
+        const int32_t a = fill + i * c, len = std::min(c, n - a);
+        const int32_t slot = heap_pop(p.heap);
+        Node* ch = &p.nodes[slot];
+        ch->slot = slot;
+        ch->ntok = len;
+        std::copy(tokens + a, tokens + a + len, p.tokens.begin() + (size_t)slot * c);
+        const uint64_t h = (share && len == c) ? chunk_hash(tokens + a, c) : 0;
+        // an append never matches, and an equal sibling keeps its place
+        ch->matchable = share && len == c && !find_child(p, node, tokens + a, c, h);
+        ch->hash = h;
+        ch->parent = node;
+        ch->children.clear();
+        ch->index.reset();
+        ch->refcount = 1;
+        add_child(node, ch);
+        seq.path.push_back(ch);
+        if (copies) copies->push_back({a, len, slot, 0});
+        node = ch;
+    }
+    seq.length += n;
+    if (n_new > 0) p.generation += 1;
+    return CA_OK;
+}
+
+void pool_undo_append(Pool& p, int64_t seq_id, const AppendUndo& u) {
+    Sequence& seq = p.seqs.at(seq_id);
+    while (seq.path.size() > u.path_size) {
+        Node* x = seq.path.back();
+        seq.path.pop_back();
+        drop_child(x->parent, x);
+        heap_push(p.heap, x->slot);
+        x->children.clear();
+        x->index.reset();
+        x->parent = nullptr;
+        x->matchable = false;
+        x->refcount = 0;
+    }
+    Node* last = u.last;
+    if (last->matchable && !u.matchable && last->parent->index) {
+        auto m = last->parent->index->find(last->hash);
+        if (m != last->parent->index->end() && m->second == last) last->parent->index->erase(m);
+    }
+    last->ntok = u.ntok;
+    last->matchable = u.matchable;
+    last->hash = u.hash;
+    seq.length = u.length;
+    p.generation = u.generation;
+}
+
 int pool_remove(Pool& p, int64_t seq_id) {
     auto it = p.seqs.find(seq_id);
     if (it == p.seqs.end()) return CA_ERR_NOT_FOUND;

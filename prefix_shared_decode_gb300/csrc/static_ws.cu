@@ -74,6 +74,8 @@ extern "C" int ca_decode_attention_static_ws(const ca_pool* pool_, const ca_sche
     a.cta_begin = reinterpret_cast<const int32_t*>(dev + s->layout.cta_begin);
     a.seq_perm = reinterpret_cast<const int32_t*>(dev + s->layout.seq_perm);
     a.pbase = reinterpret_cast<const int32_t*>(dev + s->layout.pbase);
+    a.slot_ntok = reinterpret_cast<const int32_t*>(static_cast<const unsigned char*>(pool->kv) +
+                                                   ca::pool_tile_bytes(pool->cfg));
     a.status = reinterpret_cast<int32_t*>(dev + s->layout.status);
     a.dyn_counter = reinterpret_cast<int32_t*>(dev + s->layout.counter);
     a.dyn_begin = s->plan.cta_begin[s->plan.grid];

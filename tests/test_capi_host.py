@@ -63,10 +63,20 @@ def test_golden_fixture_through_the_c_api(lib):
                 assert pool.seq_slots(op["seq_id"]) == op["slots"]
             elif op["op"] == "remove":
                 pool.remove(op["seq_id"])
+            elif op["op"] == "append":
+                assert pool.append(op["seq_id"], expand(op["tokens"])) == op["n_new"]
+                assert pool.seq_slots(op["seq_id"]) == op["slots"]
+            elif op["op"] == "append_oom":
+                from prefix_shared_decode_gb300 import CAError
+                with pytest.raises(CAError) as e:
+                    pool.append(op["seq_id"], expand(op["tokens"]))
+                assert e.value.name == "CA_ERR_OOM"
             elif op["op"] == "stats":
                 st = pool.stats()
                 assert st["live_slots"] == op["live_slots"]
                 assert st["refcount_sum"] == op["refcount_sum"]
+                if "generation" in op:
+                    assert st["generation"] == op["generation"]
             elif op["op"] == "schedule":
                 t = pool.schedule(op["seq_ids"]).tables()
                 for name in TABLES:
@@ -223,3 +233,46 @@ def test_insert_batch_is_all_or_nothing(lib):
     assert e.value.name == "CA_ERR_INVALID"
     # a later sequence of the batch shares chunks an earlier one created
     assert pool.insert_batch([6, 7], [[3] * 33, [3] * 40]) == [0, 32]
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_scripts_with_appends_bit_exact(lib, seed):
+    """Inserts, appends (filling partial chunks, growing new ones, making
+    chunks shareable) and removes through the C ABI, against the oracle."""
+    from prefix_shared_decode_gb300 import Pool
+    c = 16
+    rng = np.random.default_rng(seed)
+    pool, ref = Pool(1, 2, 64, c, 2000, host_only=True), OracleTrie(c, 2000)
+    seqs = random_segment_sequences(seed, 10, c)
+    for i, t in enumerate(seqs):
+        assert pool.insert(i, t) == ref.insert(i, t)
+    next_id = 100
+    for step in range(40):
+        live = sorted(ref.paths)
+        r = rng.random()
+        if r < 0.55:
+            sid = int(rng.choice(live))
+            add = rng.integers(0, 3, size=int(rng.integers(1, 2 * c))).tolist()
+            assert pool.append(sid, add) == ref.append(sid, add)
+            assert pool.seq_slots(sid) == ref.slots(sid)
+        elif r < 0.8 or len(live) < 3:
+            # a new sequence reusing the tokens of a live one (with a tail), so
+            # chunks filled by appends get matched
+            base = list(ref.paths[int(rng.choice(live))][0].tokens)
+            src = int(rng.choice(live))
+            toks = [t for n in ref.paths[src] for t in n.tokens]
+            toks = toks[: int(rng.integers(1, len(toks) + 1))] + rng.integers(0, 3, size=int(rng.integers(0, c))).tolist()
+            assert pool.match_prefix(toks) == ref.match_prefix(toks)
+            assert pool.insert(next_id, toks) == ref.insert(next_id, toks)
+            assert pool.seq_slots(next_id) == ref.slots(next_id)
+            next_id += 1
+        else:
+            sid = int(rng.choice(live))
+            pool.remove(sid)
+            ref.remove(sid)
+        st = pool.stats()
+        assert (st["live_slots"], st["refcount_sum"], st["generation"]) == (
+            ref.live_slots(), ref.refcount_sum(), ref.generation)
+        if step % 5 == 4:
+            batch = sorted(ref.paths)
+            assert_tables_equal(pool.schedule(batch), build_schedule(ref, batch))

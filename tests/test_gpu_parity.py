@@ -209,6 +209,54 @@ def test_insert_batch_packed_rows(torch_cuda):
         assert_close(got, A.decode_attention(trie, batch, layer, q, 1 / np.sqrt(D)), f"layer {layer}")
 
 
+def test_decode_time_appends(torch_cuda):
+    """One decoded token per sequence per step: appends that only fill a
+    partial chunk keep the cached schedule valid (the kernels read the
+    chunk's token count from the pool), appends that grow a chunk make it
+    stale and it is rebuilt; every step matches the oracle."""
+    from prefix_shared_decode_gb300 import CAError, Pool, decode_attention
+    torch = torch_cuda
+    c, H, D = 32, 4, 128
+    rng = np.random.default_rng(15)
+    seqs = random_segment_sequences(15, 6, c, n_segments=5)
+    pool, trie = Pool(1, H, D, c, 500), OracleTrie(c, 500)
+    for i, toks in enumerate(seqs):
+        k = rng.standard_normal((1, len(toks), H, D), dtype=np.float32).astype(np.float16)
+        v = rng.standard_normal((1, len(toks), H, D), dtype=np.float32).astype(np.float16)
+        trie.insert(i, toks, k, v)
+        pool.insert(i, toks, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+    batch = list(range(6))
+    sched = pool.schedule(batch)
+    cached_steps = rebuilt_steps = 0
+    for step in range(45):
+        grew = False
+        for sid in batch:
+            n_add = 1 if step % 15 else 40               # now and then a multi-token append
+            toks = [10**6 + 1000 * step + sid * 50 + j for j in range(n_add)]
+            k = rng.standard_normal((1, n_add, H, D), dtype=np.float32).astype(np.float16)
+            v = rng.standard_normal((1, n_add, H, D), dtype=np.float32).astype(np.float16)
+            g1 = trie.append(sid, toks, k, v)
+            g2 = pool.append(sid, toks, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+            assert g1 == g2
+            grew |= g2 > 0
+        handle = sched.handle.value
+        if grew:
+            q = torch.zeros((6, H, D), dtype=torch.float16, device="cuda")
+            with pytest.raises(CAError):
+                decode_attention(pool, sched, q)               # stale after growth
+        sched = pool.schedule(batch, reuse=sched)
+        if grew:
+            rebuilt_steps += 1
+        else:
+            assert sched.handle.value == handle
+            cached_steps += 1
+        q = rng.standard_normal((6, H, D), dtype=np.float32).astype(np.float16)
+        got = decode_attention(pool, sched, torch.from_numpy(q).cuda()).cpu().numpy()
+        assert sched.device_status() == 0
+        assert_close(got, A.decode_attention(trie, batch, 0, q, 1 / np.sqrt(D)), f"step {step}")
+    assert cached_steps > 20 and rebuilt_steps > 2
+
+
 def test_host_io_entry_and_repeat_calls(torch_cuda):
     from prefix_shared_decode_gb300 import decode_attention, decode_attention_host
     torch = torch_cuda

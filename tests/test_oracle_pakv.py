@@ -151,6 +151,64 @@ def run_golden_ops(g):
             assert trie.slots(op["seq_id"]) == op["slots"]
         elif op["op"] == "remove":
             trie.remove(op["seq_id"])
+        elif op["op"] == "append":
+            n_new = trie.append(op["seq_id"], op["tokens"])
+            if "n_new" in op:
+                assert n_new == op["n_new"]
+                assert trie.slots(op["seq_id"]) == op["slots"]
+        elif op["op"] == "append_oom":
+            with pytest.raises(OracleError) as e:
+                trie.append(op["seq_id"], op["tokens"])
+            assert e.value.code == "oom"
         elif op["op"] == "stats":
             assert trie.live_slots() == op["live_slots"]
             assert trie.refcount_sum() == op["refcount_sum"]
+            if "generation" in op:
+                assert trie.generation == op["generation"]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_appends_keep_counts_and_context(seed):
+    """After random inserts and appends, every sequence's materialised K/V is
+    its inserted rows followed by its appended rows, and the refcount sum is
+    the sum of ceil(len / c)."""
+    rng = np.random.default_rng(seed)
+    c, L, H, D = 2, 1, 1, 2
+    seqs = random_token_lists(seed, 6, c)
+    trie = OracleTrie(c, 500)
+    full = {}
+    for i, t in enumerate(seqs):
+        k = rng.standard_normal((L, len(t), H, D))
+        trie.insert(i, t, k, k + 1)
+        full[i] = (list(t), k)
+    # identical K/V for identical prefixes: rebuild each context from the trie's
+    # view of the inserted part, then append
+    for i in full:
+        full[i] = (full[i][0], trie.materialize(i)[0][None])
+    for step in range(12):
+        i = int(rng.integers(0, 6))
+        add = rng.integers(0, 3, size=int(rng.integers(1, 6))).tolist()
+        k = rng.standard_normal((L, len(add), H, D))
+        grown = trie.append(i, add, k, k + 1)
+        toks, kk = full[i]
+        full[i] = (toks + add, np.concatenate([kk, k], 1))
+        assert grown == -(-(len(toks) + len(add)) // c) - -(-len(toks) // c)
+    for i, (toks, kk) in full.items():
+        got_k, got_v = trie.materialize(i)
+        np.testing.assert_array_equal(got_k, kk[0])
+        np.testing.assert_array_equal(got_v, kk[0] + 1)
+        assert trie.lengths[i] == len(toks)
+    assert trie.refcount_sum() == sum(-(-len(t) // c) for t, _ in full.values())
+
+
+def test_append_errors_leave_the_trie_unchanged():
+    trie = OracleTrie(2, 3)
+    trie.insert(1, [1, 2, 3])                 # 2 slots, last chunk partial
+    with pytest.raises(OracleError) as e:
+        trie.append(1, [4, 5, 6, 7, 8])       # fills 1, needs 2 more, 1 free
+    assert e.value.code == "oom"
+    assert trie.paths[1][-1].tokens == (3,) and trie.lengths[1] == 3 and len(trie.free) == 1
+    for call, code in [(lambda: trie.append(9, [1]), "not_found"), (lambda: trie.append(1, []), "invalid")]:
+        with pytest.raises(OracleError) as e:
+            call()
+        assert e.value.code == code

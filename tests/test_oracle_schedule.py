@@ -26,7 +26,7 @@ def test_golden_schedule_tables():
     n_sched = 0
     for g in json.load(open(os.path.join(GOLDEN, "schedule_tiny_tree.json")))["scenarios"]:
         n_sched += run_golden_schedules(g)
-    assert n_sched == 4
+    assert n_sched == 6
 
 
 def run_golden_schedules(g):
@@ -37,6 +37,15 @@ def run_golden_schedules(g):
             trie.insert(op["seq_id"], op["tokens"])
         elif op["op"] == "remove":
             trie.remove(op["seq_id"])
+        elif op["op"] == "append":
+            n_new = trie.append(op["seq_id"], op["tokens"])
+            if "n_new" in op:
+                assert n_new == op["n_new"]
+                assert trie.slots(op["seq_id"]) == op["slots"]
+        elif op["op"] == "append_oom":
+            with pytest.raises(OracleError) as e:
+                trie.append(op["seq_id"], op["tokens"])
+            assert e.value.code == "oom"
         elif op["op"] == "schedule":
             t = build_schedule(trie, op["seq_ids"])
             for name in TABLES:
