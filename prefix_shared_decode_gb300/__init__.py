@@ -79,10 +79,18 @@ class Pool:
         return self._h
 
     def kv_view(self):
-        """The device pool as fp16 [slots, L, 2, H, c, D] (a view, no copy)."""
+        """The device pool's K/V tiles as fp16 [slots, L, 2, H, c, D] (a view)."""
         import torch
-        t = self._kv[self._kv_offset:self._kv_offset + self.kv_bytes].view(torch.float16)
+        tiles = self.capacity_slots * self.n_layers * 2 * self.n_heads * self.chunk * self.head_dim * 2
+        t = self._kv[self._kv_offset:self._kv_offset + tiles].view(torch.float16)
         return t.view(self.capacity_slots, self.n_layers, 2, self.n_heads, self.chunk, self.head_dim)
+
+    def slot_ntok_view(self):
+        """The pool's per-slot valid-token counts, int32 [slots] (a view)."""
+        import torch
+        tiles = self.capacity_slots * self.n_layers * 2 * self.n_heads * self.chunk * self.head_dim * 2
+        a = self._kv_offset + tiles
+        return self._kv[a:a + 4 * self.capacity_slots].view(torch.int32)
 
     def match_prefix(self, tokens) -> int:
         tok = _i32(tokens)
