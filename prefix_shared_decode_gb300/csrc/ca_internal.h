@@ -157,8 +157,13 @@ struct Sched {
     std::vector<unsigned char> blob;   // host copy of the device plan
     void* dev = nullptr;               // device plan blob
     size_t dev_bytes = 0;
-    void* host_pinned = nullptr;       // pinned staging of the blob
-    size_t host_pinned_bytes = 0;
+    // Two pinned staging buffers used in turn for the upload, each with an
+    // event marking when its last copy finished, so that building the next
+    // context never waits for the GPU (only for a copy two builds back).
+    void* pinned[2] = {nullptr, nullptr};
+    size_t pinned_bytes[2] = {0, 0};
+    void* pinned_done[2] = {nullptr, nullptr};   // cudaEvent_t
+    int pinned_next = 0;
     void* ev_begin = nullptr;
     void* ev_end = nullptr;
 };

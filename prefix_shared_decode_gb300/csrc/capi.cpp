@@ -47,6 +47,27 @@ size_t pool_bytes(const ca_pool_config& c) { return pool_total_bytes(c); }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? CA_OK : CA_ERR_CUDA; }
 
+// Copy the plan blob to the device through the next pinned staging buffer.
+int upload_plan(Sched& s, cudaStream_t stream) {
+    const int i = s.pinned_next;
+    s.pinned_next ^= 1;
+    cudaEvent_t& done = reinterpret_cast<cudaEvent_t&>(s.pinned_done[i]);
+    if (done && cudaEventSynchronize(done) != cudaSuccess) return CA_ERR_CUDA;  // its last copy
+    if (s.pinned_bytes[i] < s.blob.size()) {
+        if (s.pinned[i]) cudaFreeHost(s.pinned[i]);
+        s.pinned[i] = nullptr;
+        s.pinned_bytes[i] = 0;
+        const size_t want = s.blob.size() + s.blob.size() / 2;
+        if (cudaHostAlloc(&s.pinned[i], want, cudaHostAllocDefault) != cudaSuccess) return CA_ERR_CUDA;
+        s.pinned_bytes[i] = want;
+    }
+    if (!done && cudaEventCreateWithFlags(&done, cudaEventDisableTiming) != cudaSuccess) return CA_ERR_CUDA;
+    std::memcpy(s.pinned[i], s.blob.data(), s.blob.size());
+    if (cudaMemcpyAsync(s.dev, s.pinned[i], s.blob.size(), cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return CA_ERR_CUDA;
+    return cuda_status(cudaEventRecord(done, stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -248,10 +269,10 @@ int ca_build_schedule(ca_pool* pool, const int64_t* seq_ids, int32_t b, uint32_t
                 }
                 s->dev_bytes = s->blob.size();
             }
-            if (cudaMemcpyAsync(s->dev, s->blob.data(), s->blob.size(), cudaMemcpyHostToDevice,
-                                static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+            st = upload_plan(*s, static_cast<cudaStream_t>(stream));
+            if (st) {
                 s->generation = -1;
-                return CA_ERR_CUDA;
+                return st;
             }
         }
         s->generation = pool->generation;
@@ -262,6 +283,13 @@ int ca_build_schedule(ca_pool* pool, const int64_t* seq_ids, int32_t b, uint32_t
 
 int ca_sched_destroy(ca_sched* sched) {
     if (!sched) return CA_OK;
+    for (int i = 0; i < 2; ++i) {
+        if (sched->pinned_done[i]) {
+            cudaEventSynchronize(static_cast<cudaEvent_t>(sched->pinned_done[i]));
+            cudaEventDestroy(static_cast<cudaEvent_t>(sched->pinned_done[i]));
+        }
+        if (sched->pinned[i]) cudaFreeHost(sched->pinned[i]);
+    }
     if (sched->dev) cudaFree(sched->dev);
     delete sched;
     return CA_OK;
