@@ -215,8 +215,9 @@ int ca_export_tables(const ca_sched* sched, int32_t* seq_perm, int32_t* cf_rows,
  * n_chunks.  Any array may be NULL.  Layouts (int32):
  *   units[n_units][12] (kind, head, pos_lo, pos_hi, begin, end, part, qrow,
  *                       n_per_head, base, part_next, 0).  Chunk-first (kind 0):
- *                       chunks [begin, end) of the list for one head and
- *                       positions [pos_lo, pos_hi).  Sequence-first (kind 1):
+ *                       chunks [begin, end) of the list for the heads
+ *                       [head, head + n_per_head) and positions
+ *                       [pos_lo, pos_hi).  Sequence-first (kind 1):
  *                       position pos_lo's (head, chunk) pairs with linear
  *                       index h * n_per_head + j in [begin, end), chunk j at
  *                       list index base + j; its first head uses partial

@@ -20,7 +20,8 @@ namespace ca {
 //
 // A unit is one stretch of chunk-heads that one CTA streams:
 //  * UNIT_CF (chunk-first): rows [c_begin, c_end) of one run of chunks shared
-//    by batch positions [q_lo, q_hi) (at most 64 of them), for one head,
+//    by batch positions [q_lo, q_hi) (at most 64 of them), for the heads
+//    [head, head + n_per_head), one head after the other,
 //    against the batched queries of those positions [ChunkAttention §3.2:
 //    the queries of the sequences that share a chunk form a matrix for
 //    tensor-core matmul].
@@ -47,7 +48,7 @@ struct Unit {
     int32_t c_end;
     int32_t part;      // partial index within the first covered (position, head)
     int32_t qrow;      // SF: row of q / out of its position (seq_perm[q_lo])
-    int32_t n_per_head;  // SF: chunks of the position per head
+    int32_t n_per_head;  // SF: chunks of the position per head; CF: number of heads
     int32_t base;      // SF: ChunkRef index of the position's first chunk
     int32_t part_next; // SF: partial index within the (position, head)s after the first
     int32_t pad;

@@ -456,9 +456,16 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
         // unit a stage carries the id -1.  The plan may be read before the
         // dependency wait; the pool, the queries and the queue counter (reset
         // by the previous call's merge kernel) only after it.
-        auto first_chunk = [&](const Unit& X) {
-            return X.kind == UNIT_SF ? X.base + X.c_begin % X.n_per_head : X.c_begin;
+        // Both kinds walk a linear (head, chunk) range: step L covers chunk
+        // base + L % n of head L / n.  A chunk-first unit's n is its row count
+        // and its range spans its heads.
+        auto lin_n = [](const Unit& X) { return X.kind == UNIT_SF ? X.n_per_head : X.c_end - X.c_begin; };
+        auto lin_base = [](const Unit& X) { return X.kind == UNIT_SF ? X.base : X.c_begin; };
+        auto lin_begin = [&](const Unit& X) { return X.kind == UNIT_SF ? X.c_begin : X.head * lin_n(X); };
+        auto lin_end = [&](const Unit& X) {
+            return X.kind == UNIT_SF ? X.c_end : (X.head + X.n_per_head) * lin_n(X);
         };
+        auto first_chunk = [&](const Unit& X) { return lin_base(X) + lin_begin(X) % lin_n(X); };
         int s_next = u_begin;
         auto claim = [&]() -> int {
             if (s_next < u_end) return s_next++;
@@ -486,12 +493,12 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
             // claim and descriptor latency.
             int nxt = -1;
             bool have_next = false;
-            const int claim_at = max(U.c_begin, U.c_end - 3);
-            const bool sf = U.kind == UNIT_SF;
-            const int n = sf ? U.n_per_head : 1;
-            int h = sf ? U.c_begin / n : U.head;
-            int j = sf ? U.c_begin - h * n : 0;
-            for (int L = U.c_begin; L < U.c_end; ++L, ++it) {
+            const int n = lin_n(U), base = lin_base(U);
+            const int L0 = lin_begin(U), L1 = lin_end(U);
+            const int claim_at = max(L0, L1 - 3);
+            int h = L0 / n;
+            int j = L0 - h * n;
+            for (int L = L0; L < L1; ++L, ++it) {
                 if (!have_next && L >= claim_at) {
                     nxt = claim();
                     if (nxt >= 0) Un = p.units[nxt];
@@ -504,8 +511,8 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 const bool slot_ok = ch.slot >= 0 && ch.slot < p.capacity;
                 const int ntok = slot_ok ? p.slot_ntok[ch.slot] : 0;
                 const int head = h;
-                if (sf && ++j == n) { j = 0; ++h; }
-                if (L + 1 < U.c_end) chn = p.chunks[sf ? U.base + j : L + 1];
+                if (++j == n) { j = 0; ++h; }
+                if (L + 1 < L1) chn = p.chunks[base + j];
                 else if (nxt >= 0) chn = p.chunks[first_chunk(Un)];
                 const int st = it % S;
                 const uint32_t ph = (uint32_t)(it / S) & 1u;
@@ -678,7 +685,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
             }
         } else {
             // ---------------------------- chunk-first ----------------------------
-            const int h = fld(dc, F_HEAD), q_lo = fld(dc, F_QLO), q_hi = fld(dc, F_QHI);
+            const int h0 = fld(dc, F_HEAD), nh = fld(dc, F_N), q_lo = fld(dc, F_QLO), q_hi = fld(dc, F_QHI);
             const int c_begin = fld(dc, F_CB), c_end = fld(dc, F_CE), upart = fld(dc, F_PART);
             if (next_sf) prefetch_q(fld(d0, F_QROW), fld(d0, F_HEAD));
             const int m_rows = q_hi - q_lo;
@@ -687,112 +694,116 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
             if (T * 16 > C) T = C / 16;
             const int rb = w / T, tp = w % T;
             const bool active = rb < rblocks && rb * 16 < m_rows;
-            // Load the unit's queries [q_lo, q_hi) of head h into the swizzled
-            // Q tile; rows past m_rows are zero.
-            for (int idx = threadIdx.x; idx < kQRows * (D / 8); idx += kConsumerWarps * 32) {
-                const int r = idx / (D / 8), k = idx % (D / 8);
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (r < m_rows)
-                    v = *reinterpret_cast<const uint4*>(
-                        p.q + ((size_t)p.seq_perm[q_lo + r] * H + h) * D + k * 8);
-                *reinterpret_cast<uint4*>(qreg + swz(r, k, kQRows)) = v;
-            }
-            consumer_sync();
-            float o[D / 8][4], m[2] = {-INFINITY, -INFINITY}, s[2] = {0.f, 0.f};
-#pragma unroll
-            for (int dt = 0; dt < D / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
-            // Row block rb starts at a multiple of 8 rows, so its swizzle
-            // pattern is the tile's shifted by rb * 16 rows of 128 bytes.
-            const uint32_t qblock = smem_u32(qreg) + rb * 16 * 128;
-            const int NTw = C / T;
-            for (int c = c_begin; c < c_end; ++c, ++it) {
-                const int st = it % S;
-                if (!mbar_wait(full0 + 8 * st, (uint32_t)(it / S) & 1u)) {
-                    set_status(p.status, CA_ERR_TIMEOUT);
-                    return;
+            for (int hh = 0; hh < nh; ++hh) {
+                const int h = h0 + hh;
+                if (hh > 0) consumer_sync();   // the previous head's exchange reads are done
+                // Load the unit's queries [q_lo, q_hi) of head h into the swizzled
+                // Q tile; rows past m_rows are zero.
+                for (int idx = threadIdx.x; idx < kQRows * (D / 8); idx += kConsumerWarps * 32) {
+                    const int r = idx / (D / 8), k = idx % (D / 8);
+                    uint4 v = make_uint4(0, 0, 0, 0);
+                    if (r < m_rows)
+                        v = *reinterpret_cast<const uint4*>(
+                            p.q + ((size_t)p.seq_perm[q_lo + r] * H + h) * D + k * 8);
+                    *reinterpret_cast<uint4*>(qreg + swz(r, k, kQRows)) = v;
                 }
-                if (active) {
-                    const int ntok = stage_ntok[st];
-                    const uint32_t kt = smem_u32(stages + (size_t)st * SM::kStage);
-                    const uint32_t vt = kt + SM::kTile;
-                    if (NTw == 16) {
-                        cf_chunk<C, D, 16>(kt, vt, ntok, tp * 16, qblock, p.scale_log2, m, s, o, lane);
-                    } else if constexpr (C >= 32) {
-                        // 32 tokens at a time keeps the score tile in registers
-                        for (int t0 = tp * NTw; t0 < (tp + 1) * NTw; t0 += 32)
-                            cf_chunk<C, D, 32>(kt, vt, ntok, t0, qblock, p.scale_log2, m, s, o, lane);
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty0 + 8 * st);
-            }
-            // Row sums are per thread so far: reduce over the quad.
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                s[r] += __shfl_xor_sync(kFull, s[r], 1);
-                s[r] += __shfl_xor_sync(kFull, s[r], 2);
-            }
-            // Tree-combine the T warps that split the tokens of one row block,
-            // through the (now free) Q tile: round `half` moves warps with
-            // tp in [half, 2*half) onto tp - half.
-            float* xo = reinterpret_cast<float*>(qreg);
-            for (int half = T / 2; half >= 1; half /= 2) {
                 consumer_sync();
-                const bool writer = active && tp >= half && tp < 2 * half;
-                const int slot = rb * (T / 2) + (tp - half);    // < 2 writers per round
-                if (writer) {
-                    float* dst = xo + (size_t)slot * (16 * D);
+                float o[D / 8][4], m[2] = {-INFINITY, -INFINITY}, s[2] = {0.f, 0.f};
 #pragma unroll
-                    for (int dt = 0; dt < D / 8; ++dt)
+                for (int dt = 0; dt < D / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+                // Row block rb starts at a multiple of 8 rows, so its swizzle
+                // pattern is the tile's shifted by rb * 16 rows of 128 bytes.
+                const uint32_t qblock = smem_u32(qreg) + rb * 16 * 128;
+                const int NTw = C / T;
+                for (int c = c_begin; c < c_end; ++c, ++it) {
+                    const int st = it % S;
+                    if (!mbar_wait(full0 + 8 * st, (uint32_t)(it / S) & 1u)) {
+                        set_status(p.status, CA_ERR_TIMEOUT);
+                        return;
+                    }
+                    if (active) {
+                        const int ntok = stage_ntok[st];
+                        const uint32_t kt = smem_u32(stages + (size_t)st * SM::kStage);
+                        const uint32_t vt = kt + SM::kTile;
+                        if (NTw == 16) {
+                            cf_chunk<C, D, 16>(kt, vt, ntok, tp * 16, qblock, p.scale_log2, m, s, o, lane);
+                        } else if constexpr (C >= 32) {
+                            // 32 tokens at a time keeps the score tile in registers
+                            for (int t0 = tp * NTw; t0 < (tp + 1) * NTw; t0 += 32)
+                                cf_chunk<C, D, 32>(kt, vt, ntok, t0, qblock, p.scale_log2, m, s, o, lane);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty0 + 8 * st);
+                }
+                // Row sums are per thread so far: reduce over the quad.
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) dst[(dt * 4 + e) * 32 + lane] = o[dt][e];
-                    if ((lane & 3) == 0) {
+                for (int r = 0; r < 2; ++r) {
+                    s[r] += __shfl_xor_sync(kFull, s[r], 1);
+                    s[r] += __shfl_xor_sync(kFull, s[r], 2);
+                }
+                // Tree-combine the T warps that split the tokens of one row block,
+                // through the (now free) Q tile: round `half` moves warps with
+                // tp in [half, 2*half) onto tp - half.
+                float* xo = reinterpret_cast<float*>(qreg);
+                for (int half = T / 2; half >= 1; half /= 2) {
+                    consumer_sync();
+                    const bool writer = active && tp >= half && tp < 2 * half;
+                    const int slot = rb * (T / 2) + (tp - half);    // < 2 writers per round
+                    if (writer) {
+                        float* dst = xo + (size_t)slot * (16 * D);
+#pragma unroll
+                        for (int dt = 0; dt < D / 8; ++dt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) dst[(dt * 4 + e) * 32 + lane] = o[dt][e];
+                        if ((lane & 3) == 0) {
+                            const int g = lane >> 2;
+                            xms[slot * 64 + g * 4 + 0] = m[0];
+                            xms[slot * 64 + g * 4 + 1] = s[0];
+                            xms[slot * 64 + g * 4 + 2] = m[1];
+                            xms[slot * 64 + g * 4 + 3] = s[1];
+                        }
+                    }
+                    consumer_sync();
+                    if (active && tp < half) {
+                        const int src = rb * (T / 2) + tp;
+                        const float* so = xo + (size_t)src * (16 * D);
                         const int g = lane >> 2;
-                        xms[slot * 64 + g * 4 + 0] = m[0];
-                        xms[slot * 64 + g * 4 + 1] = s[0];
-                        xms[slot * 64 + g * 4 + 2] = m[1];
-                        xms[slot * 64 + g * 4 + 3] = s[1];
-                    }
-                }
-                consumer_sync();
-                if (active && tp < half) {
-                    const int src = rb * (T / 2) + tp;
-                    const float* so = xo + (size_t)src * (16 * D);
-                    const int g = lane >> 2;
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const float m2 = xms[src * 64 + g * 4 + 2 * r];
-                        const float s2 = xms[src * 64 + g * 4 + 2 * r + 1];
-                        const float M = fmaxf(m[r], m2);
-                        const float Mu = (M == -INFINITY) ? 0.f : M;
-                        const float a1 = ex2(m[r] - Mu), a2 = ex2(m2 - Mu);
-                        s[r] = s[r] * a1 + s2 * a2;
-                        m[r] = M;
+                        for (int r = 0; r < 2; ++r) {
+                            const float m2 = xms[src * 64 + g * 4 + 2 * r];
+                            const float s2 = xms[src * 64 + g * 4 + 2 * r + 1];
+                            const float M = fmaxf(m[r], m2);
+                            const float Mu = (M == -INFINITY) ? 0.f : M;
+                            const float a1 = ex2(m[r] - Mu), a2 = ex2(m2 - Mu);
+                            s[r] = s[r] * a1 + s2 * a2;
+                            m[r] = M;
 #pragma unroll
-                        for (int dt = 0; dt < D / 8; ++dt) {
-                            o[dt][2 * r] = o[dt][2 * r] * a1 + so[(dt * 4 + 2 * r) * 32 + lane] * a2;
-                            o[dt][2 * r + 1] =
-                                o[dt][2 * r + 1] * a1 + so[(dt * 4 + 2 * r + 1) * 32 + lane] * a2;
+                            for (int dt = 0; dt < D / 8; ++dt) {
+                                o[dt][2 * r] = o[dt][2 * r] * a1 + so[(dt * 4 + 2 * r) * 32 + lane] * a2;
+                                o[dt][2 * r + 1] =
+                                    o[dt][2 * r + 1] * a1 + so[(dt * 4 + 2 * r + 1) * 32 + lane] * a2;
+                            }
                         }
                     }
                 }
-            }
-            // Warps with tp == 0 now hold their row block: write one partial
-            // per valid row.
-            if (active && tp == 0) {
-                const int g = lane >> 2, t4 = lane & 3;
+                // Warps with tp == 0 now hold their row block: write one partial
+                // per valid row.
+                if (active && tp == 0) {
+                    const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const int row = rb * 16 + g + 8 * r;
-                    if (row < m_rows) {
-                        const int pos = q_lo + row;
-                        const int pid = p.pbase[pos * H + h] + upart;
-                        float* dst = p.part_o + (size_t)pid * D;
+                    for (int r = 0; r < 2; ++r) {
+                        const int row = rb * 16 + g + 8 * r;
+                        if (row < m_rows) {
+                            const int pos = q_lo + row;
+                            const int pid = p.pbase[pos * H + h] + upart;
+                            float* dst = p.part_o + (size_t)pid * D;
 #pragma unroll
-                        for (int dt = 0; dt < D / 8; ++dt)
-                            *reinterpret_cast<float2*>(dst + dt * 8 + 2 * t4) =
-                                make_float2(o[dt][2 * r], o[dt][2 * r + 1]);
-                        if (t4 == 0) p.part_ms[pid] = make_float2(m[r], s[r]);
+                            for (int dt = 0; dt < D / 8; ++dt)
+                                *reinterpret_cast<float2*>(dst + dt * 8 + 2 * t4) =
+                                    make_float2(o[dt][2 * r], o[dt][2 * r + 1]);
+                            if (t4 == 0) p.part_ms[pid] = make_float2(m[r], s[r]);
+                        }
                     }
                 }
             }

@@ -203,7 +203,7 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
     std::vector<int32_t> pieces(U, 0);
     struct CfUnit { Unit u; double cost; };
     std::vector<CfUnit> cf;
-    cf.reserve((size_t)U * H * 4);
+    cf.reserve((size_t)U * 8);
     for (int32_t u = 0; u < U; ++u) {
         const int32_t row0 = t.cf_runs[4 * u], nrows = t.cf_runs[4 * u + 1];
         const int32_t lo = t.cf_runs[4 * u + 2], hi = t.cf_runs[4 * u + 3], m = hi - lo;
@@ -224,9 +224,16 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
             for (int32_t k = 0; k < np; ++k) {
                 const int32_t ra = row0 + (int32_t)((int64_t)nrows * k / np);
                 const int32_t rb = row0 + (int32_t)((int64_t)nrows * (k + 1) / np);
-                for (int32_t h = 0; h < H; ++h) {
-                    Unit x{UNIT_CF, h, qa, qb, ra, rb, k, 0, 0, 0, 0, 0};
-                    cf.push_back({x, (rb - ra) * (1.0 + kCfComputePer16 * ((qb - qa + 15) / 16))});
+                // A unit covers a range of heads (the kernel reloads the query
+                // tile per head), as many as keep it within a CTA's share.
+                const double head_cost = (rb - ra) * (1.0 + kCfComputePer16 * ((qb - qa + 15) / 16));
+                const int32_t hp = std::max(1, std::min(H, (int32_t)(avg / head_cost)));
+                const int32_t nparts = (H + hp - 1) / hp;
+                for (int32_t hk = 0; hk < nparts; ++hk) {
+                    const int32_t h0 = (int32_t)((int64_t)H * hk / nparts);
+                    const int32_t h1 = (int32_t)((int64_t)H * (hk + 1) / nparts);
+                    Unit x{UNIT_CF, h0, qa, qb, ra, rb, k, 0, h1 - h0, 0, 0, 0};
+                    cf.push_back({x, (h1 - h0) * head_cost});
                 }
             }
         }

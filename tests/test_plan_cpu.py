@@ -34,9 +34,10 @@ def simulate(plan, tables, trie, q, scale, H):
     for kind, h, lo, hi, cb, ce, part, qrow, n, base, part_next, _ in plan["units"]:
         assert lo < hi and cb < ce
         if kind == 0:
-            assert 0 <= h < H and hi - lo <= 64
-            for pos in range(lo, hi):
-                emit(pos, h, part, plan["chunks"][cb:ce])
+            assert 0 <= h and h + n <= H and n >= 1 and hi - lo <= 64
+            for hh in range(h, h + n):
+                for pos in range(lo, hi):
+                    emit(pos, hh, part, plan["chunks"][cb:ce])
         else:
             assert hi == lo + 1 and qrow == perm[lo] and h == cb // n
             L = cb
