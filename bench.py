@@ -189,7 +189,8 @@ def run_ours(args):
     wl = workloads.make(args.workload)
     L, H, D, c = wl.n_layers, wl.n_heads, wl.head_dim, wl.chunk
     t0 = time.perf_counter()
-    pool = Pool(L, H, D, c, capacity_for(wl, headroom=1.5))
+    HK = wl.kv_heads
+    pool = Pool(L, H, D, c, capacity_for(wl, headroom=1.5), n_kv_heads=HK)
     staging = {}
     for sid in wl.seq_ids():
         insert_sequence(pool, wl, sid, staging=staging)
@@ -226,8 +227,8 @@ def run_ours(args):
                                wl.seq_ids()))
         nmax = max(int(p[3].sum()) for p in plan_churn)
         g = torch.Generator(device=dev).manual_seed(wl.seed)
-        kblk = torch.randn((L, nmax, H, D), generator=g, device=dev).half()
-        vblk = torch.randn((L, nmax, H, D), generator=g, device=dev).half()
+        kblk = torch.randn((L, nmax, HK, D), generator=g, device=dev).half()
+        vblk = torch.randn((L, nmax, HK, D), generator=g, device=dev).half()
         kv_views = [(kblk[:, :int(p[3].sum())], vblk[:, :int(p[3].sum())]) for p in plan_churn]
 
     def step(i):
@@ -336,7 +337,7 @@ def run_ours(args):
         no_tpp = pool.schedule(batch, no_tpp=True)
         us_no_tpp = time_calls(pool, no_tpp)
         del no_tpp
-        flat = Pool(L, H, D, c, capacity_for(wl, headroom=1.05), no_sharing=True)
+        flat = Pool(L, H, D, c, capacity_for(wl, headroom=1.05), no_sharing=True, n_kv_heads=HK)
         for sid in batch:
             insert_sequence(flat, wl, sid, staging=staging)
         us_flat = time_calls(flat, flat.schedule(batch))
@@ -352,7 +353,7 @@ def run_ours(args):
         return
 
     unique_tokens = wl.unique_tokens()
-    kv_bytes = unique_tokens * H * D * 2 * 2                   # one layer's K and V, fp16
+    kv_bytes = unique_tokens * HK * D * 2 * 2                  # one layer's K and V, fp16
     io_bytes = 2 * b * H * D * 2                               # q in, out
     alg_bytes = kv_bytes + io_bytes
     us = ms_per_step * 1e3
@@ -372,6 +373,7 @@ def run_ours(args):
         "dtype": "f16 (fp32 accumulate)",
         "data": "synthetic (seeded N(0,1) fp16 Q/K/V; token segments shaped like the pages' shared system prompts)",
         "config": {"workload": wl.name, "description": wl.description, "batch": b, "n_heads": H,
+                   "n_kv_heads": HK,
                    "head_dim": D, "chunk": c, "layers_per_call": 1,
                    "unique_kv_tokens": unique_tokens, "unique_kv_bytes": kv_bytes,
                    "l2": "no flush: steps run back to back; inputs exceed L2 (%d MB vs %d MB L2) and "

@@ -71,14 +71,18 @@ typedef struct ca_sched ca_sched;
 
 /* Shape of a pool.  head_dim must be 64 or 128, chunk 16, 32 or 64 tokens
  * (the paper's kernel default is 64 [CA §4.1]); n_layers, n_heads and
- * capacity_slots >= 1. */
+ * capacity_slots >= 1.  n_kv_heads: key/value heads stored in the pool
+ * (grouped-query attention: query head h reads key/value head
+ * h / (n_heads / n_kv_heads)); 0 means n_heads; n_heads must be a multiple
+ * of it and the group n_heads / n_kv_heads at most 64. */
 typedef struct {
     int32_t  n_layers;
-    int32_t  n_heads;
+    int32_t  n_heads;         /* query heads (q and out)                       */
     int32_t  head_dim;
     int32_t  chunk;           /* c: tokens per chunk                           */
     int32_t  capacity_slots;  /* chunk slots in the device pool                */
     uint32_t flags;           /* CA_NO_SHARING or 0                            */
+    int32_t  n_kv_heads;      /* key/value heads (0: n_heads)                  */
 } ca_pool_config;
 
 typedef struct {
@@ -90,7 +94,7 @@ typedef struct {
 } ca_stats;
 
 /* ---- pool ----------------------------------------------------------------
- * Device layout: the K/V tiles (row-major, fp16)
+ * Device layout: the K/V tiles (row-major, fp16, head = key/value head)
  *     kv[slot][layer][K|V][head][c][head_dim]
  * so one chunk of one head is a contiguous c x head_dim tile (16 KiB at
  * c = 64, D = 128) that the kernels fetch whole with TMA; then one int32 per
@@ -121,7 +125,7 @@ int ca_match_prefix(const ca_pool* pool, const int32_t* tokens, int32_t n,
  * sequences add paths].  Full chunks that match the tree along the path gain a
  * reference; every other chunk (and always the trailing partial chunk) gets a
  * new slot, lowest free index first, and its K/V rows are copied on `stream`
- * from k_dev / v_dev: fp16 [n_layers][n][n_heads][head_dim], contiguous, 16-byte
+ * from k_dev / v_dev: fp16 [n_layers][n][n_kv_heads][head_dim], contiguous, 16-byte
  * aligned.  Rows of matched tokens are not read (the first inserter's rows are
  * kept).  k_dev/v_dev must be NULL for a host-only pool and non-NULL
  * otherwise.  n_shared_out (may be NULL) receives the matched token count.
@@ -136,7 +140,7 @@ int ca_insert_tokens(ca_pool* pool, int64_t seq_id, const int32_t* tokens,
  * in order (a later sequence may share chunks an earlier one created), but
  * with one call and one KV copy launch per 128 new chunks.
  *   tokens   int32, the n_seqs token lists concatenated; lengths[i] >= 1
- *   k_dev / v_dev  fp16 [n_layers][sum(lengths)][n_heads][head_dim]: the
+ *   k_dev / v_dev  fp16 [n_layers][sum(lengths)][n_kv_heads][head_dim]: the
  *            rows of sequence i start at row lengths[0] + ... + lengths[i-1]
  *            (a packed prefill output); rows of matched tokens are not read
  *   n_shared_out   int32[n_seqs] or NULL
@@ -152,7 +156,7 @@ int ca_insert_batch(ca_pool* pool, int32_t n_seqs, const int64_t* seq_ids,
  * partial last chunk in place, then grow new private chunks (lowest free
  * slots first); an append never matches existing chunks.  A chunk that
  * becomes full becomes shareable by later inserts (unless its parent already
- * holds an equal one).  k_dev / v_dev: fp16 [n_layers][n][n_heads][head_dim]
+ * holds an equal one).  k_dev / v_dev: fp16 [n_layers][n][n_kv_heads][head_dim]
  * for the n appended tokens.  Filling the partial chunk does not change the
  * tree's structure, so schedules stay valid (their exported ntok values are
  * as of their build; the kernels read current counts from the pool); growing

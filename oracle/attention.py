@@ -9,7 +9,10 @@ FlashAttention-style online-softmax compatibility]:
     out_{i,h} = sum_t softmax_t(scale * q_{i,h} . k_{t,h}) v_{t,h}
 
 over every token t of sequence i's context (reading R7: the tokens inserted
-for it; no causal mask inside one decode query).  ``decode_attention`` is that
+for it; no causal mask inside one decode query).  With grouped-query
+attention (fewer key/value heads than query heads, the "other model
+configurations" of [CA-summary §7]) query head h reads key/value head
+h // (Hq / Hkv).  ``decode_attention`` is that
 definition written out.  The partial triple and the merge follow the pages'
 statement of the two phases:
 
@@ -35,16 +38,27 @@ import numpy as np
 from .pakv import OracleError, OracleTrie
 
 
+def kv_head_of(n_q_heads: int, n_kv_heads: int) -> np.ndarray:
+    """Grouped-query attention: query head h reads key/value head h // G,
+    G = n_q_heads / n_kv_heads (G = 1 is multi-head attention)."""
+    if n_kv_heads <= 0 or n_q_heads % n_kv_heads:
+        raise OracleError("invalid", "query heads must be a multiple of key/value heads")
+    return np.arange(n_q_heads) // (n_q_heads // n_kv_heads)
+
+
 def softmax_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float) -> np.ndarray:
     """One query per head against a dense context.
 
-    q [H, D]; k, v [n, H, D]  ->  [H, D], all float64.
+    q [Hq, D]; k, v [n, Hkv, D] with Hq a multiple of Hkv  ->  [Hq, D],
+    all float64.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     if k.shape[0] == 0:
         raise OracleError("invalid", "empty context")
+    g = kv_head_of(q.shape[0], k.shape[1])
+    k, v = k[:, g], v[:, g]                             # each query head's key/value head
     x = scale * np.einsum("hd,nhd->hn", q, k)          # scores [H, n]
     w = np.exp(x - x.max(axis=1, keepdims=True))        # softmax numerators
     w /= w.sum(axis=1, keepdims=True)
@@ -72,11 +86,14 @@ def partial(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float):
     H, D = q.shape
     if k.shape[0] == 0:
         return np.zeros((H, D)), np.full(H, -np.inf), np.zeros(H)
-    x = scale * np.einsum("hd,nhd->hn", q, np.asarray(k, dtype=np.float64))
+    g = kv_head_of(H, k.shape[1])
+    k = np.asarray(k, dtype=np.float64)[:, g]
+    v = np.asarray(v, dtype=np.float64)[:, g]
+    x = scale * np.einsum("hd,nhd->hn", q, k)
     m = x.max(axis=1)
     e = np.exp(x - m[:, None])
     s = e.sum(axis=1)
-    o = np.einsum("hn,nhd->hd", e, np.asarray(v, dtype=np.float64))
+    o = np.einsum("hn,nhd->hd", e, v)
     return o, m, s
 
 

@@ -44,11 +44,12 @@ class Pool:
 
     def __init__(self, n_layers: int, n_heads: int, head_dim: int, chunk: int,
                  capacity_slots: int, no_sharing: bool = False, host_only: bool = False,
-                 device=None):
+                 device=None, n_kv_heads: int | None = None):
         L = capi.lib()
         self.cfg = capi.PoolConfig(n_layers, n_heads, head_dim, chunk, capacity_slots,
-                                   capi.CA_NO_SHARING if no_sharing else 0)
+                                   capi.CA_NO_SHARING if no_sharing else 0, n_kv_heads or 0)
         self.n_layers, self.n_heads, self.head_dim, self.chunk = n_layers, n_heads, head_dim, chunk
+        self.n_kv_heads = n_kv_heads or n_heads
         self.capacity_slots = capacity_slots
         nbytes = C.c_size_t()
         check(L.ca_pool_bytes(C.byref(self.cfg), C.byref(nbytes)), "ca_pool_bytes")
@@ -81,14 +82,14 @@ class Pool:
     def kv_view(self):
         """The device pool's K/V tiles as fp16 [slots, L, 2, H, c, D] (a view)."""
         import torch
-        tiles = self.capacity_slots * self.n_layers * 2 * self.n_heads * self.chunk * self.head_dim * 2
+        tiles = self.capacity_slots * self.n_layers * 2 * self.n_kv_heads * self.chunk * self.head_dim * 2
         t = self._kv[self._kv_offset:self._kv_offset + tiles].view(torch.float16)
-        return t.view(self.capacity_slots, self.n_layers, 2, self.n_heads, self.chunk, self.head_dim)
+        return t.view(self.capacity_slots, self.n_layers, 2, self.n_kv_heads, self.chunk, self.head_dim)
 
     def slot_ntok_view(self):
         """The pool's per-slot valid-token counts, int32 [slots] (a view)."""
         import torch
-        tiles = self.capacity_slots * self.n_layers * 2 * self.n_heads * self.chunk * self.head_dim * 2
+        tiles = self.capacity_slots * self.n_layers * 2 * self.n_kv_heads * self.chunk * self.head_dim * 2
         a = self._kv_offset + tiles
         return self._kv[a:a + 4 * self.capacity_slots].view(torch.int32)
 
@@ -100,13 +101,13 @@ class Pool:
         return n.value
 
     def insert(self, seq_id: int, tokens, k=None, v=None, stream=None) -> int:
-        """Insert a sequence; k, v are fp16 device tensors [L, n, H, D]
+        """Insert a sequence; k, v are fp16 device tensors [L, n, Hkv, D]
         (None for a host-only pool).  Returns the number of shared tokens."""
         tok = _i32(tokens)
         kp = vp = None
         if k is not None:
             assert k.is_contiguous() and v.is_contiguous()
-            assert tuple(k.shape) == (self.n_layers, len(tok), self.n_heads, self.head_dim)
+            assert tuple(k.shape) == (self.n_layers, len(tok), self.n_kv_heads, self.head_dim)
             kp, vp = k.data_ptr(), v.data_ptr()
         shared = C.c_int32()
         check(capi.lib().ca_insert_tokens(self._h, int(seq_id), tok.ctypes.data_as(C.POINTER(C.c_int32)),
@@ -131,7 +132,7 @@ class Pool:
         kp = vp = None
         if k is not None:
             assert k.is_contiguous() and v.is_contiguous()
-            assert tuple(k.shape) == (self.n_layers, int(lens.sum()), self.n_heads, self.head_dim)
+            assert tuple(k.shape) == (self.n_layers, int(lens.sum()), self.n_kv_heads, self.head_dim)
             kp, vp = k.data_ptr(), v.data_ptr()
         shared = np.zeros(len(ids), dtype=np.int32)
         P32 = C.POINTER(C.c_int32)
@@ -149,7 +150,7 @@ class Pool:
         kp = vp = None
         if k is not None:
             assert k.is_contiguous() and v.is_contiguous()
-            assert tuple(k.shape) == (self.n_layers, len(tok), self.n_heads, self.head_dim)
+            assert tuple(k.shape) == (self.n_layers, len(tok), self.n_kv_heads, self.head_dim)
             kp, vp = k.data_ptr(), v.data_ptr()
         grown = C.c_int32()
         check(capi.lib().ca_append_tokens(self._h, int(seq_id), tok.ctypes.data_as(C.POINTER(C.c_int32)),

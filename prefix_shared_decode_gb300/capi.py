@@ -33,7 +33,8 @@ EXPORTS = [
 
 class PoolConfig(C.Structure):
     _fields_ = [("n_layers", C.c_int32), ("n_heads", C.c_int32), ("head_dim", C.c_int32),
-                ("chunk", C.c_int32), ("capacity_slots", C.c_int32), ("flags", C.c_uint32)]
+                ("chunk", C.c_int32), ("capacity_slots", C.c_int32), ("flags", C.c_uint32),
+                ("n_kv_heads", C.c_int32)]
 
 
 class Stats(C.Structure):

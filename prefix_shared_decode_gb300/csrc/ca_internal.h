@@ -75,7 +75,8 @@ struct AttnParams {
     uint16_t* out;               // fp16 [b][H][D]
     float* part_o;               // [P][D] unnormalised partial outputs
     float2* part_ms;             // [P] (running max in log2 units, sum of exp2)
-    int32_t n_layers, n_heads, layer, capacity;
+    int32_t n_layers, n_heads, layer, capacity;   // n_heads: query heads
+    int32_t n_kv_heads, group;                     // key/value heads, n_heads / n_kv_heads
     float scale_log2;            // scale * log2(e)
     int32_t n_stages;
 };
@@ -175,6 +176,10 @@ struct Sched {
 struct ScatterChunk {
     int32_t src_row, n_rows, slot, dst_row;
 };
+
+// Key/value heads of a pool (grouped-query attention; 0 in the config means
+// one per query head).
+inline int32_t kv_heads(const ca_pool_config& c) { return c.n_kv_heads > 0 ? c.n_kv_heads : c.n_heads; }
 
 // Device bytes of the pool: the K/V tiles, then the per-slot token counts.
 size_t pool_tile_bytes(const ca_pool_config& c);

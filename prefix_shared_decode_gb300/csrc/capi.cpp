@@ -37,8 +37,10 @@ int check_cfg(const ca_pool_config* c) {
     if (c->head_dim != 64 && c->head_dim != 128) return CA_ERR_UNSUPPORTED;
     if (c->chunk != 16 && c->chunk != 32 && c->chunk != 64) return CA_ERR_UNSUPPORTED;
     if (c->flags & ~CA_NO_SHARING) return CA_ERR_INVALID;
+    if (c->n_kv_heads < 0 || (c->n_kv_heads > 0 && c->n_heads % c->n_kv_heads)) return CA_ERR_INVALID;
+    if (c->n_heads / kv_heads(*c) > 64) return CA_ERR_UNSUPPORTED;
     // TMA row coordinates are 32-bit.
-    const long double rows = (long double)c->capacity_slots * c->n_layers * 2 * c->n_heads * c->chunk;
+    const long double rows = (long double)c->capacity_slots * c->n_layers * 2 * kv_heads(*c) * c->chunk;
     if (rows > 2147483647.0L) return CA_ERR_UNSUPPORTED;
     return CA_OK;
 }
@@ -384,6 +386,8 @@ static int decode_launch(const ca_pool* pool, const ca_sched* s, int32_t layer, 
     a.part_ms = reinterpret_cast<float2*>(ws + s->ws.part_ms);
     a.n_layers = pool->cfg.n_layers;
     a.n_heads = pool->cfg.n_heads;
+    a.n_kv_heads = kv_heads(pool->cfg);
+    a.group = pool->cfg.n_heads / a.n_kv_heads;
     a.layer = layer;
     a.capacity = pool->cfg.capacity_slots;
     a.scale_log2 = scale * 1.4426950408889634f;

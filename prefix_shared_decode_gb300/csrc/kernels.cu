@@ -439,7 +439,9 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
     __syncthreads();
 
     const int u_begin = p.cta_begin[blockIdx.x], u_end = p.cta_begin[blockIdx.x + 1];
-    const int H = p.n_heads;
+    const int H = p.n_heads;            // query heads (q, out, partials)
+    const int HK = p.n_kv_heads;        // key/value heads (pool tiles, units)
+    const int G = p.group;              // query heads per key/value head
 
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
@@ -522,7 +524,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     break;
                 }
                 const uint32_t fb = full0 + 8 * st;
-                if (!slot_ok || head < 0 || head >= H) {
+                if (!slot_ok || head < 0 || head >= HK) {
                     set_status(p.status, CA_ERR_DEVICE_BOUNDS);
                     stage_ntok[st] = 0;
                     mbar_arrive(fb);          // release the consumers without data
@@ -531,8 +533,8 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 stage_ntok[st] = min(max(ntok, 0), C);
                 mbar_expect_tx(fb, SM::kStage);
                 const uint32_t dst = smem_u32(stages + (size_t)st * SM::kStage);
-                const int rowK = (((ch.slot * p.n_layers + p.layer) * 2 + 0) * H + head) * C;
-                const int rowV = rowK + H * C;
+                const int rowK = (((ch.slot * p.n_layers + p.layer) * 2 + 0) * HK + head) * C;
+                const int rowV = rowK + HK * C;
 #pragma unroll
                 for (int bx = 0; bx < BOXES; ++bx) {
                     tma_load_2d(dst + bx * C * 128, &tmap, bx * 64, rowK, fb, pol);
@@ -614,7 +616,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
         const int32_t d0 = dn;
         const bool next_sf = next_static && fld(d0, F_KIND) == UNIT_SF;
         consumer_sync();   // previous unit (and its exchange reads) finished
-        if (fld(dc, F_KIND) == UNIT_SF) {
+        if (fld(dc, F_KIND) == UNIT_SF && G == 1) {
             const int pos = fld(dc, F_QLO), n = fld(dc, F_N), base = fld(dc, F_BASE);
             const int qrow = fld(dc, F_QROW), c_end = fld(dc, F_CE), part_next = fld(dc, F_PNEXT);
             int L = fld(dc, F_CB), h = fld(dc, F_HEAD), part = fld(dc, F_PART);
@@ -684,27 +686,40 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 part = part_next;
             }
         } else {
-            // ---------------------------- chunk-first ----------------------------
-            const int h0 = fld(dc, F_HEAD), nh = fld(dc, F_N), q_lo = fld(dc, F_QLO), q_hi = fld(dc, F_QHI);
-            const int c_begin = fld(dc, F_CB), c_end = fld(dc, F_CE), upart = fld(dc, F_PART);
+            // ------------------------- tensor-core path -------------------------
+            // Chunk-first units, and sequence-first units when several query
+            // heads share a key/value head (G > 1).  Rows of the query tile are
+            // (position, query head) pairs: row r is position q_lo + r / G,
+            // query head kvh * G + r % G.  The unit is walked as its linear
+            // (key/value head, chunk) range, one head's piece at a time.
+            const bool is_sf = fld(dc, F_KIND) == UNIT_SF;
+            const int q_lo = fld(dc, F_QLO), q_hi = fld(dc, F_QHI);
+            const int cb = fld(dc, F_CB), ce = fld(dc, F_CE);
+            const int n = is_sf ? fld(dc, F_N) : ce - cb;
+            const int base = is_sf ? fld(dc, F_BASE) : cb;
+            int L = is_sf ? cb : fld(dc, F_HEAD) * n;
+            const int L_end = is_sf ? ce : (fld(dc, F_HEAD) + fld(dc, F_N)) * n;
+            const int part_first = fld(dc, F_PART), part_rest = is_sf ? fld(dc, F_PNEXT) : part_first;
             if (next_sf) prefetch_q(fld(d0, F_QROW), fld(d0, F_HEAD));
-            const int m_rows = q_hi - q_lo;
+            const int m_rows = (q_hi - q_lo) * G;
             const int rblocks = m_rows <= 16 ? 1 : m_rows <= 32 ? 2 : 4;
             int T = kConsumerWarps / rblocks;            // warps splitting the tokens
             if (T * 16 > C) T = C / 16;
             const int rb = w / T, tp = w % T;
             const bool active = rb < rblocks && rb * 16 < m_rows;
-            for (int hh = 0; hh < nh; ++hh) {
-                const int h = h0 + hh;
-                if (hh > 0) consumer_sync();   // the previous head's exchange reads are done
-                // Load the unit's queries [q_lo, q_hi) of head h into the swizzled
-                // Q tile; rows past m_rows are zero.
+            for (bool first = true; L < L_end; first = false) {
+                const int kvh = L / n;
+                const int seg_end = min(L_end, (kvh + 1) * n);
+                const int upart = first ? part_first : part_rest;
+                if (!first) consumer_sync();   // the previous head's exchange reads are done
+                // Load the rows' queries into the swizzled Q tile; rows past
+                // m_rows are zero.
                 for (int idx = threadIdx.x; idx < kQRows * (D / 8); idx += kConsumerWarps * 32) {
                     const int r = idx / (D / 8), k = idx % (D / 8);
                     uint4 v = make_uint4(0, 0, 0, 0);
                     if (r < m_rows)
                         v = *reinterpret_cast<const uint4*>(
-                            p.q + ((size_t)p.seq_perm[q_lo + r] * H + h) * D + k * 8);
+                            p.q + ((size_t)p.seq_perm[q_lo + r / G] * H + kvh * G + r % G) * D + k * 8);
                     *reinterpret_cast<uint4*>(qreg + swz(r, k, kQRows)) = v;
                 }
                 consumer_sync();
@@ -715,7 +730,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 // pattern is the tile's shifted by rb * 16 rows of 128 bytes.
                 const uint32_t qblock = smem_u32(qreg) + rb * 16 * 128;
                 const int NTw = C / T;
-                for (int c = c_begin; c < c_end; ++c, ++it) {
+                for (; L < seg_end; ++L, ++it) {
                     const int st = it % S;
                     if (!mbar_wait(full0 + 8 * st, (uint32_t)(it / S) & 1u)) {
                         set_status(p.status, CA_ERR_TIMEOUT);
@@ -795,8 +810,8 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     for (int r = 0; r < 2; ++r) {
                         const int row = rb * 16 + g + 8 * r;
                         if (row < m_rows) {
-                            const int pos = q_lo + row;
-                            const int pid = p.pbase[pos * H + h] + upart;
+                            const int pos = q_lo + row / G, qh = kvh * G + row % G;
+                            const int pid = p.pbase[pos * H + qh] + upart;
                             float* dst = p.part_o + (size_t)pid * D;
 #pragma unroll
                             for (int dt = 0; dt < D / 8; ++dt)
@@ -914,7 +929,7 @@ int make_tensor_map(Pool& p) {
     const ca_pool_config& c = p.cfg;
     // The pool as a 2-D tensor: rows of head_dim fp16, one row per
     // (slot, layer, K|V, head, token-in-chunk).
-    const cuuint64_t rows = (cuuint64_t)c.capacity_slots * c.n_layers * 2 * c.n_heads * c.chunk;
+    const cuuint64_t rows = (cuuint64_t)c.capacity_slots * c.n_layers * 2 * kv_heads(c) * c.chunk;
     const cuuint64_t dims[2] = {(cuuint64_t)c.head_dim, rows};
     const cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * 2};
     const cuuint32_t box[2] = {64, (cuuint32_t)c.chunk};
@@ -940,11 +955,11 @@ int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_ro
         a.total_rows = total_rows;
         a.chunk = c.chunk;
         a.n_layers = c.n_layers;
-        a.n_heads = c.n_heads;
+        a.n_heads = kv_heads(c);
         a.vec_per_row = c.head_dim / 8;
         a.n_chunks = (int32_t)cnt;
         std::copy(chunks.begin() + i, chunks.begin() + i + cnt, a.ch);
-        const unsigned blocks = (unsigned)(cnt * c.n_layers * c.n_heads);
+        const unsigned blocks = (unsigned)(cnt * c.n_layers * a.n_heads);
         dev::kv_scatter_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
         if (cudaGetLastError() != cudaSuccess) return CA_ERR_CUDA;
     }

@@ -171,7 +171,13 @@ constexpr int32_t kTailUnitMin = 2, kTailUnitMax = 8;
 }  // namespace
 
 void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
-    const int32_t H = p.cfg.n_heads, D = p.cfg.head_dim, c = p.cfg.chunk, b = t.b;
+    // Work is per key/value head (H of them); partials are per query head
+    // (HQ = H * G; G = 1 is multi-head attention).  With G > 1 a
+    // sequence-first chunk-head multiplies G query rows, on tensor cores.
+    const int32_t HQ = p.cfg.n_heads, H = kv_heads(p.cfg), G = HQ / H;
+    const int32_t D = p.cfg.head_dim, c = p.cfg.chunk, b = t.b;
+    const double sf_cost = (G == 1) ? 1.0 : 1.0 + kCfComputePer16 * ((G + 15) / 16);
+    auto rows_cost = [&](int32_t m_rows) { return (1.0 + kCfComputePer16 * ((m_rows + 15) / 16)) / sf_cost; };
     const int32_t R = (int32_t)(t.cf_rows.size() / 4), U = (int32_t)(t.cf_runs.size() / 4);
     plan.chunks.clear();
     plan.units.clear();
@@ -190,7 +196,7 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
     double cf_total = 0;
     for (int32_t u = 0; u < U; ++u) {
         const int32_t nrows = t.cf_runs[4 * u + 1], m = t.cf_runs[4 * u + 3] - t.cf_runs[4 * u + 2];
-        cf_total += (double)nrows * H * (1.0 + kCfComputePer16 * ((m + 15) / 16));
+        cf_total += (double)nrows * H * rows_cost(std::min(m, kMaxCfQueries / G) * G);
     }
     const int32_t tiles_ceiling = (int32_t)std::max(1.0, sf_total + cf_total);
     grid = std::max(1, std::min(grid, tiles_ceiling));
@@ -207,13 +213,15 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
     for (int32_t u = 0; u < U; ++u) {
         const int32_t row0 = t.cf_runs[4 * u], nrows = t.cf_runs[4 * u + 1];
         const int32_t lo = t.cf_runs[4 * u + 2], hi = t.cf_runs[4 * u + 3], m = hi - lo;
-        const int32_t ngroups = (m + kMaxCfQueries - 1) / kMaxCfQueries;
+        // query groups of at most 64 (position, query head) rows
+        const int32_t max_pos = std::max(1, kMaxCfQueries / G);
+        const int32_t ngroups = (m + max_pos - 1) / max_pos;
         const int32_t mg = (m + ngroups - 1) / ngroups;
-        const double row_cost = 1.0 + kCfComputePer16 * ((mg + 15) / 16);
-        // Enough rows per piece that partial traffic (2 x mg x (D+2) floats)
-        // stays under 1/8 of the piece's KV bytes; few enough that one piece
-        // does not outweigh a CTA's share.
-        const int32_t rmin = std::max(1, (int32_t)((16.0 * mg * (D + 2)) / ((double)c * D) + 0.999));
+        const double row_cost = rows_cost(mg * G);
+        // Enough rows per piece that partial traffic (2 x mg x G x (D+2)
+        // floats) stays under 1/8 of the piece's KV bytes; few enough that one
+        // piece does not outweigh a CTA's share.
+        const int32_t rmin = std::max(1, (int32_t)((16.0 * mg * G * (D + 2)) / ((double)c * D) + 0.999));
         const int32_t rpar = std::max(1, (int32_t)(avg / row_cost));
         const int32_t per = std::max(rmin, rpar);
         const int32_t np = std::max(1, (nrows + per - 1) / per);
@@ -226,7 +234,7 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
                 const int32_t rb = row0 + (int32_t)((int64_t)nrows * (k + 1) / np);
                 // A unit covers a range of heads (the kernel reloads the query
                 // tile per head), as many as keep it within a CTA's share.
-                const double head_cost = (rb - ra) * (1.0 + kCfComputePer16 * ((qb - qa + 15) / 16));
+                const double head_cost = (rb - ra) * rows_cost((qb - qa) * G);
                 const int32_t hp = std::max(1, std::min(H, (int32_t)(avg / head_cost)));
                 const int32_t nparts = (H + hp - 1) / hp;
                 for (int32_t hk = 0; hk < nparts; ++hk) {
@@ -368,8 +376,13 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
         }
     }
 
-    plan.pbase.assign((size_t)b * H + 1, 0);
-    for (size_t i = 0; i < (size_t)b * H; ++i) plan.pbase[i + 1] = plan.pbase[i] + npart[i];
+    // partial ids per (position, query head); the G query heads of a key/value
+    // head have the same pieces
+    plan.pbase.assign((size_t)b * HQ + 1, 0);
+    for (size_t i = 0; i < (size_t)b * HQ; ++i) {
+        const size_t pos = i / HQ, qh = i % HQ;
+        plan.pbase[i + 1] = plan.pbase[i] + npart[pos * H + qh / G];
+    }
     plan.n_partials = plan.pbase.back();
     // Counting sort by CTA (bucket `grid` is the tail queue), stable: each
     // CTA keeps its chunk-first units first, then its sequence-first pieces in
@@ -406,7 +419,7 @@ void layout_plan(const Plan& plan, int32_t b, PlanLayout& lay, std::vector<unsig
 }
 
 void layout_ws(const Plan& plan, const Pool& p, int32_t b, WsLayout& ws) {
-    const size_t H = p.cfg.n_heads, D = p.cfg.head_dim;
+    const size_t H = p.cfg.n_heads, D = p.cfg.head_dim;   // q and out use the query heads
     size_t off = 0;
     ws.part_o = off;   off = align256(off + (size_t)plan.n_partials * D * sizeof(float));
     ws.part_ms = off;  off = align256(off + (size_t)plan.n_partials * 2 * sizeof(float));

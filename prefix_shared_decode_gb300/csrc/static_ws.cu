@@ -86,6 +86,8 @@ extern "C" int ca_decode_attention_static_ws(const ca_pool* pool_, const ca_sche
     a.part_ms = reinterpret_cast<float2*>(w + s->ws.part_ms);
     a.n_layers = pool->cfg.n_layers;
     a.n_heads = pool->cfg.n_heads;
+    a.n_kv_heads = ca::kv_heads(pool->cfg);
+    a.group = pool->cfg.n_heads / a.n_kv_heads;
     a.layer = layer;
     a.capacity = pool->cfg.capacity_slots;
     a.scale_log2 = scale * 1.4426950408889634f;

@@ -38,7 +38,7 @@ def assert_close(got, want, what=""):
 def load(torch, wl, no_sharing=False, capacity=None):
     from prefix_shared_decode_gb300 import Pool
     pool = Pool(wl.n_layers, wl.n_heads, wl.head_dim, wl.chunk, capacity or capacity_for(wl),
-                no_sharing=no_sharing)
+                no_sharing=no_sharing, n_kv_heads=wl.kv_heads)
     staging = {}
     for sid in wl.seq_ids():
         insert_sequence(pool, wl, sid, staging=staging)
@@ -103,6 +103,27 @@ def test_random_trees_every_output(torch_cuda, c, D, seed):
         want = A.decode_attention(trie, batch, layer, q, 1 / np.sqrt(D))
         got, _ = run(torch, pool, batch, q, layer=layer)
         assert_close(got, want, f"c={c} D={D} layer={layer}")
+
+
+@pytest.mark.parametrize("G,Hkv,c,D", [(2, 2, 32, 128), (4, 2, 64, 128), (8, 1, 64, 64), (8, 2, 16, 128)])
+def test_grouped_query_attention_every_output(torch_cuda, G, Hkv, c, D):
+    """Grouped-query attention: G query heads per key/value head; the
+    sequence-first phase then multiplies G rows per chunk on tensor cores."""
+    from prefix_shared_decode_gb300 import Pool
+    torch = torch_cuda
+    rng = np.random.default_rng(40 + G + c)
+    seqs = random_segment_sequences(40 + G, 12, c, n_segments=10)
+    pool = Pool(1, Hkv * G, D, c, 600, n_kv_heads=Hkv)
+    trie = OracleTrie(c, 600)
+    for i, toks in enumerate(seqs):
+        k = rng.standard_normal((1, len(toks), Hkv, D), dtype=np.float32).astype(np.float16)
+        v = rng.standard_normal((1, len(toks), Hkv, D), dtype=np.float32).astype(np.float16)
+        trie.insert(i, toks, k, v)
+        pool.insert(i, toks, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+    batch = [int(x) for x in rng.permutation(12)[:11]]
+    q = rng.standard_normal((11, Hkv * G, D), dtype=np.float32).astype(np.float16)
+    got, _ = run(torch, pool, batch, q)
+    assert_close(got, A.decode_attention(trie, batch, 0, q, 1 / np.sqrt(D)), f"G={G}")
 
 
 def test_edge_cases(torch_cuda):
@@ -303,7 +324,7 @@ SAMPLE = 4
 
 
 @pytest.mark.parametrize("name", ["llama7b_p1024", "sweep_s2048_b32", "sweep_s2048_b64",
-                                  "sweep_s4096_b32", "sweep_s4096_b64", "no_sharing"])
+                                  "sweep_s4096_b32", "sweep_s4096_b64", "no_sharing", "gqa_p1024"])
 def test_full_size_workloads_sampled(torch_cuda, name):
     """The benchmark's launch configuration at full size; every output is
     finite and SAMPLE sequences (all heads) match the oracle."""

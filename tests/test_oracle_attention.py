@@ -182,3 +182,26 @@ def test_decode_attention_over_trie_matches_brute_force():
             k, v = ctx[s]
             want = brute_force(q[i].tolist(), k[layer].tolist(), v[layer].tolist(), 0.5)
             np.testing.assert_allclose(out[i], want, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("G", [1, 2, 4])
+def test_grouped_query_attention_equals_repeated_kv(G):
+    """GQA equals multi-head attention with each key/value head repeated for
+    its G query heads; brute force checks one head directly."""
+    rng = np.random.default_rng(20 + G)
+    Hkv, D, n = 2, 4, 9
+    q = rand((Hkv * G, D), rng, -2, 2)
+    k, v = rand((n, Hkv, D), rng, -2, 2), rand((n, Hkv, D), rng)
+    got = A.softmax_attention(q, k, v, 0.6)
+    want = A.softmax_attention(q, np.repeat(k, G, axis=1), np.repeat(v, G, axis=1), 0.6)
+    np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-14)
+    h = Hkv * G - 1                                       # last query head -> last kv head
+    bf = brute_force(q[h:h + 1].tolist(), k[:, Hkv - 1:Hkv].tolist(), v[:, Hkv - 1:Hkv].tolist(), 0.6)
+    np.testing.assert_allclose(got[h], bf[0], rtol=1e-12, atol=1e-13)
+    o, m, s = A.partial(q, k, v, 0.6)
+    np.testing.assert_allclose(A.merge([(o, m, s)]), got, rtol=1e-13, atol=1e-14)
+
+
+def test_grouped_query_heads_must_divide():
+    with pytest.raises(OracleError):
+        A.softmax_attention(np.zeros((3, 2)), np.zeros((1, 2, 2)), np.zeros((1, 2, 2)), 1.0)

@@ -11,7 +11,7 @@ from oracle.pakv import OracleTrie
 from tests.treegen import random_segment_sequences
 
 
-def simulate(plan, tables, trie, q, scale, H):
+def simulate(plan, tables, trie, q, scale, H, G=1):
     by_slot = {}
     stack = [trie.root]
     while stack:
@@ -22,19 +22,23 @@ def simulate(plan, tables, trie, q, scale, H):
     perm, pbase = tables["seq_perm"], plan["pbase"]
     parts = {}
     cover = {}
-    def emit(pos, h, part, chunks):
-        k = np.concatenate([by_slot[s].k[0][:t, h] for s, t in chunks])[:, None, :]
-        v = np.concatenate([by_slot[s].v[0][:t, h] for s, t in chunks])[:, None, :]
-        pid = pbase[pos * H + h] + part
-        assert pbase[pos * H + h] <= pid < pbase[pos * H + h + 1]
-        assert pid not in parts
-        parts[pid] = A.partial(q[perm[pos], h][None, :], k, v, scale)
-        cover.setdefault((pos, h), []).extend(int(s) for s, _ in chunks)
+    HQ = H * G
+
+    def emit(pos, kvh, part, chunks):
+        # one partial per query head of the key/value head
+        k = np.concatenate([by_slot[s].k[0][:t, kvh] for s, t in chunks])[:, None, :]
+        v = np.concatenate([by_slot[s].v[0][:t, kvh] for s, t in chunks])[:, None, :]
+        for qh in range(kvh * G, (kvh + 1) * G):
+            pid = pbase[pos * HQ + qh] + part
+            assert pbase[pos * HQ + qh] <= pid < pbase[pos * HQ + qh + 1]
+            assert pid not in parts
+            parts[pid] = A.partial(q[perm[pos], qh][None, :], k, v, scale)
+            cover.setdefault((pos, qh), []).extend(int(s) for s, _ in chunks)
 
     for kind, h, lo, hi, cb, ce, part, qrow, n, base, part_next, _ in plan["units"]:
         assert lo < hi and cb < ce
         if kind == 0:
-            assert 0 <= h and h + n <= H and n >= 1 and hi - lo <= 64
+            assert 0 <= h and h + n <= H and n >= 1 and (hi - lo) * G <= 64
             for hh in range(h, h + n):
                 for pos in range(lo, hi):
                     emit(pos, hh, part, plan["chunks"][cb:ce])
@@ -50,8 +54,8 @@ def simulate(plan, tables, trie, q, scale, H):
     out = np.empty(q.shape)
     b = len(perm)
     for pos in range(b):
-        for h in range(H):
-            ids = range(pbase[pos * H + h], pbase[pos * H + h + 1])
+        for h in range(HQ):
+            ids = range(pbase[pos * HQ + h], pbase[pos * HQ + h + 1])
             out[perm[pos], h] = A.merge([parts[i] for i in ids])[0]
     return out, cover
 
@@ -109,3 +113,24 @@ def test_plan_splits_large_runs_and_query_groups(lib):
     assert plan["grid"] == 304
     units_per_cta = np.diff(plan["cta_begin"])
     assert (units_per_cta > 0).sum() > 250
+
+
+@pytest.mark.parametrize("G", [2, 4, 8])
+def test_plan_with_grouped_query_heads(lib, G):
+    """Units per key/value head, partials per query head, query groups of at
+    most 64 (position, query head) rows."""
+    from prefix_shared_decode_gb300 import Pool
+    Hkv, D, c = 2, 64, 16
+    rng = np.random.default_rng(30 + G)
+    seqs = random_segment_sequences(30 + G, 12, c)
+    pool = Pool(1, Hkv * G, D, c, 500, host_only=True, n_kv_heads=Hkv)
+    trie = OracleTrie(c, 500)
+    for i, toks in enumerate(seqs):
+        k = rng.standard_normal((1, len(toks), Hkv, D))
+        trie.insert(i, toks, k, k * 0.5)
+        pool.insert(i, toks)
+    batch = [int(x) for x in rng.permutation(12)[:10]]
+    q = rng.standard_normal((len(batch), Hkv * G, D))
+    sched = pool.schedule(batch)
+    out, _ = simulate(sched.plan(), sched.tables(), trie, q, 0.125, Hkv, G)
+    np.testing.assert_allclose(out, A.decode_attention(trie, batch, 0, q, 0.125), rtol=1e-10, atol=1e-12)

@@ -60,6 +60,7 @@ class Workload:
     head_dim: int
     chunk: int
     seed: int
+    n_kv_heads: int = 0            # key/value heads (0: one per query head)
     seg_len: dict[int, int] = field(default_factory=dict)
     seqs: dict[int, list[int]] = field(default_factory=dict)  # seq_id -> segment ids
     churn: int = 0  # sequences removed and inserted per step (multi-tenant tree)
@@ -74,6 +75,10 @@ class Workload:
     def scale(self) -> float:
         return 1.0 / math.sqrt(self.head_dim)
 
+    @property
+    def kv_heads(self) -> int:
+        return self.n_kv_heads or self.n_heads
+
     def seq_ids(self) -> list[int]:
         return sorted(self.seqs)
 
@@ -86,7 +91,7 @@ class Workload:
     def segment(self, seg_id: int) -> tuple[np.ndarray, np.ndarray]:
         if seg_id not in self._kv_cache:
             self._kv_cache[seg_id] = segment_kv(self.seed, seg_id, self.seg_len[seg_id],
-                                                self.n_layers, self.n_heads, self.head_dim)
+                                                self.n_layers, self.kv_heads, self.head_dim)
         return self._kv_cache[seg_id]
 
     def kv_rows(self, seq_id: int, start: int = 0) -> tuple[np.ndarray, np.ndarray]:
@@ -101,7 +106,7 @@ class Workload:
                 vs.append(v[:, a:])
             pos += n
         if not ks:
-            shape = (self.n_layers, 0, self.n_heads, self.head_dim)
+            shape = (self.n_layers, 0, self.kv_heads, self.head_dim)
             return np.zeros(shape, np.float16), np.zeros(shape, np.float16)
         return np.concatenate(ks, axis=1), np.concatenate(vs, axis=1)
 
@@ -142,8 +147,9 @@ class Workload:
 
 
 def _shared_prefix(name, seed, b, n_shared, n_private, n_heads=32, head_dim=128,
-                   chunk=64, description="") -> Workload:
-    w = Workload(name, 1, n_heads, head_dim, chunk, seed, description=description)
+                   chunk=64, description="", n_kv_heads=0) -> Workload:
+    w = Workload(name, 1, n_heads, head_dim, chunk, seed, description=description,
+                 n_kv_heads=n_kv_heads)
     if n_shared:
         pre = w._new_seg(n_shared)
     for i in range(b):
@@ -185,6 +191,8 @@ def make(name: str) -> Workload:
                     batch 32 or 64, 512 private tokens each; seeds 2-5.
     no_sharing      32 sequences with fully private 2048-token contexts; seed 6.
     multi_tenant    the multi-tenant tree with churn; seed 7.
+    gqa_p1024       llama7b_p1024's tree with grouped-query attention: 32 query
+                    heads over 8 key/value heads; seed 8.
     """
     if name == "tiny":
         return _shared_prefix(name, 0, 4, 64, 16, n_heads=2, head_dim=64, chunk=16,
@@ -203,8 +211,13 @@ def make(name: str) -> Workload:
                               description="32 heads, D 128, chunk 64; 32 fully private 2048-token contexts")
     if name == "multi_tenant":
         return _multi_tenant(7)
+    if name == "gqa_p1024":
+        return _shared_prefix(name, 8, 32, 1024, 512, n_kv_heads=8,
+                              description="32 query heads sharing 8 key/value heads (grouped-query, "
+                                          "Llama-3-8B-like), D 128, chunk 64; 32 seqs share 1024 "
+                                          "tokens, 512 private each")
     raise KeyError(name)
 
 
 ALL = ["tiny", "llama7b_p1024", "sweep_s2048_b32", "sweep_s2048_b64",
-       "sweep_s4096_b32", "sweep_s4096_b64", "no_sharing", "multi_tenant"]
+       "sweep_s4096_b32", "sweep_s4096_b64", "no_sharing", "multi_tenant", "gqa_p1024"]

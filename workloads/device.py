@@ -14,7 +14,7 @@ def insert_sequence(pool, wl, seq_id: int, stream=None, staging: dict | None = N
     n = len(toks)
     matched = pool.match_prefix(toks)
     k_new, v_new = wl.kv_rows(seq_id, start=matched)
-    shape = (wl.n_layers, n, wl.n_heads, wl.head_dim)
+    shape = (wl.n_layers, n, wl.kv_heads, wl.head_dim)
     key = ("kv", shape)
     if staging is not None and key in staging:
         k_dev, v_dev = staging[key]
