@@ -132,6 +132,12 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
 }
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
     atomicCAS(status, 0, code);
 }
@@ -703,7 +709,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
             if (next_sf) prefetch_q(fld(d0, F_QROW), fld(d0, F_HEAD));
             const int m_rows = (q_hi - q_lo) * G;
             const int rblocks = m_rows <= 16 ? 1 : m_rows <= 32 ? 2 : 4;
-            int T = kConsumerWarps / rblocks;            // warps splitting the tokens
+            int T = kConsumerWarps / rblocks;   // warps splitting a chunk's tokens
             if (T * 16 > C) T = C / 16;
             const int rb = w / T, tp = w % T;
             const bool active = rb < rblocks && rb * 16 < m_rows;
@@ -712,16 +718,17 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 const int seg_end = min(L_end, (kvh + 1) * n);
                 const int upart = first ? part_first : part_rest;
                 if (!first) consumer_sync();   // the previous head's exchange reads are done
-                // Load the rows' queries into the swizzled Q tile; rows past
-                // m_rows are zero.
-                for (int idx = threadIdx.x; idx < kQRows * (D / 8); idx += kConsumerWarps * 32) {
+                // Copy the rows' queries into the swizzled Q tile with 16-byte
+                // asynchronous copies, all in flight at once.  Rows past m_rows
+                // are left as they are: each mma row is independent and such
+                // rows are never written out.
+                for (int idx = threadIdx.x; idx < m_rows * (D / 8); idx += kConsumerWarps * 32) {
                     const int r = idx / (D / 8), k = idx % (D / 8);
-                    uint4 v = make_uint4(0, 0, 0, 0);
-                    if (r < m_rows)
-                        v = *reinterpret_cast<const uint4*>(
-                            p.q + ((size_t)p.seq_perm[q_lo + r / G] * H + kvh * G + r % G) * D + k * 8);
-                    *reinterpret_cast<uint4*>(qreg + swz(r, k, kQRows)) = v;
+                    const uint16_t* src =
+                        p.q + ((size_t)p.seq_perm[q_lo + r / G] * H + kvh * G + r % G) * D + k * 8;
+                    cp_async16(smem_u32(qreg + swz(r, k, kQRows)), src);
                 }
+                cp_async_wait_all();
                 consumer_sync();
                 float o[D / 8][4], m[2] = {-INFINITY, -INFINITY}, s[2] = {0.f, 0.f};
 #pragma unroll

@@ -196,7 +196,9 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
     double cf_total = 0;
     for (int32_t u = 0; u < U; ++u) {
         const int32_t nrows = t.cf_runs[4 * u + 1], m = t.cf_runs[4 * u + 3] - t.cf_runs[4 * u + 2];
-        cf_total += (double)nrows * H * rows_cost(std::min(m, kMaxCfQueries / G) * G);
+        const int32_t max_pos = std::max(1, kMaxCfQueries / G);
+        const int32_t ngroups = (m + max_pos - 1) / max_pos;
+        cf_total += (double)nrows * H * ngroups * rows_cost((m + ngroups - 1) / ngroups * G);
     }
     const int32_t tiles_ceiling = (int32_t)std::max(1.0, sf_total + cf_total);
     grid = std::max(1, std::min(grid, tiles_ceiling));
@@ -219,11 +221,14 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
         const int32_t mg = (m + ngroups - 1) / ngroups;
         const double row_cost = rows_cost(mg * G);
         // Enough rows per piece that partial traffic (2 x mg x G x (D+2)
-        // floats) stays under 1/8 of the piece's KV bytes; few enough that one
-        // piece does not outweigh a CTA's share.
+        // floats) stays under 1/8 of the piece's KV bytes, but never so many
+        // that one piece outweighs a CTA's share by more than a quarter: the
+        // longest unit bounds the kernel, while extra partials are spread
+        // over every CTA and the merge.
         const int32_t rmin = std::max(1, (int32_t)((16.0 * mg * G * (D + 2)) / ((double)c * D) + 0.999));
         const int32_t rpar = std::max(1, (int32_t)(avg / row_cost));
-        const int32_t per = std::max(rmin, rpar);
+        const int32_t rcap = std::max(1, (int32_t)(1.25 * avg / row_cost));
+        const int32_t per = std::max(rpar, std::min(rmin, rcap));
         const int32_t np = std::max(1, (nrows + per - 1) / per);
         pieces[u] = np;
         for (int32_t g = 0; g < ngroups; ++g) {
