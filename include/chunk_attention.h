@@ -303,6 +303,14 @@ int ca_sched_device_status(const ca_sched* sched, void* stream);
  * after it, on `stream`.  Pass NULLs to turn it off. */
 int ca_sched_set_profile_events(ca_sched* sched, void* event_begin, void* event_end);
 
+/* Number of kernels the library has launched in this process so far (KV
+ * scatters, attention and merge kernels; every pool and device), counted
+ * when each launch is accepted.  A caller reads it before and after a run
+ * of calls to learn how many GPU kernels they issued.  Instrumentation
+ * only: the pages have no counterpart.  CA_ERR_INVALID if count_out is
+ * NULL. */
+int ca_kernel_launches(uint64_t* count_out);
+
 const char* ca_error_string(int status);
 
 #ifdef __cplusplus

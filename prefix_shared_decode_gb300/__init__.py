@@ -20,7 +20,8 @@ import numpy as np
 from . import capi
 from .capi import CAError, check
 
-__all__ = ["Pool", "Schedule", "decode_attention", "decode_attention_host", "CAError"]
+__all__ = ["Pool", "Schedule", "decode_attention", "decode_attention_host", "kernel_launches",
+           "CAError"]
 
 
 def _stream_ptr(stream) -> int | None:
@@ -301,3 +302,10 @@ def decode_attention_host(pool: Pool, sched: Schedule, q_host, out_host, layer: 
                                               ws.numel(), _stream_ptr(stream)),
           "ca_decode_attention_host")
     return out_host
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched in this process so far."""
+    n = C.c_uint64(0)
+    check(capi.lib().ca_kernel_launches(C.byref(n)), "ca_kernel_launches")
+    return int(n.value)

@@ -27,7 +27,7 @@ EXPORTS = [
     "ca_sched_counts", "ca_export_tables", "ca_export_plan", "ca_workspace_bytes", "ca_decode_attention",
     "ca_workspace_bytes_host", "ca_decode_attention_host", "ca_decode_attention_static_ws",
     "ca_sched_device_status",
-    "ca_sched_set_profile_events", "ca_error_string",
+    "ca_sched_set_profile_events", "ca_kernel_launches", "ca_error_string",
 ]
 
 
@@ -88,6 +88,7 @@ def lib() -> C.CDLL:
         "ca_decode_attention_static_ws": [vp, vp, i32, vp, vp, C.c_float, vp],
         "ca_sched_device_status": [vp, vp],
         "ca_sched_set_profile_events": [vp, vp, vp],
+        "ca_kernel_launches": [vp],
         "ca_error_string": [C.c_int],
     }
     for name, args in sig.items():

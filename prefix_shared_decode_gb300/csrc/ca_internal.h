@@ -220,5 +220,7 @@ int make_tensor_map(Pool& p);
 int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_rows,
                    const std::vector<ScatterChunk>& chunks, void* stream);
 int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void* stream);
+// Kernels this process has launched through the library (all pools, all devices).
+uint64_t kernel_launches();
 
 }  // namespace ca

@@ -437,6 +437,12 @@ int ca_sched_set_profile_events(ca_sched* s, void* event_begin, void* event_end)
     return CA_OK;
 }
 
+int ca_kernel_launches(uint64_t* count_out) {
+    if (!count_out) return CA_ERR_INVALID;
+    *count_out = ca::kernel_launches();
+    return CA_OK;
+}
+
 const char* ca_error_string(int status) {
     switch (status) {
         case CA_OK: return "ok";

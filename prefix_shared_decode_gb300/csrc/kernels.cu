@@ -29,6 +29,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 
@@ -949,6 +950,12 @@ int make_tensor_map(Pool& p) {
     return r == CUDA_SUCCESS ? CA_OK : CA_ERR_CUDA;
 }
 
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+uint64_t kernel_launches() { return g_launches.load(std::memory_order_relaxed); }
+
 int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_rows,
                    const std::vector<ScatterChunk>& chunks, void* stream) {
     const ca_pool_config& c = p.cfg;
@@ -969,6 +976,7 @@ int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_ro
         const unsigned blocks = (unsigned)(cnt * c.n_layers * a.n_heads);
         dev::kv_scatter_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
         if (cudaGetLastError() != cudaSuccess) return CA_ERR_CUDA;
+        g_launches.fetch_add(1, std::memory_order_relaxed);
     }
     return CA_OK;
 }
@@ -1001,6 +1009,7 @@ int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void*
     cudaError_t e = cudaLaunchKernelExC(&mc, fn, args);
     if (s.ev_end) cudaEventRecord(static_cast<cudaEvent_t>(s.ev_end), cs);
     if (e != cudaSuccess) return CA_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     // Merge: one warp per (position, head).
     const int n_pairs = s.t.b * p.cfg.n_heads;
     cudaLaunchConfig_t lc = {};
@@ -1018,6 +1027,7 @@ int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void*
         cudaMemsetAsync(a.dyn_counter, 0, sizeof(int32_t), cs);   // keep the next call's queue clean
         return CA_ERR_CUDA;
     }
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return CA_OK;
 }
 

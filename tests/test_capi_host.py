@@ -140,6 +140,17 @@ def test_no_tpp_schedule_makes_everything_sequence_first(lib):
         assert chunks[:, 1].sum() == 53
 
 
+def test_kernel_launch_counter_on_host_only_pools(lib):
+    import ctypes
+    from prefix_shared_decode_gb300 import Pool, kernel_launches
+    before = kernel_launches()
+    pool = Pool(1, 2, 64, 16, 8, host_only=True)
+    pool.insert(1, list(range(40)))                     # host-only: no KV scatter launched
+    pool.schedule([1])
+    assert kernel_launches() == before
+    assert lib.ca_kernel_launches(None) == -1            # CA_ERR_INVALID
+
+
 def test_errors_and_rollback(lib):
     from prefix_shared_decode_gb300 import CAError, Pool
     pool = Pool(1, 2, 64, 16, 5, host_only=True)

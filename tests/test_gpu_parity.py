@@ -296,6 +296,26 @@ def test_host_io_entry_and_repeat_calls(torch_cuda):
     assert sched.device_status() == 0
 
 
+def test_kernel_launch_counter(torch_cuda):
+    """Each decode call launches two kernels (attention, merge); an insert
+    launches one KV scatter per 128 new chunks."""
+    from prefix_shared_decode_gb300 import decode_attention, kernel_launches
+    torch = torch_cuda
+    wl = workloads.make("tiny")
+    pool = load(torch, wl)
+    sched = pool.schedule(wl.seq_ids())
+    q = torch.from_numpy(wl.queries(0)).cuda()
+    n0 = kernel_launches()
+    for _ in range(3):
+        decode_attention(pool, sched, q)
+    assert kernel_launches() - n0 == 6
+    n1 = kernel_launches()
+    k = torch.zeros((1, 40, wl.kv_heads, wl.head_dim), dtype=torch.float16, device="cuda")
+    pool.insert(1000, list(range(900000, 900040)), k, k)   # 3 new chunks of 16
+    torch.cuda.synchronize()
+    assert kernel_launches() - n1 == 1
+
+
 def test_two_ctas_per_sm(torch_cuda):
     """The persistent grid holds two CTAs per SM (registers and shared memory
     of the largest instantiation fit twice)."""
