@@ -256,10 +256,10 @@ def run_ours(args):
             removed, inserted, toks, lens, live = plan_churn[i]
             pool.remove_batch(removed)
             t1 = time.perf_counter()
-            pool.insert_batch(inserted, toks, *kv_views[i], lengths=lens)
+            pool.insert_batch(inserted, toks, *kv_views[i], lengths=lens, stream=stream)
             t2 = time.perf_counter()
             batch = live
-        sched = scheds[r] = pool.schedule(batch, reuse=sched)
+        sched = scheds[r] = pool.schedule(batch, reuse=sched, stream=stream)
         if churn:
             t3 = time.perf_counter()
             host_split["remove"].append((t1 - th) * 1e6)
@@ -268,7 +268,7 @@ def run_ours(args):
             churn_host_us.append((t3 - th) * 1e6)
         if sched.workspace_bytes() > ws.numel():
             ws = wss[r] = torch.zeros(2 * sched.workspace_bytes(), dtype=torch.uint8, device=dev)
-        decode_attention(pool, sched, qs[i % 4], out=out, scale=wl.scale, workspace=ws)
+        decode_attention(pool, sched, qs[i % 4], out=out, scale=wl.scale, workspace=ws, stream=stream)
 
     for i in range(args.warmup):
         step(i)
@@ -335,8 +335,9 @@ def run_ours(args):
     for i in range(Ke):
         r = i % n_copies
         eev[i][0].record(stream)
-        scheds[r] = pools[r].schedule(batch, reuse=scheds[r])
-        decode_attention_host(pools[r], scheds[r], qh[i % 4], oh, scale=wl.scale, workspace=wshs[r])
+        scheds[r] = pools[r].schedule(batch, reuse=scheds[r], stream=stream)
+        decode_attention_host(pools[r], scheds[r], qh[i % 4], oh, scale=wl.scale, workspace=wshs[r],
+                              stream=stream)
         eev[i][1].record(stream)
     torch.cuda.synchronize()
     e2e_us = sum(a.elapsed_time(z) for a, z in eev) / Ke * 1e3
@@ -349,11 +350,13 @@ def run_ours(args):
             ws_ = [s_.workspace() for s_ in ss]
             m = len(ps)
             for i in range(10):
-                decode_attention(ps[i % m], ss[i % m], qs[i % 4], out=out, scale=wl.scale, workspace=ws_[i % m])
+                decode_attention(ps[i % m], ss[i % m], qs[i % 4], out=out, scale=wl.scale, workspace=ws_[i % m],
+                                 stream=stream)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             for i in range(n):
-                decode_attention(ps[i % m], ss[i % m], qs[i % 4], out=out, scale=wl.scale, workspace=ws_[i % m])
+                decode_attention(ps[i % m], ss[i % m], qs[i % 4], out=out, scale=wl.scale, workspace=ws_[i % m],
+                                 stream=stream)
             e1.record(stream)
             torch.cuda.synchronize()
             return e0.elapsed_time(e1) / n * 1e3

@@ -220,6 +220,10 @@ int make_tensor_map(Pool& p);
 int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_rows,
                    const std::vector<ScatterChunk>& chunks, void* stream);
 int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void* stream);
+// Kernel parameters of one call: the schedule's device plan and counters,
+// the pool, q / out, and the partial buffers inside `ws_dev`.
+AttnParams attn_params(const Pool& pool, const Sched& s, int32_t layer, const void* q, void* out,
+                       float scale, void* ws_dev);
 // Kernels this process has launched through the library (all pools, all devices).
 uint64_t kernel_launches();
 

@@ -364,33 +364,45 @@ static int decode_checks(const ca_pool* pool, const ca_sched* s, int32_t layer, 
     return CA_OK;
 }
 
-static int decode_launch(const ca_pool* pool, const ca_sched* s, int32_t layer, const void* q,
-                         void* out, float scale, void* ws_dev, void* stream) {
-    unsigned char* dev = static_cast<unsigned char*>(s->dev);
+}  // extern "C"
+
+namespace ca {
+AttnParams attn_params(const Pool& pool, const Sched& s, int32_t layer, const void* q, void* out,
+                       float scale, void* ws_dev) {
+    unsigned char* dev = static_cast<unsigned char*>(s.dev);
     unsigned char* ws = static_cast<unsigned char*>(ws_dev);
     AttnParams a{};
-    a.chunks = reinterpret_cast<const ChunkRef*>(dev + s->layout.chunks);
-    a.units = reinterpret_cast<const Unit*>(dev + s->layout.units);
-    a.cta_begin = reinterpret_cast<const int32_t*>(dev + s->layout.cta_begin);
-    a.seq_perm = reinterpret_cast<const int32_t*>(dev + s->layout.seq_perm);
-    a.pbase = reinterpret_cast<const int32_t*>(dev + s->layout.pbase);
-    a.slot_ntok = reinterpret_cast<const int32_t*>(static_cast<const unsigned char*>(pool->kv) +
-                                                   pool_tile_bytes(pool->cfg));
-    a.status = reinterpret_cast<int32_t*>(dev + s->layout.status);
-    a.dyn_counter = reinterpret_cast<int32_t*>(dev + s->layout.counter);
-    a.dyn_begin = s->plan.cta_begin[s->plan.grid];
-    a.dyn_end = (int32_t)s->plan.units.size();
+    a.chunks = reinterpret_cast<const ChunkRef*>(dev + s.layout.chunks);
+    a.units = reinterpret_cast<const Unit*>(dev + s.layout.units);
+    a.cta_begin = reinterpret_cast<const int32_t*>(dev + s.layout.cta_begin);
+    a.seq_perm = reinterpret_cast<const int32_t*>(dev + s.layout.seq_perm);
+    a.pbase = reinterpret_cast<const int32_t*>(dev + s.layout.pbase);
+    a.slot_ntok = reinterpret_cast<const int32_t*>(static_cast<const unsigned char*>(pool.kv) +
+                                                   pool_tile_bytes(pool.cfg));
+    a.status = reinterpret_cast<int32_t*>(dev + s.layout.status);
+    a.dyn_counter = reinterpret_cast<int32_t*>(dev + s.layout.counter);
+    a.dyn_begin = s.plan.cta_begin[s.plan.grid];
+    a.dyn_end = (int32_t)s.plan.units.size();
     a.q = static_cast<const uint16_t*>(q);
     a.out = static_cast<uint16_t*>(out);
-    a.part_o = reinterpret_cast<float*>(ws + s->ws.part_o);
-    a.part_ms = reinterpret_cast<float2*>(ws + s->ws.part_ms);
-    a.n_layers = pool->cfg.n_layers;
-    a.n_heads = pool->cfg.n_heads;
-    a.n_kv_heads = kv_heads(pool->cfg);
-    a.group = pool->cfg.n_heads / a.n_kv_heads;
+    a.part_o = reinterpret_cast<float*>(ws + s.ws.part_o);
+    a.part_ms = reinterpret_cast<float2*>(ws + s.ws.part_ms);
+    a.n_layers = pool.cfg.n_layers;
+    a.n_heads = pool.cfg.n_heads;
+    a.n_kv_heads = kv_heads(pool.cfg);
+    a.group = pool.cfg.n_heads / a.n_kv_heads;
     a.layer = layer;
-    a.capacity = pool->cfg.capacity_slots;
+    a.capacity = pool.cfg.capacity_slots;
     a.scale_log2 = scale * 1.4426950408889634f;
+    return a;
+}
+}  // namespace ca
+
+extern "C" {
+
+static int decode_launch(const ca_pool* pool, const ca_sched* s, int32_t layer, const void* q,
+                         void* out, float scale, void* ws_dev, void* stream) {
+    const AttnParams a = attn_params(*pool, *s, layer, q, out, scale, ws_dev);
     return launch_attention(*pool, *s, a, stream);
 }
 
@@ -425,7 +437,14 @@ int ca_sched_device_status(const ca_sched* s, void* stream) {
     int32_t word = 0;
     int32_t* dev_word = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(s->dev) + s->layout.status);
     if (cudaMemcpy(&word, dev_word, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return CA_ERR_CUDA;
-    if (word != 0 && cudaMemset(dev_word, 0, sizeof(word)) != cudaSuccess) return CA_ERR_CUDA;
+    if (word != 0) {
+        // A call that stopped early may have left the queue counter
+        // mid-count: clear it with the word.
+        if (cudaMemset(dev_word, 0, sizeof(word)) != cudaSuccess ||
+            cudaMemset(static_cast<unsigned char*>(s->dev) + s->layout.counter, 0, sizeof(int32_t)) !=
+                cudaSuccess)
+            return CA_ERR_CUDA;
+    }
     return word;
 }
 

@@ -55,8 +55,8 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+__device__ __forceinline__ void mbar_expect_tx_only(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -153,9 +153,12 @@ __device__ __forceinline__ uint32_t swz(int r, int k, int rows) {
 // ---------------------------------------------------------------------------
 // Merge kernel: all partials of one (position, head) combined by the
 // explainer's output-combination rule, m* = max m_j,
-// out = sum 2^{m_j-m*} o_j / sum 2^{m_j-m*} s_j (m in log2 units).  One warp
-// per pair; lane j of a round of 32 holds partial j's (m, s); lane L owns
-// D/32 output dims.  Launched as a programmatic dependent of the main kernel:
+// out = sum 2^{m_j-m*} o_j / sum 2^{m_j-m*} s_j (m in log2 units), taken a
+// few partials at a time with the running maximum rescaled as it grows.  One
+// warp per pair; lane L owns D/32 output dims; lane j of a group loads (m, s)
+// of its partial while every lane loads its values of all the group's
+// partials, so a group costs one memory round trip.  Launched as a
+// programmatic dependent of the main kernel:
 // `griddepcontrol.wait` returns once the main grid has completed and its
 // stores are visible.
 // ---------------------------------------------------------------------------
@@ -164,6 +167,9 @@ __global__ void __launch_bounds__(128) merge_partials_kernel(const AttnParams p,
     constexpr int DPL = D / 32;
     constexpr int KB = 4;                          // partials whose loads are in flight together
     const int gw = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    // The next call's kernels may be scheduled now: they wait for this grid
+    // before touching anything it writes, and their prologue overlaps it.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // Plan entries may be read before the dependency wait; partials only after.
     int a = 0, n = 0, row = 0;
     if (gw < n_pairs) {
@@ -174,46 +180,46 @@ __global__ void __launch_bounds__(128) merge_partials_kernel(const AttnParams p,
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.dyn_counter = 0;   // the main grid is done with it
     if (gw >= n_pairs) return;
-    // Every lane loads (m, s) of partials lane, lane + 32, ...: max, then weights.
-    float M = -INFINITY;
-    for (int j = lane; j < n; j += 32) M = fmaxf(M, __ldcg(&p.part_ms[a + j]).x);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, off));
-    float acc[DPL], S = 0.f;
+    float M = -INFINITY, S = 0.f, acc[DPL];
 #pragma unroll
     for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
-    for (int j0 = 0; j0 < n; j0 += 32) {
+    for (int j = 0; j < n; j += KB) {
+        const int cnt = min(KB, n - j);
         float2 ms = make_float2(-INFINITY, 0.f);
-        if (j0 + lane < n) ms = __ldcg(&p.part_ms[a + j0 + lane]);
-        const float w = (ms.x == -INFINITY) ? 0.f : ex2(ms.x - M);
-        S += w * ms.y;
-        const int cnt = min(32, n - j0);
-        for (int j = 0; j < cnt; j += KB) {
-            // KB partial rows loaded at once (rows past cnt repeat the last
-            // valid one with weight 0), then accumulated.
-            float o[KB][DPL];
-            float wk[KB];
+        if (lane < cnt) ms = __ldcg(&p.part_ms[a + j + lane]);
+        float o[KB][DPL];
 #pragma unroll
-            for (int k = 0; k < KB; ++k) {
-                const int jj = min(j + k, cnt - 1);
-                wk[k] = (j + k < cnt) ? __shfl_sync(kFull, w, jj) : 0.f;
-                const float* po = p.part_o + (size_t)(a + j0 + jj) * D + lane * DPL;
-                if constexpr (DPL == 4) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
-                    o[k][0] = v.x; o[k][1] = v.y; o[k][2] = v.z; o[k][3] = v.w;
-                } else {
-                    const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
-                    o[k][0] = v.x; o[k][1] = v.y;
-                }
+        for (int k = 0; k < KB; ++k) {
+            const float* po = p.part_o + (size_t)(a + j + min(k, cnt - 1)) * D + lane * DPL;
+            if constexpr (DPL == 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
+                o[k][0] = v.x; o[k][1] = v.y; o[k][2] = v.z; o[k][3] = v.w;
+            } else {
+                const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
+                o[k][0] = v.x; o[k][1] = v.y;
             }
-#pragma unroll
-            for (int k = 0; k < KB; ++k)
-#pragma unroll
-                for (int d = 0; d < DPL; ++d) acc[d] += wk[k] * o[k][d];
         }
-    }
+        float mk[KB], sk[KB], mg = M;
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) S += __shfl_xor_sync(kFull, S, off);
+        for (int k = 0; k < KB; ++k) {
+            mk[k] = __shfl_sync(kFull, ms.x, k);
+            sk[k] = __shfl_sync(kFull, ms.y, k);
+            if (k < cnt) mg = fmaxf(mg, mk[k]);
+        }
+        const float mu = (mg == -INFINITY) ? 0.f : mg;
+        const float alpha = ex2(M - mu);            // 0 while nothing is accumulated
+        S *= alpha;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) acc[d] *= alpha;
+#pragma unroll
+        for (int k = 0; k < KB; ++k) {
+            const float w = (k < cnt && mk[k] != -INFINITY) ? ex2(mk[k] - mu) : 0.f;
+            S += w * sk[k];
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) acc[d] += w * o[k][d];
+        }
+        M = mg;
+    }
     const float inv = 1.f / S;
     uint16_t* dst = p.out + ((size_t)row * p.n_heads + gw % p.n_heads) * D + lane * DPL;
     if constexpr (DPL == 4) {
@@ -537,8 +543,10 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     mbar_arrive(fb);          // release the consumers without data
                     continue;
                 }
-                stage_ntok[st] = min(max(ntok, 0), C);
-                mbar_expect_tx(fb, SM::kStage);
+                // The copies go out first; the stage completes once they have
+                // landed and the token count (whose load may still be in
+                // flight) has been written and the producer has arrived.
+                mbar_expect_tx_only(fb, SM::kStage);
                 const uint32_t dst = smem_u32(stages + (size_t)st * SM::kStage);
                 const int rowK = (((ch.slot * p.n_layers + p.layer) * 2 + 0) * HK + head) * C;
                 const int rowV = rowK + HK * C;
@@ -547,6 +555,8 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     tma_load_2d(dst + bx * C * 128, &tmap, bx * 64, rowK, fb, pol);
                     tma_load_2d(dst + SM::kTile + bx * C * 128, &tmap, bx * 64, rowV, fb, pol);
                 }
+                stage_ntok[st] = min(max(ntok, 0), C);
+                mbar_arrive(fb);
             }
             if (!have_next) {                 // left early on a timeout
                 nxt = -1;

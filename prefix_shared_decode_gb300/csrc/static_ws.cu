@@ -65,31 +65,6 @@ extern "C" int ca_decode_attention_static_ws(const ca_pool* pool_, const ca_sche
     void* ws = nullptr;
     int st = static_ws_address(device, &ws);
     if (st) return st;
-
-    unsigned char* dev = static_cast<unsigned char*>(s->dev);
-    unsigned char* w = static_cast<unsigned char*>(ws);
-    ca::AttnParams a{};
-    a.chunks = reinterpret_cast<const ca::ChunkRef*>(dev + s->layout.chunks);
-    a.units = reinterpret_cast<const ca::Unit*>(dev + s->layout.units);
-    a.cta_begin = reinterpret_cast<const int32_t*>(dev + s->layout.cta_begin);
-    a.seq_perm = reinterpret_cast<const int32_t*>(dev + s->layout.seq_perm);
-    a.pbase = reinterpret_cast<const int32_t*>(dev + s->layout.pbase);
-    a.slot_ntok = reinterpret_cast<const int32_t*>(static_cast<const unsigned char*>(pool->kv) +
-                                                   ca::pool_tile_bytes(pool->cfg));
-    a.status = reinterpret_cast<int32_t*>(dev + s->layout.status);
-    a.dyn_counter = reinterpret_cast<int32_t*>(dev + s->layout.counter);
-    a.dyn_begin = s->plan.cta_begin[s->plan.grid];
-    a.dyn_end = (int32_t)s->plan.units.size();
-    a.q = static_cast<const uint16_t*>(q_dev);
-    a.out = static_cast<uint16_t*>(out_dev);
-    a.part_o = reinterpret_cast<float*>(w + s->ws.part_o);
-    a.part_ms = reinterpret_cast<float2*>(w + s->ws.part_ms);
-    a.n_layers = pool->cfg.n_layers;
-    a.n_heads = pool->cfg.n_heads;
-    a.n_kv_heads = ca::kv_heads(pool->cfg);
-    a.group = pool->cfg.n_heads / a.n_kv_heads;
-    a.layer = layer;
-    a.capacity = pool->cfg.capacity_slots;
-    a.scale_log2 = scale * 1.4426950408889634f;
+    const ca::AttnParams a = ca::attn_params(*pool, *s, layer, q_dev, out_dev, scale, ws);
     return ca::launch_attention(*pool, *s, a, stream);
 }

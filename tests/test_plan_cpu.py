@@ -134,3 +134,4 @@ def test_plan_with_grouped_query_heads(lib, G):
     sched = pool.schedule(batch)
     out, _ = simulate(sched.plan(), sched.tables(), trie, q, 0.125, Hkv, G)
     np.testing.assert_allclose(out, A.decode_attention(trie, batch, 0, q, 0.125), rtol=1e-10, atol=1e-12)
+
