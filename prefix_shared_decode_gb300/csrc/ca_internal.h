@@ -107,6 +107,7 @@ struct Node {
     int32_t row = -1;              // scratch: chunk-first row while building
     int32_t end_begin = 0;         // scratch: batch sequences ending here, as a
     int32_t end_count = 0;         //   range of the sorted (node, seq_id) list
+    int32_t owner = -1;            // scratch: batch row whose private chain starts here
 };
 
 struct Sequence {
@@ -143,7 +144,9 @@ struct Plan {
     int32_t grid = 0;
     int64_t n_partials = 0;
     // scratch kept across rebuilds so that a rebuild allocates nothing new
-    std::vector<std::pair<int32_t, Unit>> tagged;
+    std::vector<std::pair<int32_t, Unit>> tagged;   // chunk-first units with their CTA
+    std::vector<Unit> sf_scratch, tail_scratch;
+    std::vector<int32_t> sf_end;
 };
 
 struct Sched {

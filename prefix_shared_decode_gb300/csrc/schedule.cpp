@@ -25,47 +25,66 @@ namespace ca {
 
 int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flags, Tables& t) {
     if (b < 1 || !seq_ids) return CA_ERR_INVALID;
-    for (int32_t i = 0; i < b; ++i)
-        if (!p.seqs.count(seq_ids[i])) return CA_ERR_NOT_FOUND;
-    {
-        std::vector<int64_t> sorted(seq_ids, seq_ids + b);
-        std::sort(sorted.begin(), sorted.end());
-        if (std::adjacent_find(sorted.begin(), sorted.end()) != sorted.end()) return CA_ERR_INVALID;
+    std::vector<const Sequence*> seq_of(b);
+    for (int32_t i = 0; i < b; ++i) {
+        auto it = p.seqs.find(seq_ids[i]);
+        if (it == p.seqs.end()) return CA_ERR_NOT_FOUND;
+        seq_of[i] = &it->second;
     }
+    // (end node, seq_id, caller row): sorted, so that the sequences ending at
+    // one node are adjacent and in ascending seq_id (ids must be distinct).
+    struct End { const Node* node; int64_t id; int32_t row; };
+    std::vector<End> ends(b);
+    for (int32_t i = 0; i < b; ++i) ends[i] = {seq_of[i]->path.back(), seq_ids[i], i};
+    std::sort(ends.begin(), ends.end(), [](const End& x, const End& y) {
+        return x.node != y.node ? std::less<const Node*>()(x.node, y.node) : x.id < y.id;
+    });
+    // a repeated id has one path, so its copies sit side by side here
+    for (int32_t i = 1; i < b; ++i)
+        if (ends[i].node == ends[i - 1].node && ends[i].id == ends[i - 1].id) return CA_ERR_INVALID;
     const bool tpp = !(flags & CA_SCHED_NO_TPP);
     // Batch holders per node.  When the batch is every live sequence (the
     // usual decode step) they are the chunks' refcounts; otherwise each
     // batch path is marked (Node::mark).
     const bool all_live = (size_t)b == p.seqs.size();
     auto holders = [all_live](const Node* n) { return all_live ? n->refcount : n->mark; };
-    std::vector<const Sequence*> seq_of(b);
-    std::vector<std::pair<const Node*, int64_t>> ends(b);
-    for (int32_t i = 0; i < b; ++i) {
-        const Sequence& s = p.seqs.at(seq_ids[i]);
-        seq_of[i] = &s;
-        if (!all_live)
-            for (Node* n : s.path) n->mark += 1;
-        ends[i] = {s.path.back(), seq_ids[i]};
-    }
-    std::sort(ends.begin(), ends.end());
+    if (!all_live)
+        for (int32_t i = 0; i < b; ++i)
+            for (Node* n : seq_of[i]->path) n->mark += 1;
     for (int32_t i = 0; i < b;) {
         int32_t j = i;
-        while (j < b && ends[j].first == ends[i].first) ++j;
-        Node* n = const_cast<Node*>(ends[i].first);
+        while (j < b && ends[j].node == ends[i].node) ++j;
+        Node* n = const_cast<Node*>(ends[i].node);
         n->end_begin = i;
         n->end_count = j - i;
         i = j;
     }
+    // Each batch sequence's private chain: the suffix of its path held by it
+    // alone.  Holders never grow along a path, so its first node (the chain
+    // head) is found by bisection; the head records its sequence.
+    std::vector<int32_t> chain_at(b);
+    for (int32_t i = 0; i < b; ++i) {
+        const auto& path = seq_of[i]->path;
+        size_t lo = 0, hi = path.size();
+        while (lo < hi) {
+            const size_t mid = (lo + hi) / 2;
+            if (holders(path[mid]) >= 2) lo = mid + 1;
+            else hi = mid;
+        }
+        chain_at[i] = (int32_t)lo;
+        if (lo < path.size()) path[lo]->owner = i;
+    }
 
-    std::vector<int64_t> order;
-    order.reserve(b);
     t.b = b;
     for (auto* v : {&t.seq_perm, &t.cf_rows, &t.cf_runs, &t.sf_offsets, &t.sf_chunks, &t.merge_offsets,
                     &t.merge_runs})
         v->clear();
-    t.seq_perm.reserve(b);
-    t.sf_offsets.reserve(b + 1);
-    t.merge_offsets.reserve(b + 1);
+    // Depth-first order over the shared nodes only: at a node, the sequences
+    // ending there, then its children in insertion order; a child held by
+    // one batch sequence is that sequence's chain, which contributes exactly
+    // that sequence and no chunk-first row.
+    std::vector<int32_t>& order = t.seq_perm;     // DFS position -> caller row
+    order.reserve(b);
     std::vector<const Node*> row_node;
     struct Frame { const Node* node; size_t next; };
     std::vector<Frame> stack;
@@ -74,35 +93,27 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
         Frame& f = stack.back();
         const Node* node = f.node;
         if (f.next == 0 && node != &p.root) {
-            if (tpp && holders(node) >= 2) {
+            if (tpp) {
                 const_cast<Node*>(node)->row = (int32_t)row_node.size();
                 row_node.push_back(node);
-                t.cf_rows.insert(t.cf_rows.end(),
-                                 {node->slot, node->ntok, (int32_t)order.size(), -1});
+                t.cf_rows.insert(t.cf_rows.end(), {node->slot, node->ntok, (int32_t)order.size(), -1});
             }
-            for (int32_t k = 0; k < node->end_count; ++k) order.push_back(ends[node->end_begin + k].second);
+            for (int32_t k = 0; k < node->end_count; ++k) order.push_back(ends[node->end_begin + k].row);
         }
+        const auto& ch = node->children;
         size_t ci = f.next;
-        while (ci < node->children.size() && holders(node->children[ci]) == 0) ++ci;
-        if (ci < node->children.size()) {
+        for (; ci < ch.size(); ++ci) {
+            const int32_t hc = holders(ch[ci]);
+            if (hc >= 2) break;
+            if (hc == 1) order.push_back(ch[ci]->owner);
+        }
+        if (ci < ch.size()) {
             f.next = ci + 1;
-            stack.push_back({node->children[ci], 0});
+            stack.push_back({ch[ci], 0});
         } else {
             if (node->row >= 0) t.cf_rows[4 * node->row + 3] = (int32_t)order.size();
             stack.pop_back();
         }
-    }
-
-    // seq_perm: DFS position -> caller row.
-    std::vector<std::pair<int64_t, int32_t>> caller(b);
-    for (int32_t i = 0; i < b; ++i) caller[i] = {seq_ids[i], i};
-    std::sort(caller.begin(), caller.end());
-    t.seq_perm.resize(b);
-    std::vector<const Sequence*> seq_at(b);
-    for (int32_t pos = 0; pos < b; ++pos) {
-        const int32_t i = std::lower_bound(caller.begin(), caller.end(), std::make_pair(order[pos], INT32_MIN))->second;
-        t.seq_perm[pos] = i;
-        seq_at[pos] = seq_of[i];
     }
 
     // Runs.
@@ -118,18 +129,24 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
         }
     }
 
-    // Sequence-first lists.
-    t.sf_offsets.assign(1, 0);
+    // Sequence-first lists: each position's private chain (its whole path
+    // without the partition).
+    t.sf_offsets.resize((size_t)b + 1);
+    t.sf_offsets[0] = 0;
     for (int32_t pos = 0; pos < b; ++pos) {
-        // holders never grow along a path, so the chunks this sequence holds
-        // alone are a suffix of it
-        const auto& path = seq_at[pos]->path;
-        size_t k = path.size();
-        if (!tpp) k = 0;
-        else
-            while (k > 0 && holders(path[k - 1]) == 1) --k;
-        for (; k < path.size(); ++k) t.sf_chunks.insert(t.sf_chunks.end(), {path[k]->slot, path[k]->ntok});
-        t.sf_offsets.push_back((int32_t)(t.sf_chunks.size() / 2));
+        const int32_t i = order[pos];
+        const size_t k = tpp ? (size_t)chain_at[i] : 0;
+        t.sf_offsets[pos + 1] = t.sf_offsets[pos] + (int32_t)(seq_of[i]->path.size() - k);
+    }
+    t.sf_chunks.resize(2 * (size_t)t.sf_offsets[b]);
+    for (int32_t pos = 0; pos < b; ++pos) {
+        const int32_t i = order[pos];
+        const auto& path = seq_of[i]->path;
+        int32_t* dst = t.sf_chunks.data() + 2 * (size_t)t.sf_offsets[pos];
+        for (size_t k = tpp ? (size_t)chain_at[i] : 0; k < path.size(); ++k) {
+            *dst++ = path[k]->slot;
+            *dst++ = path[k]->ntok;
+        }
     }
 
     // Merge lists: runs are nested intervals listed in pre-order, so a
@@ -275,10 +292,11 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
     }
 
     // LPT: biggest chunk-first units first, each onto the least-loaded CTA.
-    // Units are collected flat with their CTA and counting-sorted at the end.
-    std::vector<std::pair<int32_t, Unit>>& tagged = plan.tagged;
-    tagged.clear();
-    tagged.reserve(cf.size() + (size_t)b + 2 * grid);
+    // Each CTA's list is its chunk-first units (in assignment order), then
+    // its sequence-first pieces (in list order); the tail queue follows.
+    std::vector<std::pair<int32_t, Unit>>& cf_at = plan.tagged;    // (CTA, unit)
+    cf_at.clear();
+    cf_at.reserve(cf.size());
     std::vector<double> load(grid, 0.0);
     {
         // Costs in 1/64 tile units; the heap key packs (load, CTA) into one
@@ -301,7 +319,7 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
             const int64_t top = heap.back();
             const int32_t k = (int32_t)(top & 0xfffff);
             const int64_t l = (top >> 20) + icost[i];
-            tagged.emplace_back(k, cf[i].u);
+            cf_at.emplace_back(k, cf[i].u);
             load[k] = l / 64.0;
             heap.back() = (l << 20) | k;
             std::push_heap(heap.begin(), heap.end(), greater);
@@ -312,47 +330,75 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
     // of the H heads, in the order h * n_p + j; positions are laid end to end
     // and each CTA takes a contiguous stretch up to its share (cumulative
     // rounding places every tile), cut into one unit per position it touches.
-    // A head split between two units gets one partial per piece.
+    // A head split between two units gets one partial per piece.  The walk
+    // keeps (head, chunk) of the point reached, so it needs no division.
     std::vector<int32_t> npart((size_t)b * H, 0);
     for (int32_t pos = 0; pos < b; ++pos)
         for (int32_t h = 0; h < H; ++h) npart[(size_t)pos * H + h] = nk1[pos];
+    std::vector<Unit>& sf_units = plan.sf_scratch;     // static pieces, in CTA order
+    std::vector<Unit>& tail_units = plan.tail_scratch;
+    std::vector<int32_t>& sf_end = plan.sf_end;        // sf_units after CTA k
+    sf_units.clear();
+    tail_units.clear();
+    sf_end.assign(grid, 0);
     {
         std::vector<double> quota(grid);
         double qsum = 0;
         for (int32_t k = 0; k < grid; ++k) { quota[k] = std::max(0.0, avg - load[k]); qsum += quota[k]; }
         const double scale = qsum > 0 ? sf_static / qsum : 0.0;
         auto seg_len = [&](int32_t ps) { return t.sf_offsets[ps + 1] - t.sf_offsets[ps]; };
-        int64_t placed = 0, done = 0;        // done: linear offset reached in `pos`
+        auto unit_at = [&](int32_t pos, int32_t h0, int32_t a, int32_t z, int32_t before) {
+            return Unit{UNIT_SF, h0, pos, pos + 1, a, z, nk1[pos] + before, t.seq_perm[pos], seg_len(pos),
+                        R + t.sf_offsets[pos], nk1[pos], 0};
+        };
+        int64_t placed = 0;
         double cum = 0;
-        int32_t pos = 0, head_pieces = 0;    // pieces already placed of the head holding `done`
+        int32_t pos = 0, hd = 0, jd = 0;    // point reached: chunk jd of head hd of `pos`
+        int32_t head_pieces = 0;            // pieces already placed of head hd
+        auto next_pos = [&]() {
+            hd = jd = head_pieces = 0;
+            ++pos;
+            while (pos < b && seg_len(pos) == 0) ++pos;
+        };
         while (pos < b && seg_len(pos) == 0) ++pos;
-        for (int32_t k = 0; k < grid && pos < b; ++k) {
+        int32_t k = 0;
+        for (; k < grid && pos < b; ++k) {
             cum += quota[k] * scale;
             const int64_t target = (k == grid - 1) ? (int64_t)sf_static : (int64_t)(cum + 0.5);
             int64_t room = target - placed;
             while (room > 0 && pos < b) {
                 const int32_t n = seg_len(pos);
-                const int64_t total = (int64_t)n * H;
-                const int64_t take = std::min<int64_t>(room, total - done);
-                const int64_t a = done, z = done + take;
-                const int32_t h0 = (int32_t)(a / n), hz = (int32_t)((z - 1) / n);
-                const int32_t before = (a % n == 0) ? 0 : head_pieces;
-                tagged.emplace_back(k, Unit{UNIT_SF, h0, pos, pos + 1, (int32_t)a, (int32_t)z,
-                                            nk1[pos] + before, t.seq_perm[pos], n,
-                                            R + t.sf_offsets[pos], nk1[pos], 0});
-                for (int32_t h = h0; h <= hz; ++h) npart[(size_t)pos * H + h] += 1;
-                head_pieces = (z % n == 0) ? 0 : ((z / n == h0) ? before + 1 : 1);
-                done = z;
+                const int64_t left = (int64_t)(H - hd) * n - jd;
+                const int32_t take = (int32_t)std::min<int64_t>(room, left);
+                const int32_t a = hd * n + jd, h0 = hd;
+                const int32_t before = (jd == 0) ? 0 : head_pieces;
+                sf_units.push_back(unit_at(pos, h0, a, a + take, before));
+                // every head the piece touches gets one more partial
+                int32_t rem = take, step = std::min(rem, n - jd);
+                npart[(size_t)pos * H + hd] += 1;
+                rem -= step;
+                jd += step;
+                while (rem > 0) {
+                    ++hd;
+                    npart[(size_t)pos * H + hd] += 1;
+                    step = std::min(rem, n);
+                    rem -= step;
+                    jd = step;
+                }
+                if (jd == n) {
+                    ++hd;
+                    jd = 0;
+                    head_pieces = 0;
+                } else {
+                    head_pieces = (hd == h0) ? before + 1 : 1;
+                }
                 placed += take;
                 room -= take;
-                if (done == total) {
-                    done = 0;
-                    head_pieces = 0;
-                    ++pos;
-                    while (pos < b && seg_len(pos) == 0) ++pos;
-                }
+                if (hd == H) next_pos();
             }
+            sf_end[k] = (int32_t)sf_units.size();
         }
+        for (; k < grid; ++k) sf_end[k] = (int32_t)sf_units.size();
         // The rest of the list becomes the tail queue: units of at most
         // `tail_unit` chunk-heads that never cross a head boundary.
         const int32_t tail_unit = std::max<int32_t>(
@@ -360,44 +406,53 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
                                                                    ((int64_t)kTailUnitsPerCta * grid))));
         while (pos < b) {
             const int32_t n = seg_len(pos);
-            const int64_t total = (int64_t)n * H;
-            const int64_t a = done;
-            const int64_t head_end = (a / n + 1) * n;
-            const int64_t z = std::min<int64_t>(a + tail_unit, head_end);
-            const int32_t h0 = (int32_t)(a / n);
-            const int32_t before = (a % n == 0) ? 0 : head_pieces;
-            tagged.emplace_back(grid, Unit{UNIT_SF, h0, pos, pos + 1, (int32_t)a, (int32_t)z,
-                                           nk1[pos] + before, t.seq_perm[pos], n,
-                                           R + t.sf_offsets[pos], nk1[pos], 0});
-            npart[(size_t)pos * H + h0] += 1;
-            head_pieces = (z % n == 0) ? 0 : before + 1;
-            done = z;
-            if (done == total) {
-                done = 0;
+            const int32_t a = hd * n + jd, len = std::min(tail_unit, n - jd);
+            const int32_t before = (jd == 0) ? 0 : head_pieces;
+            tail_units.push_back(unit_at(pos, hd, a, a + len, before));
+            npart[(size_t)pos * H + hd] += 1;
+            jd += len;
+            if (jd == n) {
+                ++hd;
+                jd = 0;
                 head_pieces = 0;
-                ++pos;
-                while (pos < b && seg_len(pos) == 0) ++pos;
+            } else {
+                head_pieces = before + 1;
             }
+            if (hd == H) next_pos();
         }
     }
 
     // partial ids per (position, query head); the G query heads of a key/value
     // head have the same pieces
-    plan.pbase.assign((size_t)b * HQ + 1, 0);
-    for (size_t i = 0; i < (size_t)b * HQ; ++i) {
-        const size_t pos = i / HQ, qh = i % HQ;
-        plan.pbase[i + 1] = plan.pbase[i] + npart[pos * H + qh / G];
+    plan.pbase.resize((size_t)b * HQ + 1);
+    {
+        int32_t acc = 0;
+        size_t i = 0;
+        plan.pbase[0] = 0;
+        for (int32_t pos = 0; pos < b; ++pos)
+            for (int32_t h = 0; h < H; ++h) {
+                const int32_t np = npart[(size_t)pos * H + h];
+                for (int32_t g = 0; g < G; ++g) plan.pbase[++i] = (acc += np);
+            }
     }
     plan.n_partials = plan.pbase.back();
-    // Counting sort by CTA (bucket `grid` is the tail queue), stable: each
-    // CTA keeps its chunk-first units first, then its sequence-first pieces in
-    // list order.
-    std::vector<int32_t> start(grid + 2, 0);
-    for (const auto& x : tagged) start[x.first + 1] += 1;
-    for (int32_t k = 0; k <= grid; ++k) start[k + 1] += start[k];
-    plan.cta_begin.assign(start.begin(), start.begin() + grid + 1);
-    plan.units.resize(tagged.size());
-    for (const auto& x : tagged) plan.units[start[x.first]++] = x.second;
+    // Lay the lists out: per CTA its chunk-first units, then its pieces.
+    plan.cta_begin.resize((size_t)grid + 1);
+    std::vector<int32_t> cur(grid, 0);
+    for (const auto& x : cf_at) cur[x.first] += 1;
+    int32_t off = 0;
+    for (int32_t k = 0; k < grid; ++k) {
+        plan.cta_begin[k] = off;
+        off += cur[k] + sf_end[k] - (k ? sf_end[k - 1] : 0);
+        cur[k] = plan.cta_begin[k];
+    }
+    plan.cta_begin[grid] = off;
+    plan.units.resize((size_t)off + tail_units.size());
+    for (const auto& x : cf_at) plan.units[cur[x.first]++] = x.second;
+    for (int32_t k = 0; k < grid; ++k)
+        std::copy(sf_units.begin() + (k ? sf_end[k - 1] : 0), sf_units.begin() + sf_end[k],
+                  plan.units.begin() + cur[k]);
+    std::copy(tail_units.begin(), tail_units.end(), plan.units.begin() + off);
 }
 
 namespace {
