@@ -64,6 +64,9 @@ def cpu_baseline(wl, seconds: float = CPU_SAMPLE_SECONDS) -> dict:
     trie = OracleTrie(wl.chunk, 1 << 20)
     for sid in wl.seq_ids():
         k, v = wl.kv_rows(sid)
+        if wl.kv_dtype == "fp8":             # the oracle attends over the dequantised rows
+            from oracle import fp8
+            k, v = fp8.dequantize(fp8.quantize(k, 1.0), 1.0), fp8.dequantize(fp8.quantize(v, 1.0), 1.0)
         trie.insert(sid, wl.tokens(sid), k, v)
     batch = wl.seq_ids()
     q = wl.queries(0)
@@ -204,13 +207,15 @@ def run_ours(args):
     def make_pools(n, no_sharing=False, headroom=1.5):
         ps = []
         for _ in range(n):
-            pc = Pool(L, H, D, c, capacity_for(wl, headroom=headroom), no_sharing=no_sharing, n_kv_heads=HK)
+            pc = Pool(L, H, D, c, capacity_for(wl, headroom=headroom), no_sharing=no_sharing, n_kv_heads=HK,
+                      kv_dtype=wl.kv_dtype)
             for sid in batch:
                 insert_sequence(pc, wl, sid, staging=staging)
             ps.append(pc)
         return ps
 
-    kv_bytes = wl.unique_tokens() * HK * D * 2 * 2              # one layer's K and V, fp16
+    eb = 1 if wl.kv_dtype == "fp8" else 2                       # bytes per stored K/V element
+    kv_bytes = wl.unique_tokens() * HK * D * 2 * eb             # one layer's K and V
     n_copies = 1 if churn else copies_for(kv_bytes)
     pools = make_pools(n_copies)
     pool = pools[0]
@@ -363,7 +368,7 @@ def run_ours(args):
         no_tpp = [p_.schedule(batch, no_tpp=True) for p_ in pools]
         us_no_tpp = time_calls(pools, no_tpp)
         del no_tpp
-        flat_bytes = sum(wl.seq_len(sid) for sid in batch) * HK * D * 2 * 2
+        flat_bytes = sum(wl.seq_len(sid) for sid in batch) * HK * D * 2 * eb
         flats = make_pools(copies_for(flat_bytes), no_sharing=True, headroom=1.05)
         us_flat = time_calls(flats, [f.schedule(batch) for f in flats])
         del flats
@@ -394,7 +399,8 @@ def run_ours(args):
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16 (fp32 accumulate)",
+        "dtype": ("f16 q/out, fp8 e4m3 K/V storage (fp32 accumulate)" if wl.kv_dtype == "fp8"
+                  else "f16 (fp32 accumulate)"),
         "data": "synthetic (seeded N(0,1) fp16 Q/K/V; token segments shaped like the pages' shared system prompts)",
         "config": {"workload": wl.name, "description": wl.description, "batch": b, "n_heads": H,
                    "n_kv_heads": HK,

@@ -29,6 +29,8 @@
  *    stream).  All device work is enqueued asynchronously on it.
  *  - Objects are not thread-safe: serialise calls on one pool.
  *  - Element type of K, V, Q and out is IEEE fp16; accumulation is fp32.
+ *    A pool created with CA_KV_FP8 stores K and V as 8-bit floats (below);
+ *    its inputs and outputs stay fp16.
  */
 #ifndef CHUNK_ATTENTION_H
 #define CHUNK_ATTENTION_H
@@ -58,6 +60,18 @@ extern "C" {
 /* Never match prefixes: every sequence owns a private chain of chunks.  This
  * is the flat paged-KV layout [CA §5, PagedAttention] used as the control. */
 #define CA_NO_SHARING        1u
+/* Store K and V as FP8 E4M3 (OCP 8-bit float: 1 sign, 4 exponent bits with
+ * bias 7, 3 mantissa bits, largest finite 448, no infinities) instead of
+ * fp16, halving the pool's bytes and the bytes every decode call reads.
+ * Inserted rows are quantised on the device as
+ *     code = E4M3(fp32(x) * fp32(1 / scale)),  round to nearest even,
+ *     values beyond +-448 saturate to +-448,
+ * with scale = k_scale for keys and v_scale for values, and read back as
+ * code * scale exactly.  Attention is then the plain definition over those
+ * dequantised keys and values.  Needs head_dim 128.  The pages' own kernels
+ * keep fp16; this is one of the variants their tuning discussion leaves open
+ * [CA §4.1 on other model configurations]. */
+#define CA_KV_FP8            2u
 
 /* ---- schedule flags ---------------------------------------------------- */
 /* Treat every chunk as sequence-first even when the batch shares it (no
@@ -81,8 +95,10 @@ typedef struct {
     int32_t  head_dim;
     int32_t  chunk;           /* c: tokens per chunk                           */
     int32_t  capacity_slots;  /* chunk slots in the device pool                */
-    uint32_t flags;           /* CA_NO_SHARING or 0                            */
+    uint32_t flags;           /* CA_NO_SHARING | CA_KV_FP8, or 0               */
     int32_t  n_kv_heads;      /* key/value heads (0: n_heads)                  */
+    float    k_scale;         /* CA_KV_FP8 only: key scale (0: 1.0)            */
+    float    v_scale;         /* CA_KV_FP8 only: value scale (0: 1.0)          */
 } ca_pool_config;
 
 typedef struct {
@@ -94,10 +110,11 @@ typedef struct {
 } ca_stats;
 
 /* ---- pool ----------------------------------------------------------------
- * Device layout: the K/V tiles (row-major, fp16, head = key/value head)
+ * Device layout: the K/V tiles (row-major, fp16 or with CA_KV_FP8 one byte
+ * per element, head = key/value head)
  *     kv[slot][layer][K|V][head][c][head_dim]
  * so one chunk of one head is a contiguous c x head_dim tile (16 KiB at
- * c = 64, D = 128) that the kernels fetch whole with TMA; then one int32 per
+ * c = 64, D = 128 in fp16) that the kernels fetch whole with TMA; then one int32 per
  * slot holding the chunk's valid-token count (the kernels read it, so a
  * decode-time append can grow a partial chunk without a new schedule).
  */

@@ -23,6 +23,8 @@ Modules:
                  Prefix-Aware KV Cache / 動的プレフィックス検出].
 * ``schedule``  the per-step tables of the two-phase partition
                  [CA-summary §3.2, §3.3].
+* ``fp8``       FP8 E4M3 quantisation of stored K/V for an 8-bit pool (the
+                 published E4M3 format, restated from its definition).
 * ``attention`` decode attention by its plain definition, the partial-result
                  triple (o, m, s) and its log-sum-exp merge, and the two-phase
                  evaluation over the schedule tables [CA-blog, Two-Phase

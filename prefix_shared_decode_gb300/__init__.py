@@ -41,14 +41,20 @@ class Pool:
     """A prefix-aware KV cache: the chunk trie and its device pool.
 
     With ``host_only=True`` no GPU memory is touched (trie, allocator and
-    schedule tables only)."""
+    schedule tables only).  ``kv_dtype="fp8"`` stores K and V as FP8 E4M3
+    with the given scales (inserted rows stay fp16; the library quantises)."""
 
     def __init__(self, n_layers: int, n_heads: int, head_dim: int, chunk: int,
                  capacity_slots: int, no_sharing: bool = False, host_only: bool = False,
-                 device=None, n_kv_heads: int | None = None):
+                 device=None, n_kv_heads: int | None = None, kv_dtype: str = "fp16",
+                 k_scale: float = 1.0, v_scale: float = 1.0):
         L = capi.lib()
-        self.cfg = capi.PoolConfig(n_layers, n_heads, head_dim, chunk, capacity_slots,
-                                   capi.CA_NO_SHARING if no_sharing else 0, n_kv_heads or 0)
+        if kv_dtype not in ("fp16", "fp8"):
+            raise ValueError("kv_dtype must be 'fp16' or 'fp8'")
+        flags = (capi.CA_NO_SHARING if no_sharing else 0) | (capi.CA_KV_FP8 if kv_dtype == "fp8" else 0)
+        self.cfg = capi.PoolConfig(n_layers, n_heads, head_dim, chunk, capacity_slots, flags,
+                                   n_kv_heads or 0, float(k_scale), float(v_scale))
+        self.kv_dtype, self.k_scale, self.v_scale = kv_dtype, float(k_scale), float(v_scale)
         self.n_layers, self.n_heads, self.head_dim, self.chunk = n_layers, n_heads, head_dim, chunk
         self.n_kv_heads = n_kv_heads or n_heads
         self.capacity_slots = capacity_slots
@@ -80,18 +86,23 @@ class Pool:
     def handle(self):
         return self._h
 
+    def _tile_bytes(self) -> int:
+        eb = 1 if self.kv_dtype == "fp8" else 2
+        return self.capacity_slots * self.n_layers * 2 * self.n_kv_heads * self.chunk * self.head_dim * eb
+
     def kv_view(self):
-        """The device pool's K/V tiles as fp16 [slots, L, 2, H, c, D] (a view)."""
+        """The device pool's K/V tiles as [slots, L, 2, H, c, D] (a view):
+        fp16, or the E4M3 codes as uint8 for an fp8 pool."""
         import torch
-        tiles = self.capacity_slots * self.n_layers * 2 * self.n_kv_heads * self.chunk * self.head_dim * 2
-        t = self._kv[self._kv_offset:self._kv_offset + tiles].view(torch.float16)
+        t = self._kv[self._kv_offset:self._kv_offset + self._tile_bytes()]
+        if self.kv_dtype == "fp16":
+            t = t.view(torch.float16)
         return t.view(self.capacity_slots, self.n_layers, 2, self.n_kv_heads, self.chunk, self.head_dim)
 
     def slot_ntok_view(self):
         """The pool's per-slot valid-token counts, int32 [slots] (a view)."""
         import torch
-        tiles = self.capacity_slots * self.n_layers * 2 * self.n_kv_heads * self.chunk * self.head_dim * 2
-        a = self._kv_offset + tiles
+        a = self._kv_offset + self._tile_bytes()
         return self._kv[a:a + 4 * self.capacity_slots].view(torch.int32)
 
     def match_prefix(self, tokens) -> int:

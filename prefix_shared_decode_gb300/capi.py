@@ -18,6 +18,7 @@ ERRORS = {
 }
 CA_STATIC_WS_BYTES = 16 << 20
 CA_NO_SHARING = 1
+CA_KV_FP8 = 2
 CA_SCHED_NO_TPP = 1
 
 # Every symbol the header declares, in header order.
@@ -34,7 +35,7 @@ EXPORTS = [
 class PoolConfig(C.Structure):
     _fields_ = [("n_layers", C.c_int32), ("n_heads", C.c_int32), ("head_dim", C.c_int32),
                 ("chunk", C.c_int32), ("capacity_slots", C.c_int32), ("flags", C.c_uint32),
-                ("n_kv_heads", C.c_int32)]
+                ("n_kv_heads", C.c_int32), ("k_scale", C.c_float), ("v_scale", C.c_float)]
 
 
 class Stats(C.Structure):

@@ -77,7 +77,8 @@ struct AttnParams {
     float2* part_ms;             // [P] (running max in log2 units, sum of exp2)
     int32_t n_layers, n_heads, layer, capacity;   // n_heads: query heads
     int32_t n_kv_heads, group;                     // key/value heads, n_heads / n_kv_heads
-    float scale_log2;            // scale * log2(e)
+    float scale_log2;            // scale * log2(e) (times the key scale of an fp8 pool)
+    float out_scale;             // value scale of an fp8 pool, else 1
     int32_t n_stages;
 };
 
@@ -185,6 +186,10 @@ struct ScatterChunk {
 inline int32_t kv_heads(const ca_pool_config& c) { return c.n_kv_heads > 0 ? c.n_kv_heads : c.n_heads; }
 
 // Device bytes of the pool: the K/V tiles, then the per-slot token counts.
+// Bytes per stored K/V element (fp16, or 1 for an FP8 pool) and the
+// effective dequantisation scales.
+inline int kv_elem_bytes(const ca_pool_config& c) { return (c.flags & CA_KV_FP8) ? 1 : 2; }
+inline float kv_scale_of(float s) { return s == 0.f ? 1.f : s; }
 size_t pool_tile_bytes(const ca_pool_config& c);
 size_t pool_total_bytes(const ca_pool_config& c);
 
@@ -217,8 +222,8 @@ void layout_plan(const Plan& plan, int32_t b, PlanLayout& lay, std::vector<unsig
 void layout_ws(const Plan& plan, const Pool& p, int32_t b, WsLayout& ws);
 
 // kernels.cu
-int kernel_smem_bytes(int chunk, int head_dim, int* n_stages, size_t* bytes);
-int kernel_ctas_per_sm(int chunk, int head_dim, int* ctas);
+int kernel_smem_bytes(const ca_pool_config& c, int* n_stages, size_t* bytes);
+int kernel_ctas_per_sm(const ca_pool_config& c, int* ctas);
 int make_tensor_map(Pool& p);
 int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_rows,
                    const std::vector<ScatterChunk>& chunks, void* stream);

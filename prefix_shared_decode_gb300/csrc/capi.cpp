@@ -36,7 +36,12 @@ int check_cfg(const ca_pool_config* c) {
     if (c->n_layers < 1 || c->n_heads < 1 || c->capacity_slots < 1) return CA_ERR_INVALID;
     if (c->head_dim != 64 && c->head_dim != 128) return CA_ERR_UNSUPPORTED;
     if (c->chunk != 16 && c->chunk != 32 && c->chunk != 64) return CA_ERR_UNSUPPORTED;
-    if (c->flags & ~CA_NO_SHARING) return CA_ERR_INVALID;
+    if (c->flags & ~(CA_NO_SHARING | CA_KV_FP8)) return CA_ERR_INVALID;
+    if (c->flags & CA_KV_FP8) {
+        if (c->head_dim != 128) return CA_ERR_UNSUPPORTED;
+        for (float sc : {c->k_scale, c->v_scale})
+            if (!(sc == 0.f || (sc > 0.f && sc < 3.0e38f))) return CA_ERR_INVALID;
+    }
     if (c->n_kv_heads < 0 || (c->n_kv_heads > 0 && c->n_heads % c->n_kv_heads)) return CA_ERR_INVALID;
     if (c->n_heads / kv_heads(*c) > 64) return CA_ERR_UNSUPPORTED;
     // TMA row coordinates are 32-bit.
@@ -102,7 +107,7 @@ int ca_pool_create(const ca_pool_config* cfg, void* kv_dev, size_t kv_bytes, ca_
             if (cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess)
                 return CA_ERR_CUDA;
             int ctas = 1;
-            st = kernel_ctas_per_sm(cfg->chunk, cfg->head_dim, &ctas);
+            st = kernel_ctas_per_sm(*cfg, &ctas);
             if (st) return st;
             p->num_sms *= ctas;   // grid = resident CTAs
             st = make_tensor_map(*p);
@@ -393,7 +398,9 @@ AttnParams attn_params(const Pool& pool, const Sched& s, int32_t layer, const vo
     a.group = pool.cfg.n_heads / a.n_kv_heads;
     a.layer = layer;
     a.capacity = pool.cfg.capacity_slots;
-    a.scale_log2 = scale * 1.4426950408889634f;
+    const bool f8 = (pool.cfg.flags & CA_KV_FP8) != 0;
+    a.scale_log2 = scale * 1.4426950408889634f * (f8 ? kv_scale_of(pool.cfg.k_scale) : 1.f);
+    a.out_scale = f8 ? kv_scale_of(pool.cfg.v_scale) : 1.f;
     return a;
 }
 }  // namespace ca

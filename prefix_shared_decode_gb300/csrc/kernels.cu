@@ -133,6 +133,19 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
 }
+// FP8 E4M3 <-> fp16/fp32 conversions (hardware cvt, round to nearest even).
+// In a packed pair the byte at the lower address is the low half.
+__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t v16) {
+    uint32_t r;
+    const uint16_t v = (uint16_t)v16;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -220,7 +233,7 @@ __global__ void __launch_bounds__(128) merge_partials_kernel(const AttnParams p,
         }
         M = mg;
     }
-    const float inv = 1.f / S;
+    const float inv = p.out_scale / S;          // an fp8 pool's value scale, else 1
     uint16_t* dst = p.out + ((size_t)row * p.n_heads + gw % p.n_heads) * D + lane * DPL;
     if constexpr (DPL == 4) {
         uint2 v;
@@ -238,14 +251,14 @@ __global__ void __launch_bounds__(128) merge_partials_kernel(const AttnParams p,
 // Scores are reduce-scattered across the warp so that each lane ends with
 // the score of token (L >> (5 - log2 NT)); online softmax in log2 units.
 // ---------------------------------------------------------------------------
-template <int C, int D>
+template <int C, int D, int EB>
 __device__ __forceinline__ void sf_chunk(const uint8_t* kt, const uint8_t* vt, int ntok,
                                          const float (&q)[D / 32], float& m, float& s,
                                          float (&o)[D / 32], int w, int lane) {
     constexpr int DPL = D / 32;
     constexpr int NT = C / kConsumerWarps;
     constexpr int LOGNT = NT == 16 ? 4 : NT == 8 ? 3 : 2;
-    constexpr int BPL = DPL * 2;                      // bytes per lane per row
+    constexpr int BPL = DPL * EB;                     // bytes per lane per row
     const int kidx = (lane * BPL) >> 4, within = (lane * BPL) & 15;
 
     float part[NT];
@@ -253,7 +266,13 @@ __device__ __forceinline__ void sf_chunk(const uint8_t* kt, const uint8_t* vt, i
     for (int t = 0; t < NT; ++t) {
         const int r = w * NT + t;
         const uint8_t* src = kt + swz(r, kidx, C) + within;
-        if constexpr (DPL == 4) {
+        if constexpr (EB == 1) {                      // fp8: four bytes, two converts
+            const uint32_t raw = *reinterpret_cast<const uint32_t*>(src);
+            const uint32_t lo = f16x2_from_e4m3x2(raw & 0xffffu), hi = f16x2_from_e4m3x2(raw >> 16);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+            part[t] = q[0] * a.x + q[1] * a.y + q[2] * b.x + q[3] * b.y;
+        } else if constexpr (DPL == 4) {
             const uint2 raw = *reinterpret_cast<const uint2*>(src);
             const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
             const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
@@ -300,7 +319,13 @@ __device__ __forceinline__ void sf_chunk(const uint8_t* kt, const uint8_t* vt, i
     for (int t = 0; t < NT; ++t) {
         const float pt = __shfl_sync(kFull, pj, t << (5 - LOGNT));
         const uint8_t* src = vt + swz(w * NT + t, kidx, C) + within;
-        if constexpr (DPL == 4) {
+        if constexpr (EB == 1) {
+            const uint32_t raw = *reinterpret_cast<const uint32_t*>(src);
+            const uint32_t lo = f16x2_from_e4m3x2(raw & 0xffffu), hi = f16x2_from_e4m3x2(raw >> 16);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+            o[0] += pt * a.x; o[1] += pt * a.y; o[2] += pt * b.x; o[3] += pt * b.y;
+        } else if constexpr (DPL == 4) {
             const uint2 raw = *reinterpret_cast<const uint2*>(src);
             const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
             const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
@@ -401,33 +426,56 @@ __device__ __forceinline__ void cf_chunk(uint32_t kt, uint32_t vt, int ntok, int
     }
 }
 
-// Shared-memory map of one CTA.
-template <int C, int D>
+// An fp8 chunk-head tile (C rows of 128 one-byte dims, 128-byte swizzled as
+// TMA stores it) widened to the fp16 tile layout the tensor-core code reads
+// (two 64-dim boxes, each 128-byte swizzled).  E4M3 values are exact in fp16.
+// All consumer threads take part.
+template <int C>
+__device__ __forceinline__ void f8_tile_to_f16(const uint8_t* src, uint8_t* dst, int tid) {
+#pragma unroll 2
+    for (int i = tid; i < C * 8; i += kConsumerWarps * 32) {
+        const int r = i >> 3, kc = i & 7;
+        const uint4 v = *reinterpret_cast<const uint4*>(src + r * 128 + ((kc ^ (r & 7)) << 4));
+        uint4 a, b;
+        a.x = f16x2_from_e4m3x2(v.x & 0xffffu); a.y = f16x2_from_e4m3x2(v.x >> 16);
+        a.z = f16x2_from_e4m3x2(v.y & 0xffffu); a.w = f16x2_from_e4m3x2(v.y >> 16);
+        b.x = f16x2_from_e4m3x2(v.z & 0xffffu); b.y = f16x2_from_e4m3x2(v.z >> 16);
+        b.z = f16x2_from_e4m3x2(v.w & 0xffffu); b.w = f16x2_from_e4m3x2(v.w >> 16);
+        *reinterpret_cast<uint4*>(dst + swz(r, 2 * kc, C)) = a;
+        *reinterpret_cast<uint4*>(dst + swz(r, 2 * kc + 1, C)) = b;
+    }
+}
+
+// Shared-memory map of one CTA.  EB: bytes per stored K/V element (2 for
+// fp16, 1 for fp8, which adds an fp16 copy of one stage for the tensor cores).
+template <int C, int D, int EB>
 struct Smem {
-    static constexpr int kTile = C * D * 2;     // one K or V tile of one chunk-head
+    static constexpr int kTile = C * D * EB;    // one K or V tile of one chunk-head
     static constexpr int kStage = 2 * kTile;    // K then V
+    static constexpr int kConvBytes = EB == 1 ? 2 * C * D * 2 : 0;
     static constexpr int kQBytes = kQRows * D * 2;
     static constexpr int kXmsBytes = 512;
     static constexpr int kBarBytes = 2 * kMaxStages * 8;
     static constexpr int kRingBytes = kRing * 4 + kMaxStages * 4;
     static size_t bytes(int stages) {
-        return (size_t)stages * kStage + kQBytes + kXmsBytes + kBarBytes + kRingBytes;
+        return (size_t)stages * kStage + kConvBytes + kQBytes + kXmsBytes + kBarBytes + kRingBytes;
     }
 };
 
 // ---------------------------------------------------------------------------
 // The persistent two-phase kernel.
 // ---------------------------------------------------------------------------
-template <int C, int D>
+template <int C, int D, int EB>
 __global__ void __launch_bounds__(kThreads, 2)
 two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnParams p) {
-    using SM = Smem<C, D>;
+    using SM = Smem<C, D, EB>;
     constexpr int DPL = D / 32;
-    constexpr int BOXES = D / 64;
+    constexpr int BOXES = D * EB / 128;   // 128-byte boxes per tile row
     extern __shared__ __align__(1024) uint8_t smem[];
     const int S = p.n_stages;
     uint8_t* stages = smem;
-    uint8_t* qreg = smem + (size_t)S * SM::kStage;
+    uint8_t* conv = smem + (size_t)S * SM::kStage;       // fp8 pools: fp16 copy of one stage
+    uint8_t* qreg = conv + SM::kConvBytes;
     float* xms = reinterpret_cast<float*>(qreg + SM::kQBytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xms) + SM::kXmsBytes);
     volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(bars + 2 * kMaxStages);
@@ -552,8 +600,8 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 const int rowV = rowK + HK * C;
 #pragma unroll
                 for (int bx = 0; bx < BOXES; ++bx) {
-                    tma_load_2d(dst + bx * C * 128, &tmap, bx * 64, rowK, fb, pol);
-                    tma_load_2d(dst + SM::kTile + bx * C * 128, &tmap, bx * 64, rowV, fb, pol);
+                    tma_load_2d(dst + bx * C * 128, &tmap, bx * (128 / EB), rowK, fb, pol);
+                    tma_load_2d(dst + SM::kTile + bx * C * 128, &tmap, bx * (128 / EB), rowV, fb, pol);
                 }
                 stage_ntok[st] = min(max(ntok, 0), C);
                 mbar_arrive(fb);
@@ -653,7 +701,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
 #pragma unroll
                     for (int d = 0; d < DPL; ++d) { q[d] *= p.scale_log2; o[d] = 0.f; }
                 }
-                for (int j = L - h * n; L < seg_end; ++L, ++j, ++it) {
+                for (; L < seg_end; ++L, ++it) {
                     const int st = it % S;
                     if (!mbar_wait(full0 + 8 * st, (uint32_t)(it / S) & 1u)) {
                         set_status(p.status, CA_ERR_TIMEOUT);
@@ -661,7 +709,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     }
                     const int ntok = stage_ntok[st];
                     const uint8_t* kt = stages + (size_t)st * SM::kStage;
-                    sf_chunk<C, D>(kt, kt + SM::kTile, ntok, q, m, s, o, w, lane);
+                    sf_chunk<C, D, EB>(kt, kt + SM::kTile, ntok, q, m, s, o, w, lane);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(empty0 + 8 * st);
                 }
@@ -754,10 +802,22 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                         set_status(p.status, CA_ERR_TIMEOUT);
                         return;
                     }
+                    uint32_t kt = smem_u32(stages + (size_t)st * SM::kStage);
+                    uint32_t vt = kt + SM::kTile;
+                    const int ntok = stage_ntok[st];
+                    if constexpr (EB == 1) {
+                        // Widen the stage into the fp16 copy (once every warp is
+                        // done with the previous one), then free the stage.
+                        consumer_sync();
+                        const uint8_t* sk = stages + (size_t)st * SM::kStage;
+                        f8_tile_to_f16<C>(sk, conv, threadIdx.x);
+                        f8_tile_to_f16<C>(sk + SM::kTile, conv + SM::kConvBytes / 2, threadIdx.x);
+                        consumer_sync();
+                        if (lane == 0) mbar_arrive(empty0 + 8 * st);
+                        kt = smem_u32(conv);
+                        vt = kt + SM::kConvBytes / 2;
+                    }
                     if (active) {
-                        const int ntok = stage_ntok[st];
-                        const uint32_t kt = smem_u32(stages + (size_t)st * SM::kStage);
-                        const uint32_t vt = kt + SM::kTile;
                         if (NTw == 16) {
                             cf_chunk<C, D, 16>(kt, vt, ntok, tp * 16, qblock, p.scale_log2, m, s, o, lane);
                         } else if constexpr (C >= 32) {
@@ -766,8 +826,10 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                                 cf_chunk<C, D, 32>(kt, vt, ntok, t0, qblock, p.scale_log2, m, s, o, lane);
                         }
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(empty0 + 8 * st);
+                    if constexpr (EB == 2) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(empty0 + 8 * st);
+                    }
                 }
                 // Row sums are per thread so far: reduce over the quad.
 #pragma unroll
@@ -853,28 +915,60 @@ constexpr int kScatterMaxChunks = 128;    // chunks per launch (small parameter 
 struct ScatterArgs {
     const uint4* k;
     const uint4* v;
-    uint4* pool;
+    void* pool;
     int32_t* slot_ntok;
     int32_t total_rows, chunk, n_layers, n_heads, vec_per_row, n_chunks;
+    float inv_k, inv_v;                   // fp8 pools: 1 / scale (fp32)
     ScatterChunk ch[kScatterMaxChunks];
 };
 
+// One CTA per (chunk, layer, head): a c x D tile of K and one of V, eight
+// elements per step.  An fp8 pool stores E4M3(fp32(x) * inv_scale).  A chunk
+// written from its first row (a new chunk) gets zeros in the rows past its
+// tokens: the kernels give those rows weight 0, which must not meet a NaN.
+template <bool F8>
 __global__ void __launch_bounds__(256) kv_scatter_kernel(const __grid_constant__ ScatterArgs a) {
-    // one CTA per (chunk, layer, head): a c x D tile of K and one of V
     const int h = blockIdx.x % a.n_heads;
     const int rest = blockIdx.x / a.n_heads;
     const int ci = rest % a.n_chunks, l = rest / a.n_chunks;
     const ScatterChunk c = a.ch[ci];
-    const int total = c.n_rows * a.vec_per_row;
+    const int total = (c.dst_row == 0 ? a.chunk : c.n_rows) * a.vec_per_row;
     if (h == 0 && l == 0 && threadIdx.x == 0) a.slot_ntok[c.slot] = c.dst_row + c.n_rows;
     const long long tile = ((((long long)c.slot * a.n_layers + l) * 2 * a.n_heads + h) * a.chunk +
                             c.dst_row) * a.vec_per_row;
     const long long vtile = tile + (long long)a.n_heads * a.chunk * a.vec_per_row;
     for (int i = threadIdx.x; i < total; i += blockDim.x) {
         const int r = i / a.vec_per_row, vec = i % a.vec_per_row;
+        if (r >= c.n_rows) {                     // past the tokens of a new chunk
+            if constexpr (F8) {
+                static_cast<uint2*>(a.pool)[tile + i] = make_uint2(0u, 0u);
+                static_cast<uint2*>(a.pool)[vtile + i] = make_uint2(0u, 0u);
+            } else {
+                static_cast<uint4*>(a.pool)[tile + i] = make_uint4(0u, 0u, 0u, 0u);
+                static_cast<uint4*>(a.pool)[vtile + i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            continue;
+        }
         const long long src = (((long long)l * a.total_rows + c.src_row + r) * a.n_heads + h) * a.vec_per_row + vec;
-        a.pool[tile + i] = a.k[src];
-        a.pool[vtile + i] = a.v[src];
+        if constexpr (F8) {
+            auto pack = [](const uint4 x, float inv) {
+                const __half2* hp = reinterpret_cast<const __half2*>(&x);
+                uint32_t w[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 f = __half22float2(hp[k]);
+                    w[k] = e4m3x2_from_f32(f.x * inv, f.y * inv);
+                }
+                return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+            };
+            uint2* pool = static_cast<uint2*>(a.pool);
+            pool[tile + i] = pack(a.k[src], a.inv_k);
+            pool[vtile + i] = pack(a.v[src], a.inv_v);
+        } else {
+            uint4* pool = static_cast<uint4*>(a.pool);
+            pool[tile + i] = a.k[src];
+            pool[vtile + i] = a.v[src];
+        }
     }
 }
 
@@ -884,46 +978,53 @@ __global__ void __launch_bounds__(256) kv_scatter_kernel(const __grid_constant__
 // Host launchers.
 // ---------------------------------------------------------------------------
 namespace {
-template <int C, int D>
+template <int C, int D, int EB>
 void* kernel_ptr() {
-    return reinterpret_cast<void*>(&dev::two_phase_attention_kernel<C, D>);
+    return reinterpret_cast<void*>(&dev::two_phase_attention_kernel<C, D, EB>);
 }
-void* pick_kernel(int chunk, int head_dim) {
-    if (head_dim == 128) {
-        if (chunk == 64) return kernel_ptr<64, 128>();
-        if (chunk == 32) return kernel_ptr<32, 128>();
-        if (chunk == 16) return kernel_ptr<16, 128>();
-    } else if (head_dim == 64) {
-        if (chunk == 64) return kernel_ptr<64, 64>();
-        if (chunk == 32) return kernel_ptr<32, 64>();
-        if (chunk == 16) return kernel_ptr<16, 64>();
+void* pick_kernel(const ca_pool_config& c) {
+    if (kv_elem_bytes(c) == 1) {
+        if (c.head_dim != 128) return nullptr;
+        if (c.chunk == 64) return kernel_ptr<64, 128, 1>();
+        if (c.chunk == 32) return kernel_ptr<32, 128, 1>();
+        if (c.chunk == 16) return kernel_ptr<16, 128, 1>();
+    } else if (c.head_dim == 128) {
+        if (c.chunk == 64) return kernel_ptr<64, 128, 2>();
+        if (c.chunk == 32) return kernel_ptr<32, 128, 2>();
+        if (c.chunk == 16) return kernel_ptr<16, 128, 2>();
+    } else if (c.head_dim == 64) {
+        if (c.chunk == 64) return kernel_ptr<64, 64, 2>();
+        if (c.chunk == 32) return kernel_ptr<32, 64, 2>();
+        if (c.chunk == 16) return kernel_ptr<16, 64, 2>();
     }
     return nullptr;
 }
-size_t smem_for(int chunk, int head_dim, int stages) {
-    const size_t stage = (size_t)2 * chunk * head_dim * 2;
-    return (size_t)stages * stage + (size_t)dev::kQRows * head_dim * 2 + 512 + 2 * dev::kMaxStages * 8 +
-           4 * dev::kRing + 4 * dev::kMaxStages;
+// The kernel's dynamic shared memory (the Smem map above, computed here).
+size_t smem_for(const ca_pool_config& c, int stages) {
+    const size_t eb = (size_t)kv_elem_bytes(c), cd = (size_t)c.chunk * c.head_dim;
+    const size_t conv = eb == 1 ? 2 * cd * 2 : 0;
+    return (size_t)stages * 2 * cd * eb + conv + (size_t)dev::kQRows * c.head_dim * 2 + 512 +
+           2 * dev::kMaxStages * 8 + 4 * dev::kRing + 4 * dev::kMaxStages;
 }
 }  // namespace
 
 // Stages that fit two CTAs per SM (113 KiB each, at most 8).
-int kernel_smem_bytes(int chunk, int head_dim, int* n_stages, size_t* bytes) {
-    if (!pick_kernel(chunk, head_dim)) return CA_ERR_UNSUPPORTED;
+int kernel_smem_bytes(const ca_pool_config& c, int* n_stages, size_t* bytes) {
+    if (!pick_kernel(c)) return CA_ERR_UNSUPPORTED;
     const size_t budget = 113 * 1024;
     int st = dev::kMaxStages;
-    while (st > 1 && smem_for(chunk, head_dim, st) > budget) --st;
+    while (st > 1 && smem_for(c, st) > budget) --st;
     *n_stages = st;
-    *bytes = smem_for(chunk, head_dim, st);
+    *bytes = smem_for(c, st);
     return CA_OK;
 }
 
-int kernel_ctas_per_sm(int chunk, int head_dim, int* ctas) {
-    void* fn = pick_kernel(chunk, head_dim);
+int kernel_ctas_per_sm(const ca_pool_config& c, int* ctas) {
+    void* fn = pick_kernel(c);
     if (!fn) return CA_ERR_UNSUPPORTED;
     int st;
     size_t bytes;
-    kernel_smem_bytes(chunk, head_dim, &st, &bytes);
+    kernel_smem_bytes(c, &st, &bytes);
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
         return CA_ERR_CUDA;
     int n = 0;
@@ -945,16 +1046,19 @@ int make_tensor_map(Pool& p) {
         q != cudaDriverEntryPointSuccess || !fn)
         return CA_ERR_CUDA;
     const ca_pool_config& c = p.cfg;
-    // The pool as a 2-D tensor: rows of head_dim fp16, one row per
-    // (slot, layer, K|V, head, token-in-chunk).
+    // The pool as a 2-D tensor: rows of head_dim elements (fp16, or bytes for
+    // an fp8 pool), one row per (slot, layer, K|V, head, token-in-chunk);
+    // boxes of 128 bytes x c rows.
+    const int eb = kv_elem_bytes(c);
     const cuuint64_t rows = (cuuint64_t)c.capacity_slots * c.n_layers * 2 * kv_heads(c) * c.chunk;
     const cuuint64_t dims[2] = {(cuuint64_t)c.head_dim, rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)c.chunk};
+    const cuuint64_t strides[1] = {(cuuint64_t)c.head_dim * eb};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / eb), (cuuint32_t)c.chunk};
     const cuuint32_t estr[2] = {1, 1};
     CUtensorMap* map = reinterpret_cast<CUtensorMap*>(p.tmap);
     CUresult r = reinterpret_cast<EncodeFn>(fn)(
-        map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.kv, dims, strides, box, estr,
+        map, eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.kv, dims, strides,
+        box, estr,
         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? CA_OK : CA_ERR_CUDA;
@@ -974,7 +1078,7 @@ int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_ro
         dev::ScatterArgs a;
         a.k = static_cast<const uint4*>(k);
         a.v = static_cast<const uint4*>(v);
-        a.pool = static_cast<uint4*>(p.kv);
+        a.pool = p.kv;
         a.slot_ntok = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(p.kv) + pool_tile_bytes(c));
         a.total_rows = total_rows;
         a.chunk = c.chunk;
@@ -982,9 +1086,14 @@ int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_ro
         a.n_heads = kv_heads(c);
         a.vec_per_row = c.head_dim / 8;
         a.n_chunks = (int32_t)cnt;
+        a.inv_k = 1.f / kv_scale_of(c.k_scale);
+        a.inv_v = 1.f / kv_scale_of(c.v_scale);
         std::copy(chunks.begin() + i, chunks.begin() + i + cnt, a.ch);
         const unsigned blocks = (unsigned)(cnt * c.n_layers * a.n_heads);
-        dev::kv_scatter_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+        if (kv_elem_bytes(c) == 1)
+            dev::kv_scatter_kernel<true><<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
+        else
+            dev::kv_scatter_kernel<false><<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
         if (cudaGetLastError() != cudaSuccess) return CA_ERR_CUDA;
         g_launches.fetch_add(1, std::memory_order_relaxed);
     }
@@ -992,11 +1101,11 @@ int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_ro
 }
 
 int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void* stream) {
-    void* fn = pick_kernel(p.cfg.chunk, p.cfg.head_dim);
+    void* fn = pick_kernel(p.cfg);
     if (!fn) return CA_ERR_UNSUPPORTED;
     int st;
     size_t bytes;
-    kernel_smem_bytes(p.cfg.chunk, p.cfg.head_dim, &st, &bytes);   // attribute set at pool creation
+    kernel_smem_bytes(p.cfg, &st, &bytes);   // attribute set at pool creation
     AttnParams a = prm;
     a.n_stages = st;
     const CUtensorMap* map = reinterpret_cast<const CUtensorMap*>(p.tmap);

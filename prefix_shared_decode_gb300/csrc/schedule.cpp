@@ -178,6 +178,7 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
 // ---------------------------------------------------------------------------
 namespace {
 constexpr double kCfComputePer16 = 0.2;
+constexpr double kF8CfFactor = 1.6;         // fp8 pools, fitted to measured per-tile times
 constexpr int32_t kMaxCfQueries = 64;
 // Share of the sequence-first tiles left to the tail queue that CTAs drain
 // dynamically once their static lists are done (absorbs the run-to-run rate
@@ -194,7 +195,14 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
     const int32_t HQ = p.cfg.n_heads, H = kv_heads(p.cfg), G = HQ / H;
     const int32_t D = p.cfg.head_dim, c = p.cfg.chunk, b = t.b;
     const double sf_cost = (G == 1) ? 1.0 : 1.0 + kCfComputePer16 * ((G + 15) / 16);
-    auto rows_cost = [&](int32_t m_rows) { return (1.0 + kCfComputePer16 * ((m_rows + 15) / 16)) / sf_cost; };
+    // An fp8 pool halves a tile's bytes, but the tensor-core phase widens each
+    // tile to fp16 in shared memory first, so there (and only there, when the
+    // sequence-first phase runs on CUDA cores) a chunk-first tile costs more
+    // relative to a sequence-first one.
+    const double cf_mult = ((p.cfg.flags & CA_KV_FP8) && G == 1) ? kF8CfFactor : 1.0;
+    auto rows_cost = [&](int32_t m_rows) {
+        return cf_mult * (1.0 + kCfComputePer16 * ((m_rows + 15) / 16)) / sf_cost;
+    };
     const int32_t R = (int32_t)(t.cf_rows.size() / 4), U = (int32_t)(t.cf_runs.size() / 4);
     plan.chunks.clear();
     plan.units.clear();

@@ -11,6 +11,7 @@ import pytest
 
 import workloads
 from oracle import attention as A
+from oracle import fp8 as F8
 from oracle.pakv import OracleTrie
 from oracle.schedule import build_schedule
 from tests.treegen import random_segment_sequences
@@ -38,7 +39,7 @@ def assert_close(got, want, what=""):
 def load(torch, wl, no_sharing=False, capacity=None):
     from prefix_shared_decode_gb300 import Pool
     pool = Pool(wl.n_layers, wl.n_heads, wl.head_dim, wl.chunk, capacity or capacity_for(wl),
-                no_sharing=no_sharing, n_kv_heads=wl.kv_heads)
+                no_sharing=no_sharing, n_kv_heads=wl.kv_heads, kv_dtype=wl.kv_dtype)
     staging = {}
     for sid in wl.seq_ids():
         insert_sequence(pool, wl, sid, staging=staging)
@@ -124,6 +125,85 @@ def test_grouped_query_attention_every_output(torch_cuda, G, Hkv, c, D):
     q = rng.standard_normal((11, Hkv * G, D), dtype=np.float32).astype(np.float16)
     got, _ = run(torch, pool, batch, q)
     assert_close(got, A.decode_attention(trie, batch, 0, q, 1 / np.sqrt(D)), f"G={G}")
+
+
+def _fp8_rows(rng, L, n, Hkv, D, scale):
+    """fp16 N(0, 1) rows, their E4M3 codes and the dequantised rows."""
+    x = rng.standard_normal((L, n, Hkv, D), dtype=np.float32).astype(np.float16)
+    return x, F8.dequantize(F8.quantize(x, scale), scale)
+
+
+def _check_fp8_bytes(pool, trie, k_scale, v_scale):
+    """Every live chunk's stored codes equal the oracle's quantisation of its
+    rows (scales are powers of two, so the dequantised rows divide back)."""
+    kv = pool.kv_view().cpu().numpy()
+    stack, n_checked = [trie.root], 0
+    while stack:
+        node = stack.pop()
+        stack.extend(node.children)
+        if node.slot < 0:
+            continue
+        t = node.ntok
+        for kvi, (rows, sc) in enumerate(((node.k, k_scale), (node.v, v_scale))):
+            want = F8.encode(np.transpose(rows / sc, (0, 2, 1, 3)))        # [L, H, t, D]
+            np.testing.assert_array_equal(kv[node.slot, :, kvi, :, :t, :], want,
+                                          err_msg=f"slot {node.slot} {'KV'[kvi]}")
+        n_checked += 1
+    assert n_checked > 0
+
+
+@pytest.mark.parametrize("c,G,k_scale,v_scale", [(16, 1, 1.0, 1.0), (32, 1, 0.5, 2.0), (64, 1, 1.0, 0.25),
+                                                 (64, 4, 2.0, 1.0), (32, 8, 1.0, 0.5)])
+def test_fp8_pool_bytes_and_every_output(torch_cuda, c, G, k_scale, v_scale):
+    """An FP8 pool: the stored codes match the oracle's E4M3 quantisation bit
+    for bit, and attention matches the definition over the dequantised K/V,
+    before and after decode-time appends (which quantise too)."""
+    from prefix_shared_decode_gb300 import Pool, decode_attention
+    torch = torch_cuda
+    Hkv, D, L = 2, 128, 2
+    rng = np.random.default_rng(60 + c + G)
+    seqs = random_segment_sequences(60 + c, 12, c, n_segments=10)
+    pool = Pool(L, Hkv * G, D, c, 700, n_kv_heads=Hkv, kv_dtype="fp8", k_scale=k_scale, v_scale=v_scale)
+    trie = OracleTrie(c, 700)
+    for i, toks in enumerate(seqs):
+        k16, kq = _fp8_rows(rng, L, len(toks), Hkv, D, k_scale)
+        v16, vq = _fp8_rows(rng, L, len(toks), Hkv, D, v_scale)
+        trie.insert(i, toks, kq, vq)
+        pool.insert(i, toks, torch.from_numpy(k16).cuda(), torch.from_numpy(v16).cuda())
+    torch.cuda.synchronize()
+    _check_fp8_bytes(pool, trie, k_scale, v_scale)
+    batch = [int(x) for x in rng.permutation(12)[:10]]
+    q = rng.standard_normal((10, Hkv * G, D), dtype=np.float32).astype(np.float16)
+    for layer in range(L):
+        want = A.decode_attention(trie, batch, layer, q, 1 / np.sqrt(D))
+        for no_tpp in (False, True):
+            got, _ = run(torch, pool, batch, q, layer=layer, no_tpp=no_tpp)
+            assert_close(got, want, f"fp8 c={c} G={G} layer={layer} no_tpp={no_tpp}")
+    for step, n_add in enumerate((1, c + 3)):            # fill in place, then grow chunks
+        for sid in batch:
+            toks = [10**6 + 1000 * step + sid * 50 + j for j in range(n_add)]
+            k16, kq = _fp8_rows(rng, L, n_add, Hkv, D, k_scale)
+            v16, vq = _fp8_rows(rng, L, n_add, Hkv, D, v_scale)
+            trie.append(sid, toks, kq, vq)
+            pool.append(sid, toks, torch.from_numpy(k16).cuda(), torch.from_numpy(v16).cuda())
+        sched = pool.schedule(batch)
+        got = decode_attention(pool, sched, torch.from_numpy(q).cuda(), layer=1).cpu().numpy()
+        assert sched.device_status() == 0
+        assert_close(got, A.decode_attention(trie, batch, 1, q, 1 / np.sqrt(D)), f"fp8 append {step}")
+    torch.cuda.synchronize()
+    _check_fp8_bytes(pool, trie, k_scale, v_scale)
+
+
+def test_fp8_pool_shape_limits(torch_cuda):
+    from prefix_shared_decode_gb300 import CAError, Pool
+    with pytest.raises(CAError) as e:
+        Pool(1, 2, 64, 16, 10, kv_dtype="fp8")            # fp8 needs head_dim 128
+    assert e.value.name == "CA_ERR_UNSUPPORTED"
+    with pytest.raises(CAError) as e:
+        Pool(1, 2, 128, 16, 10, kv_dtype="fp8", k_scale=-1.0)
+    assert e.value.name == "CA_ERR_INVALID"
+    p = Pool(1, 2, 128, 16, 10, kv_dtype="fp8")
+    assert p.kv_view().dtype == torch_cuda.uint8 and p.kv_bytes < Pool(1, 2, 128, 16, 10).kv_bytes
 
 
 def test_edge_cases(torch_cuda):
@@ -344,7 +424,8 @@ SAMPLE = 4
 
 
 @pytest.mark.parametrize("name", ["llama7b_p1024", "sweep_s2048_b32", "sweep_s2048_b64",
-                                  "sweep_s4096_b32", "sweep_s4096_b64", "no_sharing", "gqa_p1024"])
+                                  "sweep_s4096_b32", "sweep_s4096_b64", "no_sharing", "gqa_p1024",
+                                  "llama7b_p1024_fp8", "sweep_s4096_b64_fp8"])
 def test_full_size_workloads_sampled(torch_cuda, name):
     """The benchmark's launch configuration at full size; every output is
     finite and SAMPLE sequences (all heads) match the oracle."""
@@ -357,6 +438,8 @@ def test_full_size_workloads_sampled(torch_cuda, name):
     rng = np.random.default_rng(0)
     for i in sorted(rng.choice(len(batch), size=SAMPLE, replace=False)):
         k, v = wl.kv_rows(batch[i])
+        if wl.kv_dtype == "fp8":                         # the dequantised rows (scales 1)
+            k, v = F8.dequantize(F8.quantize(k, 1.0), 1.0), F8.dequantize(F8.quantize(v, 1.0), 1.0)
         want = A.softmax_attention(q[i], k[0], v[0], wl.scale)
         assert_close(got[i], want, f"{name} seq {batch[i]}")
 

@@ -61,6 +61,7 @@ class Workload:
     chunk: int
     seed: int
     n_kv_heads: int = 0            # key/value heads (0: one per query head)
+    kv_dtype: str = "fp16"         # pool storage: "fp16", or "fp8" (E4M3, scales 1)
     seg_len: dict[int, int] = field(default_factory=dict)
     seqs: dict[int, list[int]] = field(default_factory=dict)  # seq_id -> segment ids
     churn: int = 0  # sequences removed and inserted per step (multi-tenant tree)
@@ -193,7 +194,15 @@ def make(name: str) -> Workload:
     multi_tenant    the multi-tenant tree with churn; seed 7.
     gqa_p1024       llama7b_p1024's tree with grouped-query attention: 32 query
                     heads over 8 key/value heads; seed 8.
+    llama7b_p1024_fp8, sweep_s4096_b64_fp8
+                    those trees (same seeds) in a pool that stores K/V as FP8
+                    E4M3 with scales 1 (the inputs stay fp16 N(0, 1)).
     """
+    if name.endswith("_fp8"):
+        w = make(name[:-4])
+        w.name, w.kv_dtype = name, "fp8"
+        w.description += "; K/V stored as FP8 E4M3 (scales 1)"
+        return w
     if name == "tiny":
         return _shared_prefix(name, 0, 4, 64, 16, n_heads=2, head_dim=64, chunk=16,
                               description="2 heads, D 64, chunk 16; 64-token prefix + 4 x 16 private")
@@ -220,4 +229,5 @@ def make(name: str) -> Workload:
 
 
 ALL = ["tiny", "llama7b_p1024", "sweep_s2048_b32", "sweep_s2048_b64",
-       "sweep_s4096_b32", "sweep_s4096_b64", "no_sharing", "multi_tenant", "gqa_p1024"]
+       "sweep_s4096_b32", "sweep_s4096_b64", "no_sharing", "multi_tenant", "gqa_p1024",
+       "llama7b_p1024_fp8", "sweep_s4096_b64_fp8"]
