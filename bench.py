@@ -416,8 +416,8 @@ def run_ours(args):
         "effective_hbm_gbs": round(alg_bytes / (us * 1e-6) / 1e9, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
-                     "traffic": kernel_traffic(f"two_phase_attention_kernel<{c},{D}>:{wl.name}"),
-                     "kernel": f"two_phase_attention_kernel<{c},{D}>",
+                     "traffic": kernel_traffic(f"two_phase_attention_kernel<{c},{D},{eb}>:{wl.name}"),
+                     "kernel": f"two_phase_attention_kernel<{c},{D},{eb}>",
                      "kernel_us": round(kern_ms_avg * 1e3, 3),
                      "kernel_timing": f"CUDA events around the main kernel on {len(kev)} of the {K} timed steps",
                      "algorithmic_bytes": alg_bytes},

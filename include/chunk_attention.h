@@ -70,7 +70,7 @@ extern "C" {
  * code * scale exactly.  Attention is then the plain definition over those
  * dequantised keys and values.  Needs head_dim 128.  The pages' own kernels
  * keep fp16; this is one of the variants their tuning discussion leaves open
- * [CA §4.1 on other model configurations]. */
+ * [CA §7, Model and Hardware Compatibility]. */
 #define CA_KV_FP8            2u
 
 /* ---- schedule flags ---------------------------------------------------- */
