@@ -75,7 +75,10 @@ def cpu_baseline(wl, seconds: float = CPU_SAMPLE_SECONDS) -> dict:
     while time.perf_counter() - t_start < seconds or done == 0:
         i = done % len(batch)
         t0 = time.perf_counter()
-        A.decode_attention(trie, [batch[i]], 0, q[i:i + 1], wl.scale)
+        if wl.q_len == 1:
+            A.decode_attention(trie, [batch[i]], 0, q[i:i + 1], wl.scale)
+        else:
+            A.decode_attention_multi(trie, [batch[i]], 0, q[i:i + 1], wl.scale, causal=True)
         times.append(time.perf_counter() - t0)
         done += 1
     per_seq = sum(times) / len(times)
@@ -222,7 +225,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     setup_s = time.perf_counter() - t0
 
-    scheds = [p.schedule(batch) for p in pools]
+    skw = {"q_len": wl.q_len, "causal": wl.q_len > 1}        # several query tokens: causal
+    scheds = [p.schedule(batch, **skw) for p in pools]
     sched = scheds[0]
     # Workspace with headroom so a schedule rebuilt after churn fits without
     # allocating inside the timed steps (grown, zero-filled, only if needed).
@@ -264,7 +268,7 @@ def run_ours(args):
             pool.insert_batch(inserted, toks, *kv_views[i], lengths=lens, stream=stream)
             t2 = time.perf_counter()
             batch = live
-        sched = scheds[r] = pool.schedule(batch, reuse=sched, stream=stream)
+        sched = scheds[r] = pool.schedule(batch, reuse=sched, stream=stream, **skw)
         if churn:
             t3 = time.perf_counter()
             host_split["remove"].append((t1 - th) * 1e6)
@@ -340,7 +344,7 @@ def run_ours(args):
     for i in range(Ke):
         r = i % n_copies
         eev[i][0].record(stream)
-        scheds[r] = pools[r].schedule(batch, reuse=scheds[r], stream=stream)
+        scheds[r] = pools[r].schedule(batch, reuse=scheds[r], stream=stream, **skw)
         decode_attention_host(pools[r], scheds[r], qh[i % 4], oh, scale=wl.scale, workspace=wshs[r],
                               stream=stream)
         eev[i][1].record(stream)
@@ -365,12 +369,12 @@ def run_ours(args):
             e1.record(stream)
             torch.cuda.synchronize()
             return e0.elapsed_time(e1) / n * 1e3
-        no_tpp = [p_.schedule(batch, no_tpp=True) for p_ in pools]
+        no_tpp = [p_.schedule(batch, no_tpp=True, **skw) for p_ in pools]
         us_no_tpp = time_calls(pools, no_tpp)
         del no_tpp
         flat_bytes = sum(wl.seq_len(sid) for sid in batch) * HK * D * 2 * eb
         flats = make_pools(copies_for(flat_bytes), no_sharing=True, headroom=1.05)
-        us_flat = time_calls(flats, [f.schedule(batch) for f in flats])
+        us_flat = time_calls(flats, [f.schedule(batch, **skw) for f in flats])
         del flats
         torch.cuda.empty_cache()
         context = {"paged_flat_us": round(us_flat, 2), "paged_shared_no_tpp_us": round(us_no_tpp, 2),
@@ -383,7 +387,7 @@ def run_ours(args):
         return
 
     unique_tokens = wl.unique_tokens()
-    io_bytes = 2 * b * H * D * 2                               # q in, out
+    io_bytes = 2 * b * wl.q_len * H * D * 2                    # q in, out
     alg_bytes = kv_bytes + io_bytes
     us = ms_per_step * 1e3
     peak, peak_kind = measured_peak()
@@ -402,7 +406,8 @@ def run_ours(args):
         "dtype": ("f16 q/out, fp8 e4m3 K/V storage (fp32 accumulate)" if wl.kv_dtype == "fp8"
                   else "f16 (fp32 accumulate)"),
         "data": "synthetic (seeded N(0,1) fp16 Q/K/V; token segments shaped like the pages' shared system prompts)",
-        "config": {"workload": wl.name, "description": wl.description, "batch": b, "n_heads": H,
+        "config": {"workload": wl.name, "description": wl.description, "batch": b, "q_len": wl.q_len,
+                   "n_heads": H,
                    "n_kv_heads": HK,
                    "head_dim": D, "chunk": c, "layers_per_call": 1,
                    "unique_kv_tokens": unique_tokens, "unique_kv_bytes": kv_bytes,
@@ -421,8 +426,8 @@ def run_ours(args):
                      "kernel_us": round(kern_ms_avg * 1e3, 3),
                      "kernel_timing": f"CUDA events around the main kernel on {len(kev)} of the {K} timed steps",
                      "algorithmic_bytes": alg_bytes},
-        "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": b * H * D * 2,
-                "d2h_bytes_per_step": b * H * D * 2,
+        "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": b * wl.q_len * H * D * 2,
+                "d2h_bytes_per_step": b * wl.q_len * H * D * 2,
                 "path": "ca_decode_attention_host: pinned host q -> device, kernel, device -> host out"},
         "gpu_launches": launches,
         "gpu_launches_source": "library launch counter (ca_kernel_launches) read around the timed loop",

@@ -79,6 +79,9 @@ extern "C" {
  * the pages' PagedAttn* comparator: physically shared KV without TPP
  * [CA §4.1, Table 3]. */
 #define CA_SCHED_NO_TPP      1u
+/* Multi-token queries (ca_build_schedule_ex): query token j of a sequence
+ * whose context holds n tokens sees only tokens [0, n - q_len + j]. */
+#define CA_SCHED_CAUSAL      2u
 
 typedef struct ca_pool  ca_pool;
 typedef struct ca_sched ca_sched;
@@ -215,6 +218,22 @@ int ca_seq_slots(const ca_pool* pool, int64_t seq_id, int32_t* slots, int32_t ca
  * ids), CA_ERR_CUDA. */
 int ca_build_schedule(ca_pool* pool, const int64_t* seq_ids, int32_t b,
                       uint32_t flags, ca_sched** inout, void* stream);
+
+/* The same for q_len query tokens per sequence (multi-token queries: draft
+ * tokens to verify, or a chunk of prompt prefilled over the trie).  The
+ * blog's two-phase function takes queries of any length [CA-blog, Two-Phase
+ * Partition: queries (batch, heads, seq_len, d_k)] and lets every query
+ * token attend to the sequence's whole context; that is the default here.
+ * With CA_SCHED_CAUSAL, query token j of a sequence whose context holds n
+ * tokens attends to tokens [0, n - q_len + j] only — the form for tokens
+ * whose own K/V the caller has already appended.  q and out of the decode
+ * calls are then [b][q_len][n_heads][head_dim] (row i*q_len + j is token j
+ * of seq_ids[i]).  q_len = 1 is ca_build_schedule.  Requires
+ * q_len * (n_heads / n_kv_heads) <= 64 (CA_ERR_UNSUPPORTED otherwise) and,
+ * with CA_SCHED_CAUSAL, every context at least q_len tokens long
+ * (CA_ERR_INVALID otherwise); other errors as ca_build_schedule. */
+int ca_build_schedule_ex(ca_pool* pool, const int64_t* seq_ids, int32_t b, int32_t q_len,
+                         uint32_t flags, ca_sched** inout, void* stream);
 int ca_sched_destroy(ca_sched* sched);
 
 /* Table sizes, then the tables themselves (host copies; for bit-exact tests).
@@ -232,7 +251,7 @@ int ca_export_tables(const ca_sched* sched, int32_t* seq_perm, int32_t* cf_rows,
                      int32_t* merge_offsets, int32_t* merge_runs);
 
 /* The kernel work plan derived from the tables (inspection and tests).
- * counts[0..3] = n_units, grid (CTAs), n_pbase (= b * n_heads + 1),
+ * counts[0..3] = n_units, grid (CTAs), n_pbase (= b * q_len * n_heads + 1),
  * n_chunks.  Any array may be NULL.  Layouts (int32):
  *   units[n_units][12] (kind, head, pos_lo, pos_hi, begin, end, part, qrow,
  *                       n_per_head, base, part_next, 0).  Chunk-first (kind 0):
@@ -246,8 +265,8 @@ int ca_export_tables(const ca_sched* sched, int32_t* seq_perm, int32_t* cf_rows,
  *   cta_begin[grid+1]  static unit range of each CTA; units from
  *                      cta_begin[grid] to n_units form the tail queue that
  *                      CTAs drain dynamically after their static ranges
- *   pbase[n_pbase]     partial ids of (position p, head h) are
- *                      [pbase[p*H+h], pbase[p*H+h+1])
+ *   pbase[n_pbase]     partial ids of (position p, query token j, head h)
+ *                      are [pbase[i], pbase[i+1]) with i = (p*q_len+j)*H+h
  *   chunks[n_chunks][2] (slot, ntok) list the units index into */
 int ca_export_plan(const ca_sched* sched, int32_t counts[4], int32_t* units,
                    int32_t* cta_begin, int32_t* pbase, int32_t* chunks);
@@ -261,7 +280,9 @@ int ca_workspace_bytes(const ca_sched* sched, size_t* bytes_out);
  * t of sequence seq_ids[i]'s context, computed by the two-phase partition
  * [CA §3.2; CA-blog, Two-Phase Partition].
  *   q_dev    fp16 [b][n_heads][head_dim], row i = seq_ids[i] of the schedule
- *   out_dev  fp16 [b][n_heads][head_dim], written
+ *            ([b][q_len][n_heads][head_dim] for a ca_build_schedule_ex
+ *            schedule, masked as that call says)
+ *   out_dev  same shape as q, written
  *   layer    0 <= layer < n_layers
  *   ws_dev   >= ca_workspace_bytes(sched) bytes, 256-byte aligned, caller
  *            owned; its contents need no initialisation.  Calls sharing one

@@ -77,6 +77,30 @@ def decode_attention(trie: OracleTrie, seq_ids, layer: int, q: np.ndarray,
     return out
 
 
+def decode_attention_multi(trie: OracleTrie, seq_ids, layer: int, q: np.ndarray, scale: float,
+                           causal: bool = False) -> np.ndarray:
+    """Several query tokens per sequence: q [b, q_len, H, D] -> [b, q_len, H, D].
+
+    The blog's two-phase function takes queries of any length and lets every
+    query token attend to the whole prefix and suffix [CA-blog, Two-Phase
+    Partition]; that is the default.  Reading R16 (causal): when the query
+    tokens are the last q_len tokens of the context (their K/V appended
+    first), token j of a sequence with n context tokens attends to its first
+    n - q_len + j + 1 tokens."""
+    q = np.asarray(q, dtype=np.float64)
+    b, q_len = q.shape[:2]
+    out = np.empty(q.shape, dtype=np.float64)
+    for i, s in enumerate(seq_ids):
+        k, v = trie.materialize(int(s), layer)
+        n = k.shape[0]
+        for j in range(q_len):
+            lim = n - q_len + j + 1 if causal else n
+            if lim < 1:
+                raise OracleError("invalid", "causal context shorter than the query tokens")
+            out[i, j] = softmax_attention(q[i, j], k[:lim], v[:lim], scale)
+    return out
+
+
 def partial(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float):
     """The partial-result triple of one query per head over a token set.
 

@@ -191,18 +191,23 @@ class Pool:
         return list(buf)[:n.value]
 
     def schedule(self, seq_ids, no_tpp: bool = False, reuse: "Schedule | None" = None,
-                 stream=None) -> "Schedule":
+                 stream=None, q_len: int = 1, causal: bool = False) -> "Schedule":
         """Per-step tables for the batch ``seq_ids`` (rows of q / out in that
-        order).  Passing the previous schedule reuses it when nothing changed."""
+        order).  Passing the previous schedule reuses it when nothing changed.
+        ``q_len`` > 1: that many query tokens per sequence (q / out become
+        [b, q_len, H, D]); ``causal``: token j sees context tokens
+        [0, len - q_len + j] only."""
         ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
         s = reuse if reuse is not None else Schedule(self)
         h = s._h if s._h is not None else C.c_void_p()
-        check(capi.lib().ca_build_schedule(self._h, ids.ctypes.data_as(C.POINTER(C.c_int64)), len(ids),
-                                           capi.CA_SCHED_NO_TPP if no_tpp else 0, C.byref(h),
-                                           None if self.host_only else _stream_ptr(stream)),
-              "ca_build_schedule")
+        flags = (capi.CA_SCHED_NO_TPP if no_tpp else 0) | (capi.CA_SCHED_CAUSAL if causal else 0)
+        check(capi.lib().ca_build_schedule_ex(self._h, ids.ctypes.data_as(C.POINTER(C.c_int64)), len(ids),
+                                              int(q_len), flags, C.byref(h),
+                                              None if self.host_only else _stream_ptr(stream)),
+              "ca_build_schedule_ex")
         s._h = h
         s.b = len(ids)
+        s.q_len = int(q_len)
         return s
 
 
@@ -213,6 +218,7 @@ class Schedule:
         self.pool = pool
         self._h = None
         self.b = 0
+        self.q_len = 1
         self._ws = None
 
     def __del__(self):
@@ -286,10 +292,13 @@ class Schedule:
 def decode_attention(pool: Pool, sched: Schedule, q, out=None, layer: int = 0, scale: float | None = None,
                      workspace=None, stream=None):
     """out[i, h] = softmax(scale q[i, h] . K^T) V over sequence seq_ids[i]'s
-    context, via the two-phase kernel.  q: fp16 [b, H, D] on the GPU."""
+    context, via the two-phase kernel.  q: fp16 [b, H, D] on the GPU
+    ([b, q_len, H, D] for a multi-token schedule)."""
     import torch
     assert q.dtype == torch.float16 and q.is_contiguous()
-    assert tuple(q.shape) == (sched.b, pool.n_heads, pool.head_dim)
+    want = ((sched.b, pool.n_heads, pool.head_dim) if sched.q_len == 1
+            else (sched.b, sched.q_len, pool.n_heads, pool.head_dim))
+    assert tuple(q.shape) == want, (tuple(q.shape), want)
     if out is None:
         out = torch.empty_like(q)
     if scale is None:

@@ -20,11 +20,12 @@ CA_STATIC_WS_BYTES = 16 << 20
 CA_NO_SHARING = 1
 CA_KV_FP8 = 2
 CA_SCHED_NO_TPP = 1
+CA_SCHED_CAUSAL = 2
 
 # Every symbol the header declares, in header order.
 EXPORTS = [
     "ca_pool_bytes", "ca_pool_create", "ca_pool_destroy", "ca_match_prefix", "ca_insert_tokens",
-    "ca_insert_batch", "ca_append_tokens", "ca_remove_seq", "ca_remove_batch", "ca_pool_stats", "ca_seq_slots", "ca_build_schedule", "ca_sched_destroy",
+    "ca_insert_batch", "ca_append_tokens", "ca_remove_seq", "ca_remove_batch", "ca_pool_stats", "ca_seq_slots", "ca_build_schedule", "ca_build_schedule_ex", "ca_sched_destroy",
     "ca_sched_counts", "ca_export_tables", "ca_export_plan", "ca_workspace_bytes", "ca_decode_attention",
     "ca_workspace_bytes_host", "ca_decode_attention_host", "ca_decode_attention_static_ws",
     "ca_sched_device_status",
@@ -78,6 +79,7 @@ def lib() -> C.CDLL:
         "ca_pool_stats": [vp, P(Stats)],
         "ca_seq_slots": [vp, i64, P(i32), i32, P(i32)],
         "ca_build_schedule": [vp, P(i64), i32, u32, P(vp), vp],
+        "ca_build_schedule_ex": [vp, P(i64), i32, i32, u32, P(vp), vp],
         "ca_sched_destroy": [vp],
         "ca_sched_counts": [vp, P(i32)],
         "ca_export_tables": [vp] + [P(i32)] * 7,

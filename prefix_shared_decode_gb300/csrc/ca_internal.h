@@ -57,7 +57,7 @@ constexpr int kUnitInts = (int)(sizeof(Unit) / sizeof(int32_t));
 
 // Offsets (in bytes) of the arrays inside the device plan blob.
 struct PlanLayout {
-    size_t chunks, units, cta_begin, seq_perm, pbase, status, counter, total;
+    size_t chunks, units, cta_begin, seq_perm, pbase, status, counter, chunk_tok0, ctx_len, total;
 };
 
 // Parameters of the attention kernel (passed by value).
@@ -77,6 +77,9 @@ struct AttnParams {
     float2* part_ms;             // [P] (running max in log2 units, sum of exp2)
     int32_t n_layers, n_heads, layer, capacity;   // n_heads: query heads
     int32_t n_kv_heads, group;                     // key/value heads, n_heads / n_kv_heads
+    int32_t q_len, causal;                         // query tokens per position; causal mask
+    const int32_t* chunk_tok0;   // [chunks] first token's offset in the context
+    const int32_t* ctx_len;      // [b] context tokens of each position
     float scale_log2;            // scale * log2(e) (times the key scale of an fp8 pool)
     float out_scale;             // value scale of an fp8 pool, else 1
     int32_t n_stages;
@@ -135,10 +138,15 @@ struct Tables {
     int32_t b = 0;
     std::vector<int32_t> seq_perm, cf_rows, cf_runs, sf_offsets, sf_chunks,
         merge_offsets, merge_runs;
+    // token offset of each chunk in its sequences' contexts (cf rows, then sf
+    // chunks) and each position's context length: the causal mask's inputs
+    std::vector<int32_t> row_tok0, sf_tok0, ctx_len;
 };
 
 struct Plan {
     std::vector<ChunkRef> chunks;
+    std::vector<int32_t> chunk_tok0;   // parallel to chunks: first token's context offset
+    int32_t q_len = 1;                 // query tokens per position
     std::vector<Unit> units;       // per-CTA static lists, then the tail queue
     std::vector<int32_t> cta_begin;  // [grid + 1]; cta_begin[grid] = first queue unit
     std::vector<int32_t> pbase;
@@ -154,6 +162,7 @@ struct Sched {
     const Pool* pool = nullptr;
     int64_t generation = -1;
     uint32_t flags = 0;
+    int32_t q_len = 1;
     std::vector<int64_t> seq_ids;
     Tables t;
     Tables t_next;                     // rebuilt into, then swapped with t
@@ -216,7 +225,7 @@ int32_t pool_match(const Pool& p, const int32_t* tokens, int32_t n);
 
 // schedule.cpp
 int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flags, Tables& t);
-void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan);
+void build_plan(const Pool& p, const Tables& t, int32_t grid, int32_t q_len, Plan& plan);
 void layout_plan(const Plan& plan, int32_t b, PlanLayout& lay, std::vector<unsigned char>& blob,
                  const Tables& t);
 void layout_ws(const Plan& plan, const Pool& p, int32_t b, WsLayout& ws);

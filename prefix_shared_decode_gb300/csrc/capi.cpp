@@ -245,12 +245,27 @@ int ca_seq_slots(const ca_pool* pool, int64_t seq_id, int32_t* slots, int32_t ca
 
 int ca_build_schedule(ca_pool* pool, const int64_t* seq_ids, int32_t b, uint32_t flags,
                       ca_sched** inout, void* stream) {
-    if (!pool || !inout || !seq_ids || b < 1 || (flags & ~CA_SCHED_NO_TPP)) return CA_ERR_INVALID;
+    if (flags & ~CA_SCHED_NO_TPP) return CA_ERR_INVALID;
+    return ca_build_schedule_ex(pool, seq_ids, b, 1, flags, inout, stream);
+}
+
+int ca_build_schedule_ex(ca_pool* pool, const int64_t* seq_ids, int32_t b, int32_t q_len, uint32_t flags,
+                         ca_sched** inout, void* stream) {
+    if (!pool || !inout || !seq_ids || b < 1 || q_len < 1 || (flags & ~(CA_SCHED_NO_TPP | CA_SCHED_CAUSAL)))
+        return CA_ERR_INVALID;
+    if ((int64_t)q_len * (pool->cfg.n_heads / kv_heads(pool->cfg)) > 64) return CA_ERR_UNSUPPORTED;
+    if (q_len == 1) flags &= ~CA_SCHED_CAUSAL;       // one query token sees its whole context
     return guard([&] {
         ca_sched* s = *inout;
         if (s && s->pool == pool && s->generation == pool->generation && s->flags == flags &&
-            (int32_t)s->seq_ids.size() == b && std::equal(seq_ids, seq_ids + b, s->seq_ids.begin()))
+            s->q_len == q_len && (int32_t)s->seq_ids.size() == b &&
+            std::equal(seq_ids, seq_ids + b, s->seq_ids.begin()))
             return CA_OK;                   // context unchanged since the tree last changed
+        if (flags & CA_SCHED_CAUSAL)
+            for (int32_t i = 0; i < b; ++i) {
+                auto it = pool->seqs.find(seq_ids[i]);
+                if (it != pool->seqs.end() && it->second.length < q_len) return CA_ERR_INVALID;
+            }
         std::unique_ptr<ca_sched> fresh;
         if (!s) {
             fresh.reset(new ca_sched());
@@ -261,8 +276,9 @@ int ca_build_schedule(ca_pool* pool, const int64_t* seq_ids, int32_t b, uint32_t
         std::swap(s->t, s->t_next);
         s->pool = pool;
         s->flags = flags;
+        s->q_len = q_len;
         s->seq_ids.assign(seq_ids, seq_ids + b);
-        build_plan(*pool, s->t, pool->kv ? pool->num_sms : kHostOnlyGrid, s->plan);
+        build_plan(*pool, s->t, pool->kv ? pool->num_sms : kHostOnlyGrid, q_len, s->plan);
         layout_plan(s->plan, b, s->layout, s->blob, s->t);
         layout_ws(s->plan, *pool, b, s->ws);
         if (pool->kv) {
@@ -386,6 +402,10 @@ AttnParams attn_params(const Pool& pool, const Sched& s, int32_t layer, const vo
                                                    pool_tile_bytes(pool.cfg));
     a.status = reinterpret_cast<int32_t*>(dev + s.layout.status);
     a.dyn_counter = reinterpret_cast<int32_t*>(dev + s.layout.counter);
+    a.chunk_tok0 = reinterpret_cast<const int32_t*>(dev + s.layout.chunk_tok0);
+    a.ctx_len = reinterpret_cast<const int32_t*>(dev + s.layout.ctx_len);
+    a.q_len = s.q_len;
+    a.causal = (s.flags & CA_SCHED_CAUSAL) ? 1 : 0;
     a.dyn_begin = s.plan.cta_begin[s.plan.grid];
     a.dyn_end = (int32_t)s.plan.units.size();
     a.q = static_cast<const uint16_t*>(q);
@@ -427,7 +447,7 @@ int ca_decode_attention_host(const ca_pool* pool, const ca_sched* s, int32_t lay
     int st = decode_checks(pool, s, layer, ws_dev, ws_bytes, s ? s->ws.total_host : 0);
     if (st) return st;
     if (!q_host || !out_host) return CA_ERR_INVALID;
-    const size_t bytes = (size_t)s->t.b * pool->cfg.n_heads * pool->cfg.head_dim * 2;
+    const size_t bytes = (size_t)s->t.b * s->q_len * pool->cfg.n_heads * pool->cfg.head_dim * 2;
     unsigned char* ws = static_cast<unsigned char*>(ws_dev);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (cudaMemcpyAsync(ws + s->ws.q_stage, q_host, bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess)

@@ -29,6 +29,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <atomic>
 #include <cstdio>
 #include <cstring>
@@ -188,7 +189,9 @@ __global__ void __launch_bounds__(128) merge_partials_kernel(const AttnParams p,
     if (gw < n_pairs) {
         a = p.pbase[gw];
         n = p.pbase[gw + 1] - a;
-        row = p.seq_perm[gw / p.n_heads];
+        // pair gw = (position, query token, head); out row = that position's
+        // row of q times q_len plus the token
+        row = p.seq_perm[gw / (p.q_len * p.n_heads)] * p.q_len + (gw / p.n_heads) % p.q_len;
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (blockIdx.x == 0 && threadIdx.x == 0) *p.dyn_counter = 0;   // the main grid is done with it
@@ -345,7 +348,8 @@ __device__ __forceinline__ void sf_chunk(const uint8_t* kt, const uint8_t* vt, i
 // g = lane/4 and g + 8 of the block.
 // ---------------------------------------------------------------------------
 template <int C, int D, int NT>
-__device__ __forceinline__ void cf_chunk(uint32_t kt, uint32_t vt, int ntok, int tok0,
+__device__ __forceinline__ void cf_chunk(uint32_t kt, uint32_t vt, int ntok, int tok0, int ctx0, int lim0,
+                                         int lim1,
                                          uint32_t qrow_addr_base, float scale_log2,
                                          float (&m)[2], float (&s)[2], float (&o)[D / 8][4],
                                          int lane) {
@@ -379,7 +383,10 @@ __device__ __forceinline__ void cf_chunk(uint32_t kt, uint32_t vt, int ntok, int
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int col = tok0 + nt * 8 + 2 * (lane & 3) + (e & 1);
-            const float x = (col < ntok) ? sacc[nt][e] * scale_log2 : -INFINITY;
+            // a column counts if it holds a token and, under the causal
+            // mask, that token is at or before the row's limit
+            const bool ok = col < ntok && ctx0 + col <= ((e >> 1) ? lim1 : lim0);
+            const float x = ok ? sacc[nt][e] * scale_log2 : -INFINITY;
             sacc[nt][e] = x;
             mx[e >> 1] = fmaxf(mx[e >> 1], x);
         }
@@ -456,7 +463,7 @@ struct Smem {
     static constexpr int kQBytes = kQRows * D * 2;
     static constexpr int kXmsBytes = 512;
     static constexpr int kBarBytes = 2 * kMaxStages * 8;
-    static constexpr int kRingBytes = kRing * 4 + kMaxStages * 4;
+    static constexpr int kRingBytes = kRing * 4 + 2 * kMaxStages * 4;   // ids, then ntok and tok0 per stage
     static size_t bytes(int stages) {
         return (size_t)stages * kStage + kConvBytes + kQBytes + kXmsBytes + kBarBytes + kRingBytes;
     }
@@ -480,6 +487,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xms) + SM::kXmsBytes);
     volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(bars + 2 * kMaxStages);
     volatile int32_t* stage_ntok = ring + kRing;          // valid tokens of each stage's chunk
+    volatile int32_t* stage_tok0 = stage_ntok + kMaxStages;   // its first token's context offset
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -503,6 +511,8 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
     const int H = p.n_heads;            // query heads (q, out, partials)
     const int HK = p.n_kv_heads;        // key/value heads (pool tiles, units)
     const int G = p.group;              // query heads per key/value head
+    const int QL = p.q_len;             // query tokens per position
+    const int RW = QL * G;              // query rows per position and key/value head
 
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
@@ -538,12 +548,15 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
         int cur = (u_begin < u_end) ? s_next++ : -1;
         Unit Un = (cur >= 0) ? p.units[cur] : Unit{};
         ChunkRef chn = (cur >= 0) ? p.chunks[first_chunk(Un)] : ChunkRef{0, 0};
+        // context offsets matter only under the causal mask
+        int tkn = (cur >= 0 && p.causal) ? p.chunk_tok0[first_chunk(Un)] : 0;
         asm volatile("griddepcontrol.wait;" ::: "memory");
         if (cur < 0) {
             cur = claim();
             if (cur >= 0) {
                 Un = p.units[cur];
                 chn = p.chunks[first_chunk(Un)];
+                if (p.causal) tkn = p.chunk_tok0[first_chunk(Un)];
             }
         }
         int seq = 0;
@@ -568,6 +581,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     have_next = true;
                 }
                 const ChunkRef ch = chn;
+                const int tok0 = tkn;
                 // the chunk's token count comes from the pool's device table
                 // (appends grow partial chunks in place); the load is in
                 // flight while the producer waits for the stage
@@ -575,8 +589,13 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 const int ntok = slot_ok ? p.slot_ntok[ch.slot] : 0;
                 const int head = h;
                 if (++j == n) { j = 0; ++h; }
-                if (L + 1 < L1) chn = p.chunks[base + j];
-                else if (nxt >= 0) chn = p.chunks[first_chunk(Un)];
+                if (L + 1 < L1) {
+                    chn = p.chunks[base + j];
+                    if (p.causal) tkn = p.chunk_tok0[base + j];
+                } else if (nxt >= 0) {
+                    chn = p.chunks[first_chunk(Un)];
+                    if (p.causal) tkn = p.chunk_tok0[first_chunk(Un)];
+                }
                 const int st = it % S;
                 const uint32_t ph = (uint32_t)(it / S) & 1u;
                 if (!mbar_wait(empty0 + 8 * st, ph ^ 1u)) {
@@ -604,6 +623,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     tma_load_2d(dst + SM::kTile + bx * C * 128, &tmap, bx * (128 / EB), rowV, fb, pol);
                 }
                 stage_ntok[st] = min(max(ntok, 0), C);
+                stage_tok0[st] = tok0;
                 mbar_arrive(fb);
             }
             if (!have_next) {                 // left early on a timeout
@@ -681,7 +701,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
         const int32_t d0 = dn;
         const bool next_sf = next_static && fld(d0, F_KIND) == UNIT_SF;
         consumer_sync();   // previous unit (and its exchange reads) finished
-        if (fld(dc, F_KIND) == UNIT_SF && G == 1) {
+        if (fld(dc, F_KIND) == UNIT_SF && G == 1 && QL == 1) {
             const int pos = fld(dc, F_QLO), n = fld(dc, F_N), base = fld(dc, F_BASE);
             const int qrow = fld(dc, F_QROW), c_end = fld(dc, F_CE), part_next = fld(dc, F_PNEXT);
             int L = fld(dc, F_CB), h = fld(dc, F_HEAD), part = fld(dc, F_PART);
@@ -752,11 +772,13 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
             }
         } else {
             // ------------------------- tensor-core path -------------------------
-            // Chunk-first units, and sequence-first units when several query
-            // heads share a key/value head (G > 1).  Rows of the query tile are
-            // (position, query head) pairs: row r is position q_lo + r / G,
-            // query head kvh * G + r % G.  The unit is walked as its linear
-            // (key/value head, chunk) range, one head's piece at a time.
+            // Chunk-first units, and sequence-first units when a position has
+            // several query rows per key/value head (grouped query heads or
+            // several query tokens).  Rows of the query tile are (position,
+            // query token, query head): row r is position q_lo + r / RW, token
+            // (r % RW) / G, query head kvh * G + r % G.  The unit is walked as
+            // its linear (key/value head, chunk) range, one head's piece at a
+            // time.
             const bool is_sf = fld(dc, F_KIND) == UNIT_SF;
             const int q_lo = fld(dc, F_QLO), q_hi = fld(dc, F_QHI);
             const int cb = fld(dc, F_CB), ce = fld(dc, F_CE);
@@ -766,12 +788,23 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
             const int L_end = is_sf ? ce : (fld(dc, F_HEAD) + fld(dc, F_N)) * n;
             const int part_first = fld(dc, F_PART), part_rest = is_sf ? fld(dc, F_PNEXT) : part_first;
             if (next_sf) prefetch_q(fld(d0, F_QROW), fld(d0, F_HEAD));
-            const int m_rows = (q_hi - q_lo) * G;
+            const int m_rows = (q_hi - q_lo) * RW;
             const int rblocks = m_rows <= 16 ? 1 : m_rows <= 32 ? 2 : 4;
             int T = kConsumerWarps / rblocks;   // warps splitting a chunk's tokens
             if (T * 16 > C) T = C / 16;
             const int rb = w / T, tp = w % T;
             const bool active = rb < rblocks && rb * 16 < m_rows;
+            // Causal mask: the last context token each of this thread's two
+            // rows (rb*16 + lane/4 and 8 below) may see; the rows are the same
+            // for every head of the unit.
+            int lim[2] = {INT_MAX, INT_MAX};
+            if (p.causal) {
+#pragma unroll
+                for (int r2 = 0; r2 < 2; ++r2) {
+                    const int row = rb * 16 + (lane >> 2) + 8 * r2;
+                    if (row < m_rows) lim[r2] = p.ctx_len[q_lo + row / RW] - QL + (row % RW) / G;
+                }
+            }
             for (bool first = true; L < L_end; first = false) {
                 const int kvh = L / n;
                 const int seg_end = min(L_end, (kvh + 1) * n);
@@ -783,8 +816,8 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 // rows are never written out.
                 for (int idx = threadIdx.x; idx < m_rows * (D / 8); idx += kConsumerWarps * 32) {
                     const int r = idx / (D / 8), k = idx % (D / 8);
-                    const uint16_t* src =
-                        p.q + ((size_t)p.seq_perm[q_lo + r / G] * H + kvh * G + r % G) * D + k * 8;
+                    const size_t qrow_tok = (size_t)p.seq_perm[q_lo + r / RW] * QL + (r % RW) / G;
+                    const uint16_t* src = p.q + (qrow_tok * H + kvh * G + r % G) * D + k * 8;
                     cp_async16(smem_u32(qreg + swz(r, k, kQRows)), src);
                 }
                 cp_async_wait_all();
@@ -805,6 +838,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     uint32_t kt = smem_u32(stages + (size_t)st * SM::kStage);
                     uint32_t vt = kt + SM::kTile;
                     const int ntok = stage_ntok[st];
+                    const int ctx0 = stage_tok0[st];
                     if constexpr (EB == 1) {
                         // Widen the stage into the fp16 copy (once every warp is
                         // done with the previous one), then free the stage.
@@ -819,11 +853,13 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     }
                     if (active) {
                         if (NTw == 16) {
-                            cf_chunk<C, D, 16>(kt, vt, ntok, tp * 16, qblock, p.scale_log2, m, s, o, lane);
+                            cf_chunk<C, D, 16>(kt, vt, ntok, tp * 16, ctx0, lim[0], lim[1], qblock, p.scale_log2,
+                                               m, s, o, lane);
                         } else if constexpr (C >= 32) {
                             // 32 tokens at a time keeps the score tile in registers
                             for (int t0 = tp * NTw; t0 < (tp + 1) * NTw; t0 += 32)
-                                cf_chunk<C, D, 32>(kt, vt, ntok, t0, qblock, p.scale_log2, m, s, o, lane);
+                                cf_chunk<C, D, 32>(kt, vt, ntok, t0, ctx0, lim[0], lim[1], qblock, p.scale_log2,
+                                                   m, s, o, lane);
                         }
                     }
                     if constexpr (EB == 2) {
@@ -890,8 +926,8 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     for (int r = 0; r < 2; ++r) {
                         const int row = rb * 16 + g + 8 * r;
                         if (row < m_rows) {
-                            const int pos = q_lo + row / G, qh = kvh * G + row % G;
-                            const int pid = p.pbase[pos * H + qh] + upart;
+                            const int pos = q_lo + row / RW, jq = (row % RW) / G, qh = kvh * G + row % G;
+                            const int pid = p.pbase[((size_t)pos * QL + jq) * H + qh] + upart;
                             float* dst = p.part_o + (size_t)pid * D;
 #pragma unroll
                             for (int dt = 0; dt < D / 8; ++dt)
@@ -1004,7 +1040,7 @@ size_t smem_for(const ca_pool_config& c, int stages) {
     const size_t eb = (size_t)kv_elem_bytes(c), cd = (size_t)c.chunk * c.head_dim;
     const size_t conv = eb == 1 ? 2 * cd * 2 : 0;
     return (size_t)stages * 2 * cd * eb + conv + (size_t)dev::kQRows * c.head_dim * 2 + 512 +
-           2 * dev::kMaxStages * 8 + 4 * dev::kRing + 4 * dev::kMaxStages;
+           2 * dev::kMaxStages * 8 + 4 * dev::kRing + 2 * 4 * dev::kMaxStages;
 }
 }  // namespace
 
@@ -1130,7 +1166,7 @@ int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void*
     if (e != cudaSuccess) return CA_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
     // Merge: one warp per (position, head).
-    const int n_pairs = s.t.b * p.cfg.n_heads;
+    const int n_pairs = s.t.b * s.q_len * p.cfg.n_heads;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3((unsigned)((n_pairs + 3) / 4));
     lc.blockDim = dim3(128);

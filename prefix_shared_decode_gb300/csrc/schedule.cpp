@@ -77,8 +77,9 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
 
     t.b = b;
     for (auto* v : {&t.seq_perm, &t.cf_rows, &t.cf_runs, &t.sf_offsets, &t.sf_chunks, &t.merge_offsets,
-                    &t.merge_runs})
+                    &t.merge_runs, &t.row_tok0, &t.sf_tok0, &t.ctx_len})
         v->clear();
+    const int32_t c = p.cfg.chunk;
     // Depth-first order over the shared nodes only: at a node, the sequences
     // ending there, then its children in insertion order; a child held by
     // one batch sequence is that sequence's chain, which contributes exactly
@@ -97,6 +98,7 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
                 const_cast<Node*>(node)->row = (int32_t)row_node.size();
                 row_node.push_back(node);
                 t.cf_rows.insert(t.cf_rows.end(), {node->slot, node->ntok, (int32_t)order.size(), -1});
+                t.row_tok0.push_back((int32_t)(stack.size() - 2) * c);   // path index x c
             }
             for (int32_t k = 0; k < node->end_count; ++k) order.push_back(ends[node->end_begin + k].row);
         }
@@ -139,14 +141,19 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
         t.sf_offsets[pos + 1] = t.sf_offsets[pos] + (int32_t)(seq_of[i]->path.size() - k);
     }
     t.sf_chunks.resize(2 * (size_t)t.sf_offsets[b]);
+    t.sf_tok0.resize((size_t)t.sf_offsets[b]);
+    t.ctx_len.resize(b);
     for (int32_t pos = 0; pos < b; ++pos) {
         const int32_t i = order[pos];
         const auto& path = seq_of[i]->path;
         int32_t* dst = t.sf_chunks.data() + 2 * (size_t)t.sf_offsets[pos];
+        int32_t* tok0 = t.sf_tok0.data() + t.sf_offsets[pos];
         for (size_t k = tpp ? (size_t)chain_at[i] : 0; k < path.size(); ++k) {
             *dst++ = path[k]->slot;
             *dst++ = path[k]->ntok;
+            *tok0++ = (int32_t)k * c;        // every chunk before the last is full
         }
+        t.ctx_len[pos] = seq_of[i]->length;
     }
 
     // Merge lists: runs are nested intervals listed in pre-order, so a
@@ -188,18 +195,20 @@ constexpr int32_t kTailUnitsPerCta = 2;     // aim: about this many queue units 
 constexpr int32_t kTailUnitMin = 2, kTailUnitMax = 8;
 }  // namespace
 
-void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
-    // Work is per key/value head (H of them); partials are per query head
-    // (HQ = H * G; G = 1 is multi-head attention).  With G > 1 a
-    // sequence-first chunk-head multiplies G query rows, on tensor cores.
-    const int32_t HQ = p.cfg.n_heads, H = kv_heads(p.cfg), G = HQ / H;
+void build_plan(const Pool& p, const Tables& t, int32_t grid, int32_t q_len, Plan& plan) {
+    // Work is per key/value head (H of them); partials are per query token
+    // and query head (HQ = H * G; G = 1 is multi-head attention).  Each
+    // position brings RW = q_len * G query rows per key/value head; with
+    // RW > 1 a sequence-first chunk-head multiplies them on tensor cores.
+    const int32_t HQ = p.cfg.n_heads, H = kv_heads(p.cfg), G = HQ / H, RW = q_len * G;
     const int32_t D = p.cfg.head_dim, c = p.cfg.chunk, b = t.b;
-    const double sf_cost = (G == 1) ? 1.0 : 1.0 + kCfComputePer16 * ((G + 15) / 16);
+    plan.q_len = q_len;
+    const double sf_cost = (RW == 1) ? 1.0 : 1.0 + kCfComputePer16 * ((RW + 15) / 16);
     // An fp8 pool halves a tile's bytes, but the tensor-core phase widens each
     // tile to fp16 in shared memory first, so there (and only there, when the
     // sequence-first phase runs on CUDA cores) a chunk-first tile costs more
     // relative to a sequence-first one.
-    const double cf_mult = ((p.cfg.flags & CA_KV_FP8) && G == 1) ? kF8CfFactor : 1.0;
+    const double cf_mult = ((p.cfg.flags & CA_KV_FP8) && RW == 1) ? kF8CfFactor : 1.0;
     auto rows_cost = [&](int32_t m_rows) {
         return cf_mult * (1.0 + kCfComputePer16 * ((m_rows + 15) / 16)) / sf_cost;
     };
@@ -212,18 +221,24 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
 
     // Chunk list: chunk-first rows first (index = row), then sf chunks.
     plan.chunks.resize(R + t.sf_chunks.size() / 2);
-    for (int32_t r = 0; r < R; ++r) plan.chunks[r] = {t.cf_rows[4 * r], t.cf_rows[4 * r + 1]};
-    for (size_t i = 0; i < t.sf_chunks.size() / 2; ++i)
+    plan.chunk_tok0.resize(plan.chunks.size());
+    for (int32_t r = 0; r < R; ++r) {
+        plan.chunks[r] = {t.cf_rows[4 * r], t.cf_rows[4 * r + 1]};
+        plan.chunk_tok0[r] = t.row_tok0[r];
+    }
+    for (size_t i = 0; i < t.sf_chunks.size() / 2; ++i) {
         plan.chunks[R + i] = {t.sf_chunks[2 * i], t.sf_chunks[2 * i + 1]};
+        plan.chunk_tok0[R + i] = t.sf_tok0[i];
+    }
 
     // Totals for the per-CTA budget.
     double sf_total = (double)(t.sf_chunks.size() / 2) * H;
     double cf_total = 0;
     for (int32_t u = 0; u < U; ++u) {
         const int32_t nrows = t.cf_runs[4 * u + 1], m = t.cf_runs[4 * u + 3] - t.cf_runs[4 * u + 2];
-        const int32_t max_pos = std::max(1, kMaxCfQueries / G);
+        const int32_t max_pos = std::max(1, kMaxCfQueries / RW);
         const int32_t ngroups = (m + max_pos - 1) / max_pos;
-        cf_total += (double)nrows * H * ngroups * rows_cost((m + ngroups - 1) / ngroups * G);
+        cf_total += (double)nrows * H * ngroups * rows_cost((m + ngroups - 1) / ngroups * RW);
     }
     const int32_t tiles_ceiling = (int32_t)std::max(1.0, sf_total + cf_total);
     grid = std::max(1, std::min(grid, tiles_ceiling));
@@ -240,17 +255,17 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
     for (int32_t u = 0; u < U; ++u) {
         const int32_t row0 = t.cf_runs[4 * u], nrows = t.cf_runs[4 * u + 1];
         const int32_t lo = t.cf_runs[4 * u + 2], hi = t.cf_runs[4 * u + 3], m = hi - lo;
-        // query groups of at most 64 (position, query head) rows
-        const int32_t max_pos = std::max(1, kMaxCfQueries / G);
+        // query groups of at most 64 (position, query token, query head) rows
+        const int32_t max_pos = std::max(1, kMaxCfQueries / RW);
         const int32_t ngroups = (m + max_pos - 1) / max_pos;
         const int32_t mg = (m + ngroups - 1) / ngroups;
-        const double row_cost = rows_cost(mg * G);
+        const double row_cost = rows_cost(mg * RW);
         // Enough rows per piece that partial traffic (2 x mg x G x (D+2)
         // floats) stays under 1/8 of the piece's KV bytes, but never so many
         // that one piece outweighs a CTA's share by more than a quarter: the
         // longest unit bounds the kernel, while extra partials are spread
         // over every CTA and the merge.
-        const int32_t rmin = std::max(1, (int32_t)((16.0 * mg * G * (D + 2)) / ((double)c * D) + 0.999));
+        const int32_t rmin = std::max(1, (int32_t)((16.0 * mg * RW * (D + 2)) / ((double)c * D) + 0.999));
         const int32_t rpar = std::max(1, (int32_t)(avg / row_cost));
         const int32_t rcap = std::max(1, (int32_t)(1.25 * avg / row_cost));
         const int32_t per = std::max(rpar, std::min(rmin, rcap));
@@ -264,7 +279,7 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
                 const int32_t rb = row0 + (int32_t)((int64_t)nrows * (k + 1) / np);
                 // A unit covers a range of heads (the kernel reloads the query
                 // tile per head), as many as keep it within a CTA's share.
-                const double head_cost = (rb - ra) * rows_cost((qb - qa) * G);
+                const double head_cost = (rb - ra) * rows_cost((qb - qa) * RW);
                 const int32_t hp = std::max(1, std::min(H, (int32_t)(avg / head_cost)));
                 const int32_t nparts = (H + hp - 1) / hp;
                 for (int32_t hk = 0; hk < nparts; ++hk) {
@@ -430,18 +445,19 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, Plan& plan) {
         }
     }
 
-    // partial ids per (position, query head); the G query heads of a key/value
-    // head have the same pieces
-    plan.pbase.resize((size_t)b * HQ + 1);
+    // partial ids per (position, query token, query head); every query token
+    // and the G query heads of a key/value head have the same pieces
+    plan.pbase.resize((size_t)b * q_len * HQ + 1);
     {
         int32_t acc = 0;
         size_t i = 0;
         plan.pbase[0] = 0;
         for (int32_t pos = 0; pos < b; ++pos)
-            for (int32_t h = 0; h < H; ++h) {
-                const int32_t np = npart[(size_t)pos * H + h];
-                for (int32_t g = 0; g < G; ++g) plan.pbase[++i] = (acc += np);
-            }
+            for (int32_t j = 0; j < q_len; ++j)
+                for (int32_t h = 0; h < H; ++h) {
+                    const int32_t np = npart[(size_t)pos * H + h];
+                    for (int32_t g = 0; g < G; ++g) plan.pbase[++i] = (acc += np);
+                }
     }
     plan.n_partials = plan.pbase.back();
     // Lay the lists out: per CTA its chunk-first units, then its pieces.
@@ -477,6 +493,8 @@ void layout_plan(const Plan& plan, int32_t b, PlanLayout& lay, std::vector<unsig
     lay.pbase = off;     off = align256(off + plan.pbase.size() * sizeof(int32_t));
     lay.status = off;    off = align256(off + sizeof(int32_t));
     lay.counter = off;   off = align256(off + sizeof(int32_t));
+    lay.chunk_tok0 = off; off = align256(off + plan.chunk_tok0.size() * sizeof(int32_t));
+    lay.ctx_len = off;   off = align256(off + (size_t)b * sizeof(int32_t));
     lay.total = off;
     blob.assign(off, 0);
     std::memcpy(blob.data() + lay.chunks, plan.chunks.data(), plan.chunks.size() * sizeof(ChunkRef));
@@ -484,6 +502,8 @@ void layout_plan(const Plan& plan, int32_t b, PlanLayout& lay, std::vector<unsig
     std::memcpy(blob.data() + lay.cta_begin, plan.cta_begin.data(), plan.cta_begin.size() * sizeof(int32_t));
     std::memcpy(blob.data() + lay.seq_perm, t.seq_perm.data(), (size_t)b * sizeof(int32_t));
     std::memcpy(blob.data() + lay.pbase, plan.pbase.data(), plan.pbase.size() * sizeof(int32_t));
+    std::memcpy(blob.data() + lay.chunk_tok0, plan.chunk_tok0.data(), plan.chunk_tok0.size() * sizeof(int32_t));
+    std::memcpy(blob.data() + lay.ctx_len, t.ctx_len.data(), (size_t)b * sizeof(int32_t));
 }
 
 void layout_ws(const Plan& plan, const Pool& p, int32_t b, WsLayout& ws) {
@@ -492,8 +512,8 @@ void layout_ws(const Plan& plan, const Pool& p, int32_t b, WsLayout& ws) {
     ws.part_o = off;   off = align256(off + (size_t)plan.n_partials * D * sizeof(float));
     ws.part_ms = off;  off = align256(off + (size_t)plan.n_partials * 2 * sizeof(float));
     ws.total = off;
-    ws.q_stage = off;  off = align256(off + (size_t)b * H * D * 2);
-    ws.out_stage = off; off = align256(off + (size_t)b * H * D * 2);
+    ws.q_stage = off;  off = align256(off + (size_t)b * plan.q_len * H * D * 2);
+    ws.out_stage = off; off = align256(off + (size_t)b * plan.q_len * H * D * 2);
     ws.total_host = off;
 }
 

@@ -46,9 +46,9 @@ def load(torch, wl, no_sharing=False, capacity=None):
     return pool
 
 
-def run(torch, pool, batch, q, no_tpp=False, layer=0, scale=None):
+def run(torch, pool, batch, q, no_tpp=False, layer=0, scale=None, q_len=1):
     from prefix_shared_decode_gb300 import decode_attention
-    sched = pool.schedule(batch, no_tpp=no_tpp)
+    sched = pool.schedule(batch, no_tpp=no_tpp, q_len=q_len, causal=q_len > 1)
     out = decode_attention(pool, sched, torch.from_numpy(q).cuda(), layer=layer, scale=scale)
     assert sched.device_status() == 0
     return out.cpu().numpy(), sched
@@ -204,6 +204,76 @@ def test_fp8_pool_shape_limits(torch_cuda):
     assert e.value.name == "CA_ERR_INVALID"
     p = Pool(1, 2, 128, 16, 10, kv_dtype="fp8")
     assert p.kv_view().dtype == torch_cuda.uint8 and p.kv_bytes < Pool(1, 2, 128, 16, 10).kv_bytes
+
+
+@pytest.mark.parametrize("q_len,causal,G,c,kv_dtype", [(2, False, 1, 16, "fp16"), (4, True, 1, 64, "fp16"),
+                                                      (3, True, 2, 32, "fp16"), (8, True, 1, 32, "fp16"),
+                                                      (2, True, 4, 64, "fp16"), (16, True, 4, 16, "fp16"),
+                                                      (4, True, 1, 64, "fp8")])
+def test_multi_token_queries_every_output(torch_cuda, q_len, causal, G, c, kv_dtype):
+    """Several query tokens per sequence (q / out [b, q_len, H, D]), with and
+    without the causal mask, against the definition."""
+    from prefix_shared_decode_gb300 import Pool, decode_attention, decode_attention_host
+    torch = torch_cuda
+    Hkv, D, L = 2, 128, 2
+    rng = np.random.default_rng(80 + q_len + c)
+    seqs = random_segment_sequences(80 + q_len, 12, c, n_segments=10)
+    pool = Pool(L, Hkv * G, D, c, 700, n_kv_heads=Hkv, kv_dtype=kv_dtype)
+    trie = OracleTrie(c, 700)
+    for i, toks in enumerate(seqs):
+        k = rng.standard_normal((L, len(toks), Hkv, D), dtype=np.float32).astype(np.float16)
+        v = rng.standard_normal((L, len(toks), Hkv, D), dtype=np.float32).astype(np.float16)
+        if kv_dtype == "fp8":
+            trie.insert(i, toks, F8.dequantize(F8.quantize(k, 1.0), 1.0), F8.dequantize(F8.quantize(v, 1.0), 1.0))
+        else:
+            trie.insert(i, toks, k, v)
+        pool.insert(i, toks, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+    batch = [int(x) for x in rng.permutation(12) if len(seqs[x]) >= q_len][:10]
+    q = rng.standard_normal((len(batch), q_len, Hkv * G, D), dtype=np.float32).astype(np.float16)
+    for layer in range(L):
+        want = A.decode_attention_multi(trie, batch, layer, q, 1 / np.sqrt(D), causal)
+        for no_tpp in (False, True):
+            sched = pool.schedule(batch, no_tpp=no_tpp, q_len=q_len, causal=causal)
+            got = decode_attention(pool, sched, torch.from_numpy(q).cuda(), layer=layer).cpu().numpy()
+            assert sched.device_status() == 0
+            assert_close(got, want, f"q_len={q_len} causal={causal} G={G} layer={layer} no_tpp={no_tpp}")
+    # the host-buffer entry point with the same schedule
+    qh = torch.from_numpy(q).pin_memory()
+    oh = torch.empty_like(qh).pin_memory()
+    decode_attention_host(pool, sched, qh, oh, layer=1)
+    torch.cuda.synchronize()
+    assert_close(oh.numpy(), A.decode_attention_multi(trie, batch, 1, q, 1 / np.sqrt(D), causal), "host io")
+
+
+def test_speculative_verification_over_appended_drafts(torch_cuda):
+    """Draft tokens are appended to each sequence (filling and growing
+    chunks), then all of them are verified in one causal multi-token call;
+    then they are accepted one more step."""
+    from prefix_shared_decode_gb300 import Pool, decode_attention
+    torch = torch_cuda
+    c, H, D, q_len = 64, 4, 128, 5
+    rng = np.random.default_rng(90)
+    seqs = random_segment_sequences(90, 8, c, n_segments=6)
+    pool, trie = Pool(1, H, D, c, 500), OracleTrie(c, 500)
+    for i, toks in enumerate(seqs):
+        k = rng.standard_normal((1, len(toks), H, D), dtype=np.float32).astype(np.float16)
+        v = rng.standard_normal((1, len(toks), H, D), dtype=np.float32).astype(np.float16)
+        trie.insert(i, toks, k, v)
+        pool.insert(i, toks, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+    batch = list(range(8))
+    for step in range(3):
+        for sid in batch:
+            toks = [10**6 + 1000 * step + 50 * sid + j for j in range(q_len)]
+            k = rng.standard_normal((1, q_len, H, D), dtype=np.float32).astype(np.float16)
+            v = rng.standard_normal((1, q_len, H, D), dtype=np.float32).astype(np.float16)
+            trie.append(sid, toks, k, v)
+            pool.append(sid, toks, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+        q = rng.standard_normal((8, q_len, H, D), dtype=np.float32).astype(np.float16)
+        sched = pool.schedule(batch, q_len=q_len, causal=True)
+        got = decode_attention(pool, sched, torch.from_numpy(q).cuda()).cpu().numpy()
+        assert sched.device_status() == 0
+        assert_close(got, A.decode_attention_multi(trie, batch, 0, q, 1 / np.sqrt(D), causal=True),
+                     f"step {step}")
 
 
 def test_edge_cases(torch_cuda):
@@ -425,7 +495,7 @@ SAMPLE = 4
 
 @pytest.mark.parametrize("name", ["llama7b_p1024", "sweep_s2048_b32", "sweep_s2048_b64",
                                   "sweep_s4096_b32", "sweep_s4096_b64", "no_sharing", "gqa_p1024",
-                                  "llama7b_p1024_fp8", "sweep_s4096_b64_fp8"])
+                                  "llama7b_p1024_fp8", "sweep_s4096_b64_fp8", "llama7b_p1024_q4"])
 def test_full_size_workloads_sampled(torch_cuda, name):
     """The benchmark's launch configuration at full size; every output is
     finite and SAMPLE sequences (all heads) match the oracle."""
@@ -433,14 +503,19 @@ def test_full_size_workloads_sampled(torch_cuda, name):
     pool = load(torch_cuda, wl)
     batch = wl.seq_ids()
     q = wl.queries(0)
-    got, sched = run(torch_cuda, pool, batch, q)
+    got, sched = run(torch_cuda, pool, batch, q, q_len=wl.q_len)
     assert np.isfinite(got).all()
     rng = np.random.default_rng(0)
     for i in sorted(rng.choice(len(batch), size=SAMPLE, replace=False)):
         k, v = wl.kv_rows(batch[i])
         if wl.kv_dtype == "fp8":                         # the dequantised rows (scales 1)
             k, v = F8.dequantize(F8.quantize(k, 1.0), 1.0), F8.dequantize(F8.quantize(v, 1.0), 1.0)
-        want = A.softmax_attention(q[i], k[0], v[0], wl.scale)
+        if wl.q_len == 1:
+            want = A.softmax_attention(q[i], k[0], v[0], wl.scale)
+        else:                                            # causal: token j sees n - q_len + j + 1 tokens
+            n = k.shape[1]
+            want = np.stack([A.softmax_attention(q[i, j], k[0, :n - wl.q_len + j + 1], v[0, :n - wl.q_len + j + 1],
+                                                 wl.scale) for j in range(wl.q_len)])
         assert_close(got[i], want, f"{name} seq {batch[i]}")
 
 

@@ -205,3 +205,74 @@ def test_grouped_query_attention_equals_repeated_kv(G):
 def test_grouped_query_heads_must_divide():
     with pytest.raises(OracleError):
         A.softmax_attention(np.zeros((3, 2)), np.zeros((1, 2, 2)), np.zeros((1, 2, 2)), 1.0)
+
+
+def _trie_with(rng, n_seqs, lengths, H=2, D=4, c=3):
+    trie = OracleTrie(c, 200)
+    for s in range(n_seqs):
+        toks = list(range(7)) + [100 + 20 * s + i for i in range(lengths[s])]
+        trie.insert(s, toks, rand((1, len(toks), H, D), rng), rand((1, len(toks), H, D), rng))
+    return trie
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_multi_token_queries_with_one_token_are_decode_attention(causal):
+    rng = np.random.default_rng(30)
+    trie = _trie_with(rng, 3, [2, 5, 1])
+    q = rand((3, 1, 2, 4), rng)
+    np.testing.assert_allclose(A.decode_attention_multi(trie, [2, 0, 1], 0, q, 0.5, causal)[:, 0],
+                               A.decode_attention(trie, [2, 0, 1], 0, q[:, 0], 0.5), rtol=1e-13, atol=1e-14)
+
+
+def test_multi_token_queries_without_mask_are_independent_queries():
+    # every token sees the whole context: each token row is its own decode query
+    rng = np.random.default_rng(31)
+    trie = _trie_with(rng, 2, [4, 3])
+    q = rand((2, 3, 2, 4), rng)
+    got = A.decode_attention_multi(trie, [0, 1], 0, q, 0.7)
+    for j in range(3):
+        np.testing.assert_allclose(got[:, j], A.decode_attention(trie, [0, 1], 0, q[:, j], 0.7),
+                                   rtol=1e-13, atol=1e-14)
+
+
+def test_causal_queries_over_a_whole_sequence_are_causal_self_attention():
+    # q_len = n: token j attends to tokens 0..j (brute force per token)
+    rng = np.random.default_rng(32)
+    H, D, n = 2, 4, 9
+    trie = OracleTrie(4, 10)
+    k, v = rand((1, n, H, D), rng), rand((1, n, H, D), rng)
+    trie.insert(0, list(range(n)), k, v)
+    q = rand((1, n, H, D), rng)
+    got = A.decode_attention_multi(trie, [0], 0, q, 0.6, causal=True)
+    for j in range(n):
+        want = brute_force(q[0, j].tolist(), k[0, :j + 1].tolist(), v[0, :j + 1].tolist(), 0.6)
+        np.testing.assert_allclose(got[0, j], want, rtol=1e-12, atol=1e-13)
+    # the last token sees everything, the first only itself
+    np.testing.assert_allclose(got[0, -1], A.softmax_attention(q[0, -1], k[0], v[0], 0.6), rtol=1e-13)
+    np.testing.assert_allclose(got[0, 0], v[0, 0], rtol=0, atol=1e-15)
+
+
+def test_multi_token_queries_match_the_two_phase_form():
+    # the blog's two-phase function over a shared prefix, token by token
+    rng = np.random.default_rng(33)
+    b, H, D, ns, ql = 3, 2, 4, 6, 2
+    pk, pv = rand((ns, H, D), rng), rand((ns, H, D), rng)
+    sk = [rand((int(rng.integers(1, 5)), H, D), rng) for _ in range(b)]
+    sv = [rand((x.shape[0], H, D), rng) for x in sk]
+    trie = OracleTrie(ns, 50)
+    for i in range(b):
+        toks = list(range(ns)) + [1000 + 10 * i + t for t in range(sk[i].shape[0])]
+        trie.insert(i, toks, np.concatenate([pk, sk[i]])[None], np.concatenate([pv, sv[i]])[None])
+    q = rand((b, ql, H, D), rng)
+    got = A.decode_attention_multi(trie, list(range(b)), 0, q, 0.4)
+    for j in range(ql):
+        np.testing.assert_allclose(got[:, j], A.two_phase_single_prefix(q[:, j], pk, pv, sk, sv, 0.4),
+                                   rtol=1e-12, atol=1e-13)
+
+
+def test_causal_context_shorter_than_the_queries_is_an_error():
+    rng = np.random.default_rng(34)
+    trie = OracleTrie(3, 10)
+    trie.insert(0, [1, 2], rand((1, 2, 1, 2), rng), rand((1, 2, 1, 2), rng))
+    with pytest.raises(OracleError):
+        A.decode_attention_multi(trie, [0], 0, rand((1, 3, 1, 2), rng), 1.0, causal=True)

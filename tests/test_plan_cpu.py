@@ -135,3 +135,98 @@ def test_plan_with_grouped_query_heads(lib, G):
     out, _ = simulate(sched.plan(), sched.tables(), trie, q, 0.125, Hkv, G)
     np.testing.assert_allclose(out, A.decode_attention(trie, batch, 0, q, 0.125), rtol=1e-10, atol=1e-12)
 
+
+
+def simulate_multi(plan, tables, trie, batch, q, scale, H, G, q_len, causal):
+    """The exported plan evaluated for q_len query tokens per position: rows
+    (position, token, query head); under the causal mask a chunk's row r at
+    context offset depth * c counts for token j iff offset + r <= n - q_len + j."""
+    c = trie.chunk
+    node_of, depth = {}, {}
+    stack = [(trie.root, -1)]
+    while stack:
+        n, d = stack.pop()
+        if n.slot >= 0:
+            node_of[n.slot], depth[n.slot] = n, d
+        stack.extend((ch, d + 1) for ch in n.children)
+    perm, pbase = tables["seq_perm"], plan["pbase"]
+    HQ = H * G
+    n_ctx = [trie.lengths[batch[perm[pos]]] for pos in range(len(perm))]
+    parts = {}
+
+    def emit(pos, kvh, part, chunks):
+        for j in range(q_len):
+            lim = n_ctx[pos] - q_len + j if causal else 1 << 30
+            ks, vs = [], []
+            for s, t in chunks:
+                rows = [r for r in range(int(t)) if depth[int(s)] * c + r <= lim]
+                ks.append(node_of[int(s)].k[0][rows, kvh])
+                vs.append(node_of[int(s)].v[0][rows, kvh])
+            k = np.concatenate(ks)[:, None, :]
+            v = np.concatenate(vs)[:, None, :]
+            for qh in range(kvh * G, (kvh + 1) * G):
+                i = (pos * q_len + j) * HQ + qh
+                pid = pbase[i] + part
+                assert pbase[i] <= pid < pbase[i + 1]
+                assert pid not in parts
+                parts[pid] = A.partial(q[perm[pos], j, qh][None, :], k, v, scale)
+
+    for kind, h, lo, hi, cb, ce, part, qrow, n, base, part_next, _ in plan["units"]:
+        if kind == 0:
+            assert (hi - lo) * q_len * G <= 64
+            for hh in range(h, h + n):
+                for pos in range(lo, hi):
+                    emit(pos, hh, part, plan["chunks"][cb:ce])
+        else:
+            L = cb
+            while L < ce:
+                hh, j = divmod(L, n)
+                z = min(ce, (hh + 1) * n)
+                emit(lo, hh, part if hh == h else part_next, plan["chunks"][base + j:base + j + (z - L)])
+                L = z
+    assert len(parts) == pbase[-1]
+    out = np.empty(q.shape)
+    for pos in range(len(perm)):
+        for j in range(q_len):
+            for h in range(HQ):
+                i = (pos * q_len + j) * HQ + h
+                out[perm[pos], j, h] = A.merge([parts[x] for x in range(pbase[i], pbase[i + 1])])[0]
+    return out
+
+
+@pytest.mark.parametrize("q_len,causal,G", [(2, False, 1), (3, True, 1), (5, True, 2), (4, False, 2), (8, True, 1)])
+@pytest.mark.parametrize("seed", range(3))
+def test_plan_with_multi_token_queries(lib, q_len, causal, G, seed):
+    from prefix_shared_decode_gb300 import Pool
+    Hkv, D, c = 2, 64, 16
+    rng = np.random.default_rng(70 + seed)
+    seqs = random_segment_sequences(70 + seed, 10, c)
+    pool = Pool(1, Hkv * G, D, c, 600, host_only=True, n_kv_heads=Hkv)
+    trie = OracleTrie(c, 600)
+    for i, toks in enumerate(seqs):
+        k = rng.standard_normal((1, len(toks), Hkv, D))
+        trie.insert(i, toks, k, k * 0.3 + 1)
+        pool.insert(i, toks)
+    # a causal batch needs every context at least q_len tokens long
+    batch = [int(x) for x in rng.permutation(10) if len(seqs[x]) >= q_len][:8]
+    q = rng.standard_normal((len(batch), q_len, Hkv * G, D))
+    for no_tpp in (False, True):
+        sched = pool.schedule(batch, no_tpp=no_tpp, q_len=q_len, causal=causal)
+        out = simulate_multi(sched.plan(), sched.tables(), trie, batch, q, 0.125, Hkv, G, q_len, causal)
+        want = A.decode_attention_multi(trie, batch, 0, q, 0.125, causal)
+        np.testing.assert_allclose(out, want, rtol=1e-10, atol=1e-12)
+
+
+def test_multi_token_schedule_limits(lib):
+    from prefix_shared_decode_gb300 import CAError, Pool
+    pool = Pool(1, 8, 64, 16, 50, host_only=True, n_kv_heads=2)       # G = 4
+    pool.insert(0, list(range(20)))
+    pool.insert(1, list(range(3)))
+    with pytest.raises(CAError) as e:
+        pool.schedule([0], q_len=17)                                     # 17 * 4 rows > 64
+    assert e.value.name == "CA_ERR_UNSUPPORTED"
+    with pytest.raises(CAError) as e:
+        pool.schedule([0, 1], q_len=4, causal=True)                      # a 3-token context
+    assert e.value.name == "CA_ERR_INVALID"
+    pool.schedule([0, 1], q_len=4)                                       # no mask: fine
+    assert len(pool.schedule([0], q_len=16).plan()["pbase"]) == 16 * 8 + 1

@@ -45,10 +45,12 @@ def segment_kv(seed: int, seg_id: int, n: int, n_layers: int, n_heads: int,
 
 
 def step_queries(seed: int, step: int, b: int, n_heads: int, head_dim: int,
-                 layer: int = 0) -> np.ndarray:
-    """Decode queries of one step, float16 [b, H, D], N(0, 1)."""
+                 layer: int = 0, q_len: int = 1) -> np.ndarray:
+    """Decode queries of one step, float16 [b, H, D] ([b, q_len, H, D] for
+    several query tokens per sequence), N(0, 1)."""
     rng = np.random.default_rng([seed, 2, step, layer])
-    return rng.standard_normal((b, n_heads, head_dim), dtype=np.float32).astype(np.float16)
+    shape = (b, n_heads, head_dim) if q_len == 1 else (b, q_len, n_heads, head_dim)
+    return rng.standard_normal(shape, dtype=np.float32).astype(np.float16)
 
 
 @dataclass
@@ -62,6 +64,7 @@ class Workload:
     seed: int
     n_kv_heads: int = 0            # key/value heads (0: one per query head)
     kv_dtype: str = "fp16"         # pool storage: "fp16", or "fp8" (E4M3, scales 1)
+    q_len: int = 1                 # query tokens per sequence (> 1: causal, the last q_len tokens)
     seg_len: dict[int, int] = field(default_factory=dict)
     seqs: dict[int, list[int]] = field(default_factory=dict)  # seq_id -> segment ids
     churn: int = 0  # sequences removed and inserted per step (multi-tenant tree)
@@ -113,7 +116,7 @@ class Workload:
 
     def queries(self, step: int, b: int | None = None, layer: int = 0) -> np.ndarray:
         return step_queries(self.seed, step, len(self.seqs) if b is None else b,
-                            self.n_heads, self.head_dim, layer)
+                            self.n_heads, self.head_dim, layer, self.q_len)
 
     def unique_tokens(self) -> int:
         """Tokens of the distinct segments the live sequences use."""
@@ -197,7 +200,16 @@ def make(name: str) -> Workload:
     llama7b_p1024_fp8, sweep_s4096_b64_fp8
                     those trees (same seeds) in a pool that stores K/V as FP8
                     E4M3 with scales 1 (the inputs stay fp16 N(0, 1)).
+    llama7b_p1024_q4
+                    llama7b_p1024 with 4 query tokens per sequence (draft
+                    tokens being verified): causal, token j sees the context
+                    up to its own position, the last 4 tokens.
     """
+    if name.endswith("_q4"):
+        w = make(name[:-3])
+        w.name, w.q_len = name, 4
+        w.description += "; 4 query tokens per sequence under the causal mask (the last 4 context tokens)"
+        return w
     if name.endswith("_fp8"):
         w = make(name[:-4])
         w.name, w.kv_dtype = name, "fp8"
@@ -230,4 +242,4 @@ def make(name: str) -> Workload:
 
 ALL = ["tiny", "llama7b_p1024", "sweep_s2048_b32", "sweep_s2048_b64",
        "sweep_s4096_b32", "sweep_s4096_b64", "no_sharing", "multi_tenant", "gqa_p1024",
-       "llama7b_p1024_fp8", "sweep_s4096_b64_fp8"]
+       "llama7b_p1024_fp8", "sweep_s4096_b64_fp8", "llama7b_p1024_q4"]
