@@ -199,6 +199,8 @@ inline int32_t kv_heads(const ca_pool_config& c) { return c.n_kv_heads > 0 ? c.n
 // effective dequantisation scales.
 inline int kv_elem_bytes(const ca_pool_config& c) { return (c.flags & CA_KV_FP8) ? 1 : 2; }
 inline float kv_scale_of(float s) { return s == 0.f ? 1.f : s; }
+// Query rows one tensor-core unit takes: 64, or 32 at head_dim 256.
+inline int32_t max_query_rows(const ca_pool_config& c) { return c.head_dim == 256 ? 32 : 64; }
 size_t pool_tile_bytes(const ca_pool_config& c);
 size_t pool_total_bytes(const ca_pool_config& c);
 

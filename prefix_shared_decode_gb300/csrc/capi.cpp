@@ -34,7 +34,10 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 int check_cfg(const ca_pool_config* c) {
     if (!c) return CA_ERR_INVALID;
     if (c->n_layers < 1 || c->n_heads < 1 || c->capacity_slots < 1) return CA_ERR_INVALID;
-    if (c->head_dim != 64 && c->head_dim != 128) return CA_ERR_UNSUPPORTED;
+    if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return CA_ERR_UNSUPPORTED;
+    // head_dim 256: chunks of at most 32 tokens (two stages of K+V must fit
+    // beside the query tile), fp16 only
+    if (c->head_dim == 256 && (c->chunk > 32 || (c->flags & CA_KV_FP8))) return CA_ERR_UNSUPPORTED;
     if (c->chunk != 16 && c->chunk != 32 && c->chunk != 64) return CA_ERR_UNSUPPORTED;
     if (c->flags & ~(CA_NO_SHARING | CA_KV_FP8)) return CA_ERR_INVALID;
     if (c->flags & CA_KV_FP8) {
@@ -43,7 +46,7 @@ int check_cfg(const ca_pool_config* c) {
             if (!(sc == 0.f || (sc > 0.f && sc < 3.0e38f))) return CA_ERR_INVALID;
     }
     if (c->n_kv_heads < 0 || (c->n_kv_heads > 0 && c->n_heads % c->n_kv_heads)) return CA_ERR_INVALID;
-    if (c->n_heads / kv_heads(*c) > 64) return CA_ERR_UNSUPPORTED;
+    if (c->n_heads / kv_heads(*c) > max_query_rows(*c)) return CA_ERR_UNSUPPORTED;
     // TMA row coordinates are 32-bit.
     const long double rows = (long double)c->capacity_slots * c->n_layers * 2 * kv_heads(*c) * c->chunk;
     if (rows > 2147483647.0L) return CA_ERR_UNSUPPORTED;
@@ -253,7 +256,8 @@ int ca_build_schedule_ex(ca_pool* pool, const int64_t* seq_ids, int32_t b, int32
                          ca_sched** inout, void* stream) {
     if (!pool || !inout || !seq_ids || b < 1 || q_len < 1 || (flags & ~(CA_SCHED_NO_TPP | CA_SCHED_CAUSAL)))
         return CA_ERR_INVALID;
-    if ((int64_t)q_len * (pool->cfg.n_heads / kv_heads(pool->cfg)) > 64) return CA_ERR_UNSUPPORTED;
+    if ((int64_t)q_len * (pool->cfg.n_heads / kv_heads(pool->cfg)) > max_query_rows(pool->cfg))
+        return CA_ERR_UNSUPPORTED;
     if (q_len == 1) flags &= ~CA_SCHED_CAUSAL;       // one query token sees its whole context
     return guard([&] {
         ca_sched* s = *inout;

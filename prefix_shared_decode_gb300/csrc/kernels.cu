@@ -42,7 +42,10 @@ namespace dev {
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kMaxStages = 8;
-constexpr int kQRows = 64;                 // queries per chunk-first unit, max
+constexpr int kQRows = 64;                 // query rows per tensor-core unit, max (D <= 128)
+// Query rows of the Q tile: 32 at head_dim 256 (the tile stays 16 KiB).
+template <int D>
+__host__ __device__ constexpr int q_rows() { return D == 256 ? 32 : kQRows; }
 constexpr int kRing = 16;                  // unit announcements (producer -> consumers)
 constexpr unsigned kFull = 0xffffffffu;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
@@ -147,6 +150,43 @@ __device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     return r;
 }
+// A lane's DPL consecutive values: fp16 loads as packed pairs, fp32 loads and
+// stores (DPL = 2, 4 or 8).
+template <int DPL>
+__device__ __forceinline__ void ld_h(const void* src, uint32_t (&w)[DPL / 2]) {
+    if constexpr (DPL == 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src);
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    } else if constexpr (DPL == 4) {
+        const uint2 v = *reinterpret_cast<const uint2*>(src);
+        w[0] = v.x; w[1] = v.y;
+    } else {
+        w[0] = *reinterpret_cast<const uint32_t*>(src);
+    }
+}
+template <int DPL>
+__device__ __forceinline__ void ldcg_f(const float* src, float (&v)[DPL]) {
+    if constexpr (DPL >= 4) {
+#pragma unroll
+        for (int i = 0; i < DPL; i += 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(src + i));
+            v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
+        }
+    } else {
+        const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+        v[0] = x.x; v[1] = x.y;
+    }
+}
+template <int DPL>
+__device__ __forceinline__ void st_f(float* dst, const float (&v)[DPL]) {
+    if constexpr (DPL >= 4) {
+#pragma unroll
+        for (int i = 0; i < DPL; i += 4)
+            *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    } else {
+        *reinterpret_cast<float2*>(dst) = make_float2(v[0], v[1]);
+    }
+}
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -206,14 +246,7 @@ __global__ void __launch_bounds__(128) merge_partials_kernel(const AttnParams p,
         float o[KB][DPL];
 #pragma unroll
         for (int k = 0; k < KB; ++k) {
-            const float* po = p.part_o + (size_t)(a + j + min(k, cnt - 1)) * D + lane * DPL;
-            if constexpr (DPL == 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(po));
-                o[k][0] = v.x; o[k][1] = v.y; o[k][2] = v.z; o[k][3] = v.w;
-            } else {
-                const float2 v = __ldcg(reinterpret_cast<const float2*>(po));
-                o[k][0] = v.x; o[k][1] = v.y;
-            }
+            ldcg_f<DPL>(p.part_o + (size_t)(a + j + min(k, cnt - 1)) * D + lane * DPL, o[k]);
         }
         float mk[KB], sk[KB], mg = M;
 #pragma unroll
@@ -238,13 +271,15 @@ __global__ void __launch_bounds__(128) merge_partials_kernel(const AttnParams p,
     }
     const float inv = p.out_scale / S;          // an fp8 pool's value scale, else 1
     uint16_t* dst = p.out + ((size_t)row * p.n_heads + gw % p.n_heads) * D + lane * DPL;
-    if constexpr (DPL == 4) {
-        uint2 v;
-        v.x = pack_half2(acc[0] * inv, acc[1] * inv);
-        v.y = pack_half2(acc[2] * inv, acc[3] * inv);
-        *reinterpret_cast<uint2*>(dst) = v;
+    uint32_t h[DPL / 2];
+#pragma unroll
+    for (int i = 0; i < DPL / 2; ++i) h[i] = pack_half2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+    if constexpr (DPL == 8) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(h[0], h[1], h[2], h[3]);
+    } else if constexpr (DPL == 4) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(h[0], h[1]);
     } else {
-        *reinterpret_cast<uint32_t*>(dst) = pack_half2(acc[0] * inv, acc[1] * inv);
+        *reinterpret_cast<uint32_t*>(dst) = h[0];
     }
 }
 
@@ -275,6 +310,16 @@ __device__ __forceinline__ void sf_chunk(const uint8_t* kt, const uint8_t* vt, i
             const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
             const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
             part[t] = q[0] * a.x + q[1] * a.y + q[2] * b.x + q[3] * b.y;
+        } else if constexpr (DPL == 8) {
+            uint32_t raw[4];
+            ld_h<8>(src, raw);
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw[i]));
+                acc += q[2 * i] * a.x + q[2 * i + 1] * a.y;
+            }
+            part[t] = acc;
         } else if constexpr (DPL == 4) {
             const uint2 raw = *reinterpret_cast<const uint2*>(src);
             const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
@@ -328,6 +373,15 @@ __device__ __forceinline__ void sf_chunk(const uint8_t* kt, const uint8_t* vt, i
             const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
             const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
             o[0] += pt * a.x; o[1] += pt * a.y; o[2] += pt * b.x; o[3] += pt * b.y;
+        } else if constexpr (DPL == 8) {
+            uint32_t raw[4];
+            ld_h<8>(src, raw);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw[i]));
+                o[2 * i] += pt * a.x;
+                o[2 * i + 1] += pt * a.y;
+            }
         } else if constexpr (DPL == 4) {
             const uint2 raw = *reinterpret_cast<const uint2*>(src);
             const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
@@ -347,24 +401,20 @@ __device__ __forceinline__ void sf_chunk(const uint8_t* kt, const uint8_t* vt, i
 // takes tokens [tok0, tok0 + NT) of the chunk.  Row state per thread: rows
 // g = lane/4 and g + 8 of the block.
 // ---------------------------------------------------------------------------
+// Scores of a 16-row block against NT tokens [tok0, tok0 + NT) of a chunk
+// tile, over the head dims [16 kk0, 16 kk1): S = Q K^T with the Q fragments
+// read from the swizzled Q tile (row lane%16, 16-byte chunk 2kk + lane/16).
 template <int C, int D, int NT>
-__device__ __forceinline__ void cf_chunk(uint32_t kt, uint32_t vt, int ntok, int tok0, int ctx0, int lim0,
-                                         int lim1,
-                                         uint32_t qrow_addr_base, float scale_log2,
-                                         float (&m)[2], float (&s)[2], float (&o)[D / 8][4],
-                                         int lane) {
-    float sacc[NT / 8][4];
+__device__ __forceinline__ void cf_scores(uint32_t kt, int tok0, uint32_t qrow_addr_base, int kk0, int kk1,
+                                          float (&sacc)[NT / 8][4], int lane) {
 #pragma unroll
     for (int i = 0; i < NT / 8; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
-    // S = Q K^T over the D dims, 16 at a time.
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        // A fragment of the query block for dims [16 kk, 16 kk + 16), read from
-        // the swizzled Q tile (row rb*16 + lane%16, 16-byte chunk 2kk + lane/16).
+    for (int kk = kk0; kk < kk1; ++kk) {
         uint32_t qa[4];
         {
             const int qr = (lane & 15), qc = 2 * kk + (lane >> 4);
-            ldsm_x4(qrow_addr_base + swz(qr, qc, kQRows), qa[0], qa[1], qa[2], qa[3]);
+            ldsm_x4(qrow_addr_base + swz(qr, qc, q_rows<D>()), qa[0], qa[1], qa[2], qa[3]);
         }
 #pragma unroll
         for (int np = 0; np < NT / 16; ++np) {
@@ -376,7 +426,15 @@ __device__ __forceinline__ void cf_chunk(uint32_t kt, uint32_t vt, int ntok, int
             mma16816(sacc[2 * np + 1], qa, b2, b3);
         }
     }
-    // Online softmax per row (log2 units); columns past ntok are masked.
+}
+
+// Online softmax of a scored 16-row block (log2 units; columns past ntok,
+// and under the causal mask past each row's limit, are masked), then
+// O += P V for the OD output dims [16 dp0, 16 dp0 + OD).
+template <int C, int NT, int OD>
+__device__ __forceinline__ void cf_softmax_pv(uint32_t vt, int ntok, int tok0, int ctx0, int lim0, int lim1,
+                                              float scale_log2, float (&sacc)[NT / 8][4], int dp0,
+                                              float (&m)[2], float (&s)[2], float (&o)[OD / 8][4], int lane) {
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int nt = 0; nt < NT / 8; ++nt) {
@@ -414,23 +472,58 @@ __device__ __forceinline__ void cf_chunk(uint32_t kt, uint32_t vt, int ntok, int
         pa[nt >> 1][(nt & 1) * 2 + 1] = pack_half2(p2, p3);
     }
 #pragma unroll
-    for (int dt = 0; dt < D / 8; ++dt) {
+    for (int dt = 0; dt < OD / 8; ++dt) {
         o[dt][0] *= alpha[0]; o[dt][1] *= alpha[0];
         o[dt][2] *= alpha[1]; o[dt][3] *= alpha[1];
     }
-    // O += P V over this warp's NT tokens.
 #pragma unroll
     for (int j = 0; j < NT / 16; ++j) {
 #pragma unroll
-        for (int dp = 0; dp < D / 16; ++dp) {
+        for (int dq = 0; dq < OD / 16; ++dq) {
             const int tok = tok0 + 16 * j + (lane & 7) + (((lane >> 3) & 1) << 3);
-            const int kc = 2 * dp + (lane >> 4);
+            const int kc = 2 * (dp0 + dq) + (lane >> 4);
             uint32_t b0, b1, b2, b3;
             ldsm_x4_t(vt + swz(tok, kc, C), b0, b1, b2, b3);
-            mma16816(o[2 * dp], pa[j], b0, b1);
-            mma16816(o[2 * dp + 1], pa[j], b2, b3);
+            mma16816(o[2 * dq], pa[j], b0, b1);
+            mma16816(o[2 * dq + 1], pa[j], b2, b3);
         }
     }
+}
+
+// One warp, one 16-row block, NT tokens, every head dim.
+template <int C, int D, int NT>
+__device__ __forceinline__ void cf_chunk(uint32_t kt, uint32_t vt, int ntok, int tok0, int ctx0, int lim0,
+                                         int lim1, uint32_t qrow_addr_base, float scale_log2,
+                                         float (&m)[2], float (&s)[2], float (&o)[D / 8][4], int lane) {
+    float sacc[NT / 8][4];
+    cf_scores<C, D, NT>(kt, tok0, qrow_addr_base, 0, D / 16, sacc, lane);
+    cf_softmax_pv<C, NT, D>(vt, ntok, tok0, ctx0, lim0, lim1, scale_log2, sacc, 0, m, s, o, lane);
+}
+
+// head_dim 256: two warps share a 16-row block, warp `half` owning head dims
+// [128 half, 128 half + 128) (128 fp32 accumulators per thread for all 256
+// would not fit the register budget).  Each scores the block over its dims,
+// the pair adds the two halves through shared memory (xs_w its own slot,
+// xs_p the partner's; the slots alternate by chunk parity, so one pair
+// barrier per chunk keeps the next chunk's writes clear of this chunk's
+// reads), both take the same softmax, and each accumulates P V for its dims.
+template <int C, int NT>
+__device__ __forceinline__ void cf_chunk_split(uint32_t kt, uint32_t vt, int ntok, int tok0, int ctx0, int lim0,
+                                               int lim1, uint32_t qrow_addr_base, float scale_log2, int half,
+                                               float* xs_w, const float* xs_p, int bar_id,
+                                               float (&m)[2], float (&s)[2], float (&o)[16][4], int lane) {
+    float sacc[NT / 8][4];
+    cf_scores<C, 256, NT>(kt, tok0, qrow_addr_base, 8 * half, 8 * half + 8, sacc, lane);
+#pragma unroll
+    for (int i = 0; i < NT / 8; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) xs_w[(i * 4 + e) * 32 + lane] = sacc[i][e];
+    asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
+#pragma unroll
+    for (int i = 0; i < NT / 8; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[i][e] += xs_p[(i * 4 + e) * 32 + lane];
+    cf_softmax_pv<C, NT, 128>(vt, ntok, tok0, ctx0, lim0, lim1, scale_log2, sacc, 8 * half, m, s, o, lane);
 }
 
 // An fp8 chunk-head tile (C rows of 128 one-byte dims, 128-byte swizzled as
@@ -460,12 +553,14 @@ struct Smem {
     static constexpr int kTile = C * D * EB;    // one K or V tile of one chunk-head
     static constexpr int kStage = 2 * kTile;    // K then V
     static constexpr int kConvBytes = EB == 1 ? 2 * C * D * 2 : 0;
-    static constexpr int kQBytes = kQRows * D * 2;
+    static constexpr int kQBytes = q_rows<D>() * D * 2;
+    // head_dim 256: score halves exchanged by warp pairs, two chunk parities
+    static constexpr int kXsBytes = D == 256 ? 2 * kConsumerWarps * (C / 8) * 4 * 32 * 4 : 0;
     static constexpr int kXmsBytes = 512;
     static constexpr int kBarBytes = 2 * kMaxStages * 8;
     static constexpr int kRingBytes = kRing * 4 + 2 * kMaxStages * 4;   // ids, then ntok and tok0 per stage
     static size_t bytes(int stages) {
-        return (size_t)stages * kStage + kConvBytes + kQBytes + kXmsBytes + kBarBytes + kRingBytes;
+        return (size_t)stages * kStage + kConvBytes + kXsBytes + kQBytes + kXmsBytes + kBarBytes + kRingBytes;
     }
 };
 
@@ -482,7 +577,8 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
     const int S = p.n_stages;
     uint8_t* stages = smem;
     uint8_t* conv = smem + (size_t)S * SM::kStage;       // fp8 pools: fp16 copy of one stage
-    uint8_t* qreg = conv + SM::kConvBytes;
+    float* xs = reinterpret_cast<float*>(conv + SM::kConvBytes);   // head_dim 256 score exchange
+    uint8_t* qreg = conv + SM::kConvBytes + SM::kXsBytes;
     float* xms = reinterpret_cast<float*>(qreg + SM::kQBytes);
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xms) + SM::kXmsBytes);
     volatile int32_t* ring = reinterpret_cast<volatile int32_t*>(bars + 2 * kMaxStages);
@@ -662,19 +758,24 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
         return lane < kUnitInts ? reinterpret_cast<const int32_t*>(p.units + u)[lane] : 0;
     };
     auto fld = [&](int32_t d, int i) -> int32_t { return __shfl_sync(kFull, d, i); };
-    auto load_q = [&](int qrow, int head) -> uint2 {
+    auto load_q = [&](int qrow, int head) -> uint4 {
         const uint16_t* qp = p.q + ((size_t)qrow * H + head) * D + lane * DPL;
-        if constexpr (DPL == 4) return *reinterpret_cast<const uint2*>(qp);
-        else return make_uint2(*reinterpret_cast<const uint32_t*>(qp), 0u);
+        if constexpr (DPL == 8) return *reinterpret_cast<const uint4*>(qp);
+        else if constexpr (DPL == 4) {
+            const uint2 v = *reinterpret_cast<const uint2*>(qp);
+            return make_uint4(v.x, v.y, 0u, 0u);
+        } else {
+            return make_uint4(*reinterpret_cast<const uint32_t*>(qp), 0u, 0u, 0u);
+        }
     };
-    uint2 qn = make_uint2(0u, 0u);        // prefetched query row ...
+    uint4 qn = make_uint4(0u, 0u, 0u, 0u);   // prefetched query row ...
     int qn_row = -1, qn_head = -1;        // ... and which (row, head) it is
     auto prefetch_q = [&](int qrow, int head) {
         qn = load_q(qrow, head);
         qn_row = qrow;
         qn_head = head;
     };
-    auto take_q = [&](int qrow, int head) -> uint2 {
+    auto take_q = [&](int qrow, int head) -> uint4 {
         return (qrow == qn_row && head == qn_head) ? qn : load_q(qrow, head);
     };
     // Unit ids come from the ring (the producer writes each before the
@@ -707,16 +808,17 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
             int L = fld(dc, F_CB), h = fld(dc, F_HEAD), part = fld(dc, F_PART);
             while (L < c_end) {                   // one head's piece at a time
                 const int seg_end = min(c_end, (h + 1) * n);
-                const uint2 qraw = take_q(qrow, h);
+                const uint4 qraw = take_q(qrow, h);
                 if (seg_end < c_end) prefetch_q(qrow, h + 1);
                 else if (next_sf) prefetch_q(fld(d0, F_QROW), fld(d0, F_HEAD));
                 float q[DPL], o[DPL], m = -INFINITY, s = 0.f;
                 {
-                    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&qraw.x));
-                    q[0] = a.x; q[1] = a.y;
-                    if constexpr (DPL == 4) {
-                        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&qraw.y));
-                        q[2] = b.x; q[3] = b.y;
+                    const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w};
+#pragma unroll
+                    for (int i = 0; i < DPL / 2; ++i) {
+                        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&qw[i]));
+                        q[2 * i] = a.x;
+                        q[2 * i + 1] = a.y;
                     }
 #pragma unroll
                     for (int d = 0; d < DPL; ++d) { q[d] *= p.scale_log2; o[d] = 0.f; }
@@ -758,12 +860,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                         for (int d = 0; d < DPL; ++d) acc[d] += wt * xo[v * D + lane * DPL + d];
                     }
                     const int pid = p.pbase[pos * H + h] + part;
-                    float* dst = p.part_o + (size_t)pid * D + lane * DPL;
-                    if constexpr (DPL == 4) {
-                        *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                    } else {
-                        *reinterpret_cast<float2*>(dst) = make_float2(acc[0], acc[1]);
-                    }
+                    st_f<DPL>(p.part_o + (size_t)pid * D + lane * DPL, acc);
                     if (lane == 0) p.part_ms[pid] = make_float2(M, sum);
                 }
                 ++flush;
@@ -790,9 +887,13 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
             if (next_sf) prefetch_q(fld(d0, F_QROW), fld(d0, F_HEAD));
             const int m_rows = (q_hi - q_lo) * RW;
             const int rblocks = m_rows <= 16 ? 1 : m_rows <= 32 ? 2 : 4;
-            int T = kConsumerWarps / rblocks;   // warps splitting a chunk's tokens
+            // head_dim 256: warp pairs split the head dims (at most 32 rows)
+            constexpr bool kSplit = D == 256;
+            constexpr int OD = kSplit ? 128 : D;          // output dims per warp
+            int T = kSplit ? 1 : kConsumerWarps / rblocks;   // warps splitting a chunk's tokens
             if (T * 16 > C) T = C / 16;
-            const int rb = w / T, tp = w % T;
+            const int rb = kSplit ? (w >> 1) : w / T, tp = kSplit ? 0 : w % T;
+            const int dhalf = kSplit ? (w & 1) : 0;
             const bool active = rb < rblocks && rb * 16 < m_rows;
             // Causal mask: the last context token each of this thread's two
             // rows (rb*16 + lane/4 and 8 below) may see; the rows are the same
@@ -818,13 +919,13 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     const int r = idx / (D / 8), k = idx % (D / 8);
                     const size_t qrow_tok = (size_t)p.seq_perm[q_lo + r / RW] * QL + (r % RW) / G;
                     const uint16_t* src = p.q + (qrow_tok * H + kvh * G + r % G) * D + k * 8;
-                    cp_async16(smem_u32(qreg + swz(r, k, kQRows)), src);
+                    cp_async16(smem_u32(qreg + swz(r, k, q_rows<D>())), src);
                 }
                 cp_async_wait_all();
                 consumer_sync();
-                float o[D / 8][4], m[2] = {-INFINITY, -INFINITY}, s[2] = {0.f, 0.f};
+                float o[OD / 8][4], m[2] = {-INFINITY, -INFINITY}, s[2] = {0.f, 0.f};
 #pragma unroll
-                for (int dt = 0; dt < D / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+                for (int dt = 0; dt < OD / 8; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
                 // Row block rb starts at a multiple of 8 rows, so its swizzle
                 // pattern is the tile's shifted by rb * 16 rows of 128 bytes.
                 const uint32_t qblock = smem_u32(qreg) + rb * 16 * 128;
@@ -851,7 +952,15 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                         kt = smem_u32(conv);
                         vt = kt + SM::kConvBytes / 2;
                     }
-                    if (active) {
+                    if constexpr (kSplit) {
+                        if (active) {
+                            constexpr int kXs = (C / 8) * 4 * 32;     // floats per warp slot
+                            float* xw = xs + ((it & 1) * kConsumerWarps + w) * kXs;
+                            const float* xp = xs + ((it & 1) * kConsumerWarps + (w ^ 1)) * kXs;
+                            cf_chunk_split<C, C>(kt, vt, ntok, 0, ctx0, lim[0], lim[1], qblock, p.scale_log2,
+                                                 dhalf, xw, xp, 2 + rb, m, s, o, lane);
+                        }
+                    } else if (active) {
                         if (NTw == 16) {
                             cf_chunk<C, D, 16>(kt, vt, ntok, tp * 16, ctx0, lim[0], lim[1], qblock, p.scale_log2,
                                                m, s, o, lane);
@@ -884,7 +993,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     if (writer) {
                         float* dst = xo + (size_t)slot * (16 * D);
 #pragma unroll
-                        for (int dt = 0; dt < D / 8; ++dt)
+                        for (int dt = 0; dt < OD / 8; ++dt)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) dst[(dt * 4 + e) * 32 + lane] = o[dt][e];
                         if ((lane & 3) == 0) {
@@ -910,7 +1019,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                             s[r] = s[r] * a1 + s2 * a2;
                             m[r] = M;
 #pragma unroll
-                            for (int dt = 0; dt < D / 8; ++dt) {
+                            for (int dt = 0; dt < OD / 8; ++dt) {
                                 o[dt][2 * r] = o[dt][2 * r] * a1 + so[(dt * 4 + 2 * r) * 32 + lane] * a2;
                                 o[dt][2 * r + 1] =
                                     o[dt][2 * r + 1] * a1 + so[(dt * 4 + 2 * r + 1) * 32 + lane] * a2;
@@ -918,7 +1027,8 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                         }
                     }
                 }
-                // Warps with tp == 0 now hold their row block: write one partial
+                // Warps with tp == 0 now hold their row block (at head_dim 256,
+                // each warp of a pair its half of the dims): write one partial
                 // per valid row.
                 if (active && tp == 0) {
                     const int g = lane >> 2, t4 = lane & 3;
@@ -928,12 +1038,12 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                         if (row < m_rows) {
                             const int pos = q_lo + row / RW, jq = (row % RW) / G, qh = kvh * G + row % G;
                             const int pid = p.pbase[((size_t)pos * QL + jq) * H + qh] + upart;
-                            float* dst = p.part_o + (size_t)pid * D;
+                            float* dst = p.part_o + (size_t)pid * D + dhalf * OD;
 #pragma unroll
-                            for (int dt = 0; dt < D / 8; ++dt)
+                            for (int dt = 0; dt < OD / 8; ++dt)
                                 *reinterpret_cast<float2*>(dst + dt * 8 + 2 * t4) =
                                     make_float2(o[dt][2 * r], o[dt][2 * r + 1]);
-                            if (t4 == 0) p.part_ms[pid] = make_float2(m[r], s[r]);
+                            if (t4 == 0 && dhalf == 0) p.part_ms[pid] = make_float2(m[r], s[r]);
                         }
                     }
                 }
@@ -1024,6 +1134,9 @@ void* pick_kernel(const ca_pool_config& c) {
         if (c.chunk == 64) return kernel_ptr<64, 128, 1>();
         if (c.chunk == 32) return kernel_ptr<32, 128, 1>();
         if (c.chunk == 16) return kernel_ptr<16, 128, 1>();
+    } else if (c.head_dim == 256) {                 // chunks of 16 or 32 tokens
+        if (c.chunk == 32) return kernel_ptr<32, 256, 2>();
+        if (c.chunk == 16) return kernel_ptr<16, 256, 2>();
     } else if (c.head_dim == 128) {
         if (c.chunk == 64) return kernel_ptr<64, 128, 2>();
         if (c.chunk == 32) return kernel_ptr<32, 128, 2>();
@@ -1039,7 +1152,9 @@ void* pick_kernel(const ca_pool_config& c) {
 size_t smem_for(const ca_pool_config& c, int stages) {
     const size_t eb = (size_t)kv_elem_bytes(c), cd = (size_t)c.chunk * c.head_dim;
     const size_t conv = eb == 1 ? 2 * cd * 2 : 0;
-    return (size_t)stages * 2 * cd * eb + conv + (size_t)dev::kQRows * c.head_dim * 2 + 512 +
+    const size_t qrows = c.head_dim == 256 ? 32 : dev::kQRows;
+    const size_t xs = c.head_dim == 256 ? (size_t)2 * dev::kConsumerWarps * (c.chunk / 8) * 4 * 32 * 4 : 0;
+    return (size_t)stages * 2 * cd * eb + conv + xs + qrows * c.head_dim * 2 + 512 +
            2 * dev::kMaxStages * 8 + 4 * dev::kRing + 2 * 4 * dev::kMaxStages;
 }
 }  // namespace
@@ -1174,7 +1289,9 @@ int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void*
     lc.stream = cs;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    if (p.cfg.head_dim == 128)
+    if (p.cfg.head_dim == 256)
+        e = cudaLaunchKernelEx(&lc, dev::merge_partials_kernel<256>, a, n_pairs);
+    else if (p.cfg.head_dim == 128)
         e = cudaLaunchKernelEx(&lc, dev::merge_partials_kernel<128>, a, n_pairs);
     else
         e = cudaLaunchKernelEx(&lc, dev::merge_partials_kernel<64>, a, n_pairs);

@@ -186,7 +186,7 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
 namespace {
 constexpr double kCfComputePer16 = 0.2;
 constexpr double kF8CfFactor = 1.6;         // fp8 pools, fitted to measured per-tile times
-constexpr int32_t kMaxCfQueries = 64;
+
 // Share of the sequence-first tiles left to the tail queue that CTAs drain
 // dynamically once their static lists are done (absorbs the run-to-run rate
 // differences between SMs), and the size of a queued unit in chunk-heads.
@@ -236,7 +236,7 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, int32_t q_len, Pla
     double cf_total = 0;
     for (int32_t u = 0; u < U; ++u) {
         const int32_t nrows = t.cf_runs[4 * u + 1], m = t.cf_runs[4 * u + 3] - t.cf_runs[4 * u + 2];
-        const int32_t max_pos = std::max(1, kMaxCfQueries / RW);
+        const int32_t max_pos = std::max(1, max_query_rows(p.cfg) / RW);
         const int32_t ngroups = (m + max_pos - 1) / max_pos;
         cf_total += (double)nrows * H * ngroups * rows_cost((m + ngroups - 1) / ngroups * RW);
     }
@@ -255,8 +255,8 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, int32_t q_len, Pla
     for (int32_t u = 0; u < U; ++u) {
         const int32_t row0 = t.cf_runs[4 * u], nrows = t.cf_runs[4 * u + 1];
         const int32_t lo = t.cf_runs[4 * u + 2], hi = t.cf_runs[4 * u + 3], m = hi - lo;
-        // query groups of at most 64 (position, query token, query head) rows
-        const int32_t max_pos = std::max(1, kMaxCfQueries / RW);
+        // query groups of at most 64 (32 at head_dim 256) (position, query token, query head) rows
+        const int32_t max_pos = std::max(1, max_query_rows(p.cfg) / RW);
         const int32_t ngroups = (m + max_pos - 1) / max_pos;
         const int32_t mg = (m + ngroups - 1) / ngroups;
         const double row_cost = rows_cost(mg * RW);

@@ -151,6 +151,21 @@ def test_kernel_launch_counter_on_host_only_pools(lib):
     assert lib.ca_kernel_launches(None) == -1            # CA_ERR_INVALID
 
 
+def test_head_dim_256_shape_limits(lib):
+    from prefix_shared_decode_gb300 import CAError, Pool
+    for chunk, kv in ((64, "fp16"), (32, "fp8")):
+        with pytest.raises(CAError) as e:
+            Pool(1, 2, 256, chunk, 10, host_only=True, kv_dtype=kv)
+        assert e.value.name == "CA_ERR_UNSUPPORTED"
+    pool = Pool(1, 8, 256, 32, 20, host_only=True, n_kv_heads=1)       # G = 8
+    pool.insert(0, list(range(40)))
+    with pytest.raises(CAError) as e:
+        pool.schedule([0], q_len=5)                                     # 5 * 8 rows > 32
+    assert e.value.name == "CA_ERR_UNSUPPORTED"
+    plan = pool.schedule([0], q_len=4).plan()                           # 32 rows: fine
+    assert len(plan["pbase"]) == 4 * 8 + 1
+
+
 def test_errors_and_rollback(lib):
     from prefix_shared_decode_gb300 import CAError, Pool
     pool = Pool(1, 2, 64, 16, 5, host_only=True)

@@ -276,6 +276,39 @@ def test_speculative_verification_over_appended_drafts(torch_cuda):
                      f"step {step}")
 
 
+@pytest.mark.parametrize("c,G,q_len,causal", [(16, 1, 1, False), (32, 1, 1, False), (32, 4, 1, False),
+                                              (16, 2, 4, True), (32, 1, 8, True)])
+def test_head_dim_256_every_output(torch_cuda, c, G, q_len, causal):
+    """head_dim 256 (chunks of 16 or 32): the sequence-first lanes own 8 dims;
+    on the tensor cores warp pairs split the head dims and add their score
+    halves through shared memory."""
+    from prefix_shared_decode_gb300 import Pool, decode_attention
+    torch = torch_cuda
+    Hkv, D, L = 2, 256, 2
+    rng = np.random.default_rng(100 + c + G + q_len)
+    seqs = random_segment_sequences(100 + c + q_len, 12, c, n_segments=10)
+    pool = Pool(L, Hkv * G, D, c, 900, n_kv_heads=Hkv)
+    trie = OracleTrie(c, 900)
+    for i, toks in enumerate(seqs):
+        k = rng.standard_normal((L, len(toks), Hkv, D), dtype=np.float32).astype(np.float16)
+        v = rng.standard_normal((L, len(toks), Hkv, D), dtype=np.float32).astype(np.float16)
+        trie.insert(i, toks, k, v)
+        pool.insert(i, toks, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+    batch = [int(x) for x in rng.permutation(12) if len(seqs[x]) >= q_len][:10]
+    shape = (len(batch), Hkv * G, D) if q_len == 1 else (len(batch), q_len, Hkv * G, D)
+    q = rng.standard_normal(shape, dtype=np.float32).astype(np.float16)
+    for layer in range(L):
+        if q_len == 1:
+            want = A.decode_attention(trie, batch, layer, q, 1 / np.sqrt(D))
+        else:
+            want = A.decode_attention_multi(trie, batch, layer, q, 1 / np.sqrt(D), causal)
+        for no_tpp in (False, True):
+            sched = pool.schedule(batch, no_tpp=no_tpp, q_len=q_len, causal=causal)
+            got = decode_attention(pool, sched, torch.from_numpy(q).cuda(), layer=layer).cpu().numpy()
+            assert sched.device_status() == 0
+            assert_close(got, want, f"D=256 c={c} G={G} q_len={q_len} layer={layer} no_tpp={no_tpp}")
+
+
 def test_edge_cases(torch_cuda):
     """One-token contexts, exactly one chunk, one chunk plus one token,
     identical sequences (no sequence-first work at all), a batch of one."""
@@ -495,7 +528,8 @@ SAMPLE = 4
 
 @pytest.mark.parametrize("name", ["llama7b_p1024", "sweep_s2048_b32", "sweep_s2048_b64",
                                   "sweep_s4096_b32", "sweep_s4096_b64", "no_sharing", "gqa_p1024",
-                                  "llama7b_p1024_fp8", "sweep_s4096_b64_fp8", "llama7b_p1024_q4"])
+                                  "llama7b_p1024_fp8", "sweep_s4096_b64_fp8", "llama7b_p1024_q4",
+                                  "d256_p1024"])
 def test_full_size_workloads_sampled(torch_cuda, name):
     """The benchmark's launch configuration at full size; every output is
     finite and SAMPLE sequences (all heads) match the oracle."""

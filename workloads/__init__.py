@@ -200,6 +200,8 @@ def make(name: str) -> Workload:
     llama7b_p1024_fp8, sweep_s4096_b64_fp8
                     those trees (same seeds) in a pool that stores K/V as FP8
                     E4M3 with scales 1 (the inputs stay fp16 N(0, 1)).
+    d256_p1024      head_dim 256: 16 heads, chunk 32, llama7b_p1024's tree
+                    shape (same KV bytes per token); seed 9.
     llama7b_p1024_q4
                     llama7b_p1024 with 4 query tokens per sequence (draft
                     tokens being verified): causal, token j sees the context
@@ -232,6 +234,10 @@ def make(name: str) -> Workload:
                               description="32 heads, D 128, chunk 64; 32 fully private 2048-token contexts")
     if name == "multi_tenant":
         return _multi_tenant(7)
+    if name == "d256_p1024":
+        return _shared_prefix(name, 9, 32, 1024, 512, n_heads=16, head_dim=256, chunk=32,
+                              description="16 heads, D 256, chunk 32 (the same KV bytes per token as 32 x 128); "
+                                          "32 seqs share 1024 tokens, 512 private each")
     if name == "gqa_p1024":
         return _shared_prefix(name, 8, 32, 1024, 512, n_kv_heads=8,
                               description="32 query heads sharing 8 key/value heads (grouped-query, "
@@ -242,4 +248,4 @@ def make(name: str) -> Workload:
 
 ALL = ["tiny", "llama7b_p1024", "sweep_s2048_b32", "sweep_s2048_b64",
        "sweep_s4096_b32", "sweep_s4096_b64", "no_sharing", "multi_tenant", "gqa_p1024",
-       "llama7b_p1024_fp8", "sweep_s4096_b64_fp8", "llama7b_p1024_q4"]
+       "llama7b_p1024_fp8", "sweep_s4096_b64_fp8", "llama7b_p1024_q4", "d256_p1024"]
