@@ -1,0 +1,66 @@
+"""The benchmark's multi-process path on CPU: under torchrun every rank runs
+an independent replica of the step (no collective on the data path); the
+job's times are the slowest rank's (a max-reduction over `gloo` ranks here,
+NCCL on GPUs), and the whole-job time per call divides by the ranks."""
+import io
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    try:
+        q.put((rank, bench.max_over_ranks([1.0 + rank, 10.0 - rank, 0.5 * rank])))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_times_are_the_slowest_ranks_over_two_gloo_ranks():
+    torch = pytest.importorskip("torch")
+    mp = torch.multiprocessing.get_context("spawn")
+    q = mp.Queue()
+    port = _free_port()
+    procs = [mp.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got[0] == got[1] == [2.0, 10.0, 0.5]
+
+
+def test_one_process_and_whole_job_time():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks([3.0, 4.5]) == [3.0, 4.5]          # no process group
+    assert bench.whole_job_per_call(100.0, 4) == 25.0
+    assert bench.whole_job_per_call(100.0, 1) == 100.0
+
+
+def test_reference_arm_prints_on_rank_zero_only(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    args = bench.parse(["--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "1"])
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.run_reference(args)
+    assert buf.getvalue() == ""
