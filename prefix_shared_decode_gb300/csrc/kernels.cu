@@ -1,12 +1,15 @@
-// Device code of libchunk_attention: the two-phase decode attention kernel
-// and the KV scatter used by inserts.  sm_103a (GB300).
+// Device code of libchunk_attention: the two-phase decode attention kernel,
+// its merge kernel, and the KV scatter used by inserts and appends.  sm_103a
+// (GB300).
 //
 // Method: ChunkAttention's two-phase partition ("ChunkAttention: Efficient
 // Self-Attention with Prefix-Aware KV Cache and Two-Phase Partition", §3.2).
 // A shared chunk is multiplied against the batched queries of every sequence
 // holding it (chunk-first, tensor cores); each sequence's own chunks are
 // processed per query (sequence-first, CUDA cores with warp-shuffle
-// reductions); every piece of work leaves a partial triple (o, m, s) that is
+// reductions — or tensor cores too when a position brings several query rows
+// per key/value head: grouped query heads or several query tokens); every
+// piece of work leaves a partial triple (o, m, s) that is
 // combined by the rescaled-sum rule of the explainer blog's "Two-Phase
 // Partition" section.
 //
@@ -15,9 +18,10 @@
 //    of chunk-first and sequence-first units, so the tensor-core work of the
 //    shared chunks overlaps the HBM stream of the private chunks on the same
 //    SMs (two CTAs per SM);
-//  * a producer warp streams every chunk-head tile (c x D fp16, contiguous in
-//    the pool) into a ring of shared-memory stages with 2-D TMA loads,
-//    128-byte swizzled, completing on mbarriers; four consumer warps compute;
+//  * a producer warp streams every chunk-head tile (c x D, fp16 or E4M3,
+//    contiguous in the pool) into a ring of shared-memory stages with 2-D TMA
+//    loads, 128-byte swizzled, completing on mbarriers; four consumer warps
+//    compute (at head_dim 256 in pairs that split the head dims);
 //  * every unit stores its partials with plain stores (no fences, atomics or
 //    waits between units); a small merge kernel, launched as a programmatic
 //    dependent of the main kernel so that its launch overlaps the main
@@ -29,8 +33,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <climits>
 #include <atomic>
+#include <climits>
 #include <cstdio>
 #include <cstring>
 
@@ -198,14 +202,14 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
 }
 
 // Byte offset of 16-byte column chunk k of row r inside a tile stored as
-// D/64 boxes of `rows` x 128 B, each 128-byte swizzled (TMA SWIZZLE_128B:
-// chunk index XOR row mod 8).
+// boxes of `rows` x 128 B (a row's bytes split 128 at a time), each 128-byte
+// swizzled (TMA SWIZZLE_128B: chunk index XOR row mod 8).
 __device__ __forceinline__ uint32_t swz(int r, int k, int rows) {
     return (uint32_t)((k >> 3) * rows * 128 + r * 128 + (((k & 7) ^ (r & 7)) << 4));
 }
 
 // ---------------------------------------------------------------------------
-// Merge kernel: all partials of one (position, head) combined by the
+// Merge kernel: all partials of one (position, query token, head) combined by the
 // explainer's output-combination rule, m* = max m_j,
 // out = sum 2^{m_j-m*} o_j / sum 2^{m_j-m*} s_j (m in log2 units), taken a
 // few partials at a time with the running maximum rescaled as it grows.  One
@@ -396,10 +400,11 @@ __device__ __forceinline__ void sf_chunk(const uint8_t* kt, const uint8_t* vt, i
 }
 
 // ---------------------------------------------------------------------------
-// Chunk-first: one chunk-head tile against up to 16 batched queries (one m16
-// row block) with mma.sync m16n8k16 (fp16 in, fp32 accumulate).  The warp
-// takes tokens [tok0, tok0 + NT) of the chunk.  Row state per thread: rows
-// g = lane/4 and g + 8 of the block.
+// Tensor-core path (chunk-first units, and sequence-first units with several
+// query rows): one chunk-head tile against a 16-row block of the Q tile with
+// mma.sync m16n8k16 (fp16 in, fp32 accumulate).  The warp takes tokens
+// [tok0, tok0 + NT) of the chunk.  Row state per thread: rows g = lane/4 and
+// g + 8 of the block.
 // ---------------------------------------------------------------------------
 // Scores of a 16-row block against NT tokens [tok0, tok0 + NT) of a chunk
 // tile, over the head dims [16 kk0, 16 kk1): S = Q K^T with the Q fragments

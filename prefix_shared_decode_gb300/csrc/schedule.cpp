@@ -12,9 +12,10 @@
 //  * merge lists: the runs covering each position.
 //
 // Plan (GB300-specific, verified through the outputs): chunk-first runs are
-// cut into units of at most 64 queries and a balanced number of chunks;
-// sequence-first chunk-heads are spread over the CTAs in contiguous pieces so
-// that every CTA gets the same estimated time.
+// cut into units of at most 64 query rows (32 at head_dim 256) and a balanced
+// number of chunks; sequence-first chunk-heads are spread over the CTAs in
+// contiguous pieces so that every CTA gets the same estimated time, with a
+// tail of small units that CTAs claim dynamically.
 #include <algorithm>
 #include <cstring>
 #include <numeric>
@@ -179,9 +180,10 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
 // ---------------------------------------------------------------------------
 // Work plan.
 // Cost model, in "chunk-head tiles" (one chunk of one head, K and V): a
-// sequence-first tile costs 1 (HBM-bound); a chunk-first tile for m queries
-// costs 1 + kCfComputePer16 * ceil(m / 16) (tensor-core work grows with m;
-// the coefficient is fitted to measured per-chunk unit times on GB300).
+// sequence-first tile of one query row costs 1 (HBM-bound); a tile on the
+// tensor cores for m query rows costs 1 + kCfComputePer16 * ceil(m / 16)
+// (tensor-core work grows with m), relative to the sequence-first tiles'
+// own cost; the coefficients are fitted to traced unit times on GB300.
 // ---------------------------------------------------------------------------
 namespace {
 constexpr double kCfComputePer16 = 0.2;
