@@ -171,11 +171,21 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def source_fingerprint(path: str) -> str:
+    """sha256[:16] of a C++/CUDA source with comments and whitespace removed,
+    so that only code changes (not comment edits) change it."""
+    import re
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    text = re.sub(r"\s+", " ", text)
+    return hashlib.sha256(text.encode()).hexdigest()[:16]
+
+
 def kernel_traffic(kernel_name: str):
     """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
-    the current kernel source (null otherwise)."""
-    src = os.path.join(ROOT, "prefix_shared_decode_gb300", "csrc", "kernels.cu")
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    the current kernel code (null otherwise)."""
+    h = source_fingerprint(os.path.join(ROOT, "prefix_shared_decode_gb300", "csrc", "kernels.cu"))
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -184,7 +194,7 @@ def kernel_traffic(kernel_name: str):
     except ValueError:
         return None
     e = d.get(kernel_name)
-    if not e or e.get("kernels_cu_sha256_16") != h:
+    if not e or e.get("kernels_cu_code_sha256_16") != h:
         return None
     return e.get("dram_bytes_per_launch")
 

@@ -33,8 +33,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <atomic>
 #include <climits>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 
