@@ -318,10 +318,12 @@ def run_ours(args):
     # more than twice the L2 (the unique KV of one pool, or of the pool copies
     # the steps rotate through) and every KV load carries an evict-first L2
     # hint, so no flush is needed between steps.  One event pair brackets all K steps; the main
-    # kernel is additionally timed on every 8th step through the library's
-    # event hook (event records between kernels break the programmatic
-    # launch overlap, so they are kept off the other steps).
-    KEV = 8
+    # kernel is additionally timed on every 32nd step through the library's
+    # event hook.  Event records between kernels break the programmatic
+    # launch overlap (the next kernel's early start and its pool prefetch), so
+    # a timed step runs the kernel in isolation and costs a few µs; they are
+    # kept sparse to leave the back-to-back steps undisturbed.
+    KEV = 32
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range((K + KEV - 1) // KEV)]
     for a, z in kev:        # torch creates the CUDA event on first record; the library re-records it
@@ -344,6 +346,7 @@ def run_ours(args):
         step(args.warmup + i)
         if i % KEV == 0:
             scheds[r].set_profile_events(None, None)
+    enqueue = time.perf_counter() - wall0         # host time to issue the K steps
     ev_b.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -459,6 +462,7 @@ def run_ours(args):
         "gpu_launches_source": "library launch counter (ca_kernel_launches) read around the timed loop",
         "clocks": clk,
         "wall_s_timed_loop": round(wall, 3),
+        "host_enqueue_us_per_step": round(enqueue * 1e6 / K, 1),
         "setup_s": round(setup_s, 2),
     }
     if churn:

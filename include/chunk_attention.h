@@ -290,6 +290,12 @@ int ca_workspace_bytes(const ca_sched* sched, size_t* bytes_out);
  *            schedule holds the kernels' work-queue counter).
  * Two kernels run on `stream`: the two-phase kernel and a merge kernel
  * launched as its programmatic dependent (one warp per sequence and head).
+ * Both are programmatic dependents of the work before them on `stream`: they
+ * read q, the workspace and the queue counter only once that work has
+ * completed.  The two-phase kernel starts streaming the pool before then
+ * when no insert or append on this pool was launched since its last
+ * attention call, so the pool's device memory must be written only through
+ * this library's calls.
  * Errors: CA_ERR_STALE if the pool changed after the schedule was built;
  * CA_ERR_INVALID for a host-only pool, bad layer, NULL or misaligned pointers
  * or a small workspace; CA_ERR_CUDA if a launch fails.  Kernel-side faults

@@ -83,6 +83,7 @@ struct AttnParams {
     float scale_log2;            // scale * log2(e) (times the key scale of an fp8 pool)
     float out_scale;             // value scale of an fp8 pool, else 1
     int32_t n_stages;
+    int32_t kv_stable;           // no insert/append wrote the pool since the last call
 };
 
 // Workspace layout for a schedule.
@@ -132,6 +133,10 @@ struct Pool {
     std::vector<int32_t> heap;     // min-heap of free slots
     std::unordered_map<int64_t, Sequence> seqs;
     int64_t generation = 0;
+    // Set when a KV scatter (insert or append) is launched, cleared when an
+    // attention launch reads it: while clear, the pool's device contents are
+    // not written by any kernel the next attention call could overlap.
+    mutable bool kv_written = true;
 };
 
 struct Tables {

@@ -26,6 +26,11 @@
 //    waits between units); a small merge kernel, launched as a programmatic
 //    dependent of the main kernel so that its launch overlaps the main
 //    kernel's tail, combines the partials of each (sequence, head);
+//  * the main kernel is itself a programmatic dependent of the work before
+//    it: its CTAs become resident as the previous grid drains and, when no
+//    insert or append wrote the pool since the last call, start streaming
+//    their static tiles at once, before the dependency wait that guards q,
+//    the workspace and the queue counter;
 //  * every wait is bounded (~1 s) and reports CA_ERR_TIMEOUT instead of
 //    hanging.
 #include <cuda.h>
@@ -628,8 +633,8 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
         // Each unit's id is written to the ring before its first chunk is
         // issued (that chunk's barrier arrival publishes it); after the last
         // unit a stage carries the id -1.  The plan may be read before the
-        // dependency wait; the pool, the queries and the queue counter (reset
-        // by the previous call's merge kernel) only after it.
+        // dependency wait; the queue counter (reset by the previous call's
+        // merge kernel) only after it, and the pool too unless p.kv_stable.
         // Both kinds walk a linear (head, chunk) range: step L covers chunk
         // base + L % n of head L / n.  A chunk-first unit's n is its row count
         // and its range spans its heads.
@@ -641,8 +646,21 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
         };
         auto first_chunk = [&](const Unit& X) { return lin_base(X) + lin_begin(X) % lin_n(X); };
         int s_next = u_begin;
+        // The previous kernel in the stream (normally the previous call's
+        // merge) may still run.  The queue counter it resets is read only after
+        // the dependency wait, and so is the pool unless no insert or append
+        // wrote it since the last call: then this CTA's static tiles stream
+        // at once, overlapping that kernel and the previous grid's tail.
+        bool dep_done = false;
+        auto dep_wait = [&]() {
+            if (!dep_done) {
+                asm volatile("griddepcontrol.wait;" ::: "memory");
+                dep_done = true;
+            }
+        };
         auto claim = [&]() -> int {
             if (s_next < u_end) return s_next++;
+            dep_wait();
             const int k = atomicAdd(p.dyn_counter, 1);
             return (p.dyn_begin + k < p.dyn_end) ? p.dyn_begin + k : -1;
         };
@@ -651,7 +669,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
         ChunkRef chn = (cur >= 0) ? p.chunks[first_chunk(Un)] : ChunkRef{0, 0};
         // context offsets matter only under the causal mask
         int tkn = (cur >= 0 && p.causal) ? p.chunk_tok0[first_chunk(Un)] : 0;
-        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (!p.kv_stable) dep_wait();
         if (cur < 0) {
             cur = claim();
             if (cur >= 0) {
@@ -1229,6 +1247,7 @@ uint64_t kernel_launches() { return g_launches.load(std::memory_order_relaxed); 
 int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_rows,
                    const std::vector<ScatterChunk>& chunks, void* stream) {
     const ca_pool_config& c = p.cfg;
+    p.kv_written = true;
     for (size_t i = 0; i < chunks.size(); i += dev::kScatterMaxChunks) {
         const size_t cnt = std::min<size_t>(dev::kScatterMaxChunks, chunks.size() - i);
         dev::ScatterArgs a;
@@ -1264,6 +1283,11 @@ int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void*
     kernel_smem_bytes(p.cfg, &st, &bytes);   // attribute set at pool creation
     AttnParams a = prm;
     a.n_stages = st;
+    // The kernel may read the pool before its dependency wait only when no
+    // KV scatter was launched since the last attention launch: every kernel
+    // this launch can overlap then leaves the pool alone.
+    a.kv_stable = p.kv_written ? 0 : 1;
+    p.kv_written = false;
     const CUtensorMap* map = reinterpret_cast<const CUtensorMap*>(p.tmap);
     void* args[] = {const_cast<CUtensorMap*>(map), &a};
     cudaStream_t cs = static_cast<cudaStream_t>(stream);

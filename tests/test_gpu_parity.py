@@ -461,6 +461,53 @@ def test_decode_time_appends(torch_cuda):
     assert cached_steps > 20 and rebuilt_steps > 2
 
 
+def test_back_to_back_calls_and_pool_writes(torch_cuda):
+    """Calls issued back to back with no host synchronisation.  While no
+    insert or append has written a pool since its last call, a call streams
+    the pool before the previous kernel in the stream has finished; the first
+    call after an append waits for it.  Calls alternating between two pools,
+    then an append to one of them followed at once by calls on it, all match
+    the oracle (each call against the trie state it was issued on)."""
+    from prefix_shared_decode_gb300 import Pool, decode_attention
+    torch = torch_cuda
+    c, H, D = 32, 4, 128
+    rng = np.random.default_rng(23)
+    seqs = random_segment_sequences(23, 8, c, n_segments=5)
+    pools, tries = [], []
+    for _ in range(2):
+        pool, trie = Pool(1, H, D, c, 600), OracleTrie(c, 600)
+        for i, toks in enumerate(seqs):
+            k = rng.standard_normal((1, len(toks), H, D), dtype=np.float32).astype(np.float16)
+            v = rng.standard_normal((1, len(toks), H, D), dtype=np.float32).astype(np.float16)
+            trie.insert(i, toks, k, v)
+            pool.insert(i, toks, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+        pools.append(pool)
+        tries.append(trie)
+    batch = list(range(8))
+    scheds = [p.schedule(batch) for p in pools]
+    qs = [rng.standard_normal((8, H, D), dtype=np.float32).astype(np.float16) for _ in range(8)]
+    qd = [torch.from_numpy(q).cuda() for q in qs]
+    add = {sid: ([2 * 10**6 + sid], rng.standard_normal((1, 1, H, D), dtype=np.float32).astype(np.float16),
+                 rng.standard_normal((1, 1, H, D), dtype=np.float32).astype(np.float16)) for sid in batch}
+    add_d = {sid: (torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda()) for sid, (_, k, v) in add.items()}
+    torch.cuda.synchronize()
+    outs = [decode_attention(pools[i % 2], scheds[i % 2], qd[i]) for i in range(6)]
+    for sid in batch:                                   # appends, right behind the calls
+        pools[0].append(sid, add[sid][0], *add_d[sid])
+    sched0 = pools[0].schedule(batch, reuse=scheds[0])
+    outs += [decode_attention(pools[0], sched0, qd[i]) for i in (6, 7)]
+    torch.cuda.synchronize()
+    assert scheds[1].device_status() == 0 and sched0.device_status() == 0
+    for i in range(6):
+        want = A.decode_attention(tries[i % 2], batch, 0, qs[i], 1 / np.sqrt(D))
+        assert_close(outs[i].cpu().numpy(), want, f"call {i}")
+    for sid in batch:
+        tries[0].append(sid, *add[sid])
+    for j, i in enumerate((6, 7)):
+        want = A.decode_attention(tries[0], batch, 0, qs[i], 1 / np.sqrt(D))
+        assert_close(outs[6 + j].cpu().numpy(), want, f"call {i} after the append")
+
+
 def test_host_io_entry_and_repeat_calls(torch_cuda):
     from prefix_shared_decode_gb300 import decode_attention, decode_attention_host
     torch = torch_cuda
