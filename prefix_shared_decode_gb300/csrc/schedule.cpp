@@ -194,7 +194,10 @@ constexpr double kF8CfFactor = 1.6;         // fp8 pools, fitted to measured per
 // differences between SMs), and the size of a queued unit in chunk-heads.
 constexpr double kTailShare = 0.12;
 constexpr int32_t kTailUnitsPerCta = 2;     // aim: about this many queue units per CTA
-constexpr int32_t kTailUnitMin = 2, kTailUnitMax = 8;
+// At least four chunk-heads per queued unit: every unit pays a fixed cost
+// (its claim, query load, partial writes and one more partial to merge),
+// which two-tile units did not amortise (measured: 2% slower calls).
+constexpr int32_t kTailUnitMin = 4, kTailUnitMax = 8;
 }  // namespace
 
 void build_plan(const Pool& p, const Tables& t, int32_t grid, int32_t q_len, Plan& plan) {
