@@ -405,6 +405,88 @@ __device__ __forceinline__ void sf_chunk(const uint8_t* kt, const uint8_t* vt, i
 }
 
 // ---------------------------------------------------------------------------
+// Sequence-first on an fp8 pool with 64-token chunks: the same product on
+// the tensor cores.  One query row against a chunk-head tile is a matrix-
+// vector product, but on CUDA cores the E4M3 widening and the cross-lane
+// reductions made this path issue-bound (half the issue slots busy, HBM at
+// half its rate), so warp w multiplies its 16 tokens [16w, 16w + 16) with
+// mma.sync m16n8k16, the query replicated over the 8 columns, and the bytes
+// widened straight into fragment registers (fp32 accumulation throughout).
+// Lane (g, t) = (lane / 4, lane % 4).
+//  * S = K q: A = the 16-token x 16-dim key block of step kk with the dims
+//    permuted inside the step, fragment column 2t (+1) <-> dim 16kk + 4t (+1)
+//    and 2t + 8 (+9) <-> 16kk + 4t + 2 (+3), so that one 32-bit load of row g
+//    (and g + 8) gives the lane its four bytes; qb[kk] holds the query's
+//    dims in the same order.  The result rows are whole scores: tokens g and
+//    g + 8, in every lane of the group.
+//  * O^T += V^T p: per pair of 16-dim blocks, fragment row g <-> dims
+//    32qd + 4g (+2) and row g + 8 <-> 32qd + 4g + 1 (+3); fragment column
+//    (token) 2t, 2t + 1, 2t + 8, 2t + 9 <-> tokens t, 4 + t, 8 + t, 12 + t.
+//    Each lane loads 4 bytes of those four tokens and pairs them per dim with
+//    byte permutes; p arrives in the same token order by two shuffles.
+// Only columns 0 (c0, c2) of the output fragments are read, so only they are
+// rescaled.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void sf_chunk_f8_tc(const uint8_t* kt, const uint8_t* vt, int ntok,
+                                               const uint32_t (&qb)[8][2], float scale_log2, float& m,
+                                               float& s, float (&oc)[8][4], int w, int lane) {
+    constexpr int C = 64;
+    const int g = lane >> 2, t = lane & 3;
+    const int r0 = 16 * w + g, r1 = r0 + 8;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(kt + swz(r0, kk, C) + 4 * t);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(kt + swz(r1, kk, C) + 4 * t);
+        const uint32_t a[4] = {f16x2_from_e4m3x2(w0 & 0xffffu), f16x2_from_e4m3x2(w1 & 0xffffu),
+                               f16x2_from_e4m3x2(w0 >> 16), f16x2_from_e4m3x2(w1 >> 16)};
+        mma16816(acc, a, qb[kk][0], qb[kk][1]);
+    }
+    const float x0 = (r0 < ntok) ? acc[0] * scale_log2 : -INFINITY;   // token r0
+    const float x1 = (r1 < ntok) ? acc[2] * scale_log2 : -INFINITY;   // token r1
+    float mx = fmaxf(x0, x1);
+#pragma unroll
+    for (int off = 4; off <= 16; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+    const float mnew = fmaxf(m, mx);
+    const float mu = (mnew == -INFINITY) ? 0.f : mnew;
+    const float alpha = ex2(m - mu);
+    const float p0 = ex2(x0 - mu), p1 = ex2(x1 - mu);
+    float ps = p0 + p1;
+#pragma unroll
+    for (int off = 4; off <= 16; off <<= 1) ps += __shfl_xor_sync(kFull, ps, off);
+    s = s * alpha + ps;
+    m = mnew;
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+        oc[mb][0] *= alpha;
+        oc[mb][2] *= alpha;
+    }
+    // p of tokens (t, 4 + t) and (8 + t, 12 + t), as the B fragment
+    const uint32_t p2 = pack_half2(p0, p1);                   // (p[g], p[g + 8])
+    const uint32_t u = __shfl_sync(kFull, p2, 4 * t);         // (p[t], p[t + 8])
+    const uint32_t v = __shfl_sync(kFull, p2, 16 + 4 * t);    // (p[4 + t], p[12 + t])
+    const uint32_t pb0 = __byte_perm(u, v, 0x5410), pb1 = __byte_perm(u, v, 0x7632);
+    const int t0 = 16 * w + t;
+#pragma unroll
+    for (int qd = 0; qd < 4; ++qd) {
+        const int kc = 2 * qd + (g >> 2), off = 4 * (g & 3);
+        const uint32_t x0b = *reinterpret_cast<const uint32_t*>(vt + swz(t0, kc, C) + off);
+        const uint32_t x1b = *reinterpret_cast<const uint32_t*>(vt + swz(t0 + 4, kc, C) + off);
+        const uint32_t x2b = *reinterpret_cast<const uint32_t*>(vt + swz(t0 + 8, kc, C) + off);
+        const uint32_t x3b = *reinterpret_cast<const uint32_t*>(vt + swz(t0 + 12, kc, C) + off);
+        // bytes 0/1 of each token's word: dims 32qd + 4g (+1); bytes 2/3: +2 (+3)
+        const uint32_t za = __byte_perm(x0b, x1b, 0x5140), zb = __byte_perm(x2b, x3b, 0x5140);
+        const uint32_t zc = __byte_perm(x0b, x1b, 0x7362), zd = __byte_perm(x2b, x3b, 0x7362);
+        const uint32_t a0[4] = {f16x2_from_e4m3x2(za & 0xffffu), f16x2_from_e4m3x2(za >> 16),
+                                f16x2_from_e4m3x2(zb & 0xffffu), f16x2_from_e4m3x2(zb >> 16)};
+        mma16816(oc[2 * qd], a0, pb0, pb1);
+        const uint32_t a1[4] = {f16x2_from_e4m3x2(zc & 0xffffu), f16x2_from_e4m3x2(zc >> 16),
+                                f16x2_from_e4m3x2(zd & 0xffffu), f16x2_from_e4m3x2(zd >> 16)};
+        mma16816(oc[2 * qd + 1], a1, pb0, pb1);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Tensor-core path (chunk-first units, and sequence-first units with several
 // query rows): one chunk-head tile against a 16-row block of the Q tile with
 // mma.sync m16n8k16 (fp16 in, fp32 accumulate).  The warp takes tokens
@@ -583,6 +665,9 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
     using SM = Smem<C, D, EB>;
     constexpr int DPL = D / 32;
     constexpr int BOXES = D * EB / 128;   // 128-byte boxes per tile row
+    // single-row sequence-first work of an fp8 pool with 64-token chunks
+    // runs on the tensor cores (sf_chunk_f8_tc), elsewhere on CUDA cores
+    constexpr bool kF8Tc = EB == 1 && C == 64 && D == 128;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int S = p.n_stages;
     uint8_t* stages = smem;
@@ -834,37 +919,71 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 const uint4 qraw = take_q(qrow, h);
                 if (seg_end < c_end) prefetch_q(qrow, h + 1);
                 else if (next_sf) prefetch_q(fld(d0, F_QROW), fld(d0, F_HEAD));
-                float q[DPL], o[DPL], m = -INFINITY, s = 0.f;
-                {
-                    const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w};
+                float* xo = reinterpret_cast<float*>(qreg) + (flush & 1) * kConsumerWarps * D;
+                float* xm = xms + (flush & 1) * 2 * kConsumerWarps;
+                float m = -INFINITY, s = 0.f;
+                if constexpr (kF8Tc) {
+                    // The query in fragment order: lane L holds dims 4L .. 4L + 3,
+                    // step kk wants dims 16kk + 4t .. + 3, i.e. lane 4kk + t's.
+                    uint32_t qb[8][2];
 #pragma unroll
-                    for (int i = 0; i < DPL / 2; ++i) {
-                        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&qw[i]));
-                        q[2 * i] = a.x;
-                        q[2 * i + 1] = a.y;
+                    for (int kk = 0; kk < 8; ++kk) {
+                        qb[kk][0] = __shfl_sync(kFull, qraw.x, 4 * kk + (lane & 3));
+                        qb[kk][1] = __shfl_sync(kFull, qraw.y, 4 * kk + (lane & 3));
+                    }
+                    float oc[8][4];
+#pragma unroll
+                    for (int mb = 0; mb < 8; ++mb) oc[mb][0] = oc[mb][1] = oc[mb][2] = oc[mb][3] = 0.f;
+                    for (; L < seg_end; ++L, ++it) {
+                        const int st = it % S;
+                        if (!mbar_wait(full0 + 8 * st, (uint32_t)(it / S) & 1u)) {
+                            set_status(p.status, CA_ERR_TIMEOUT);
+                            return;
+                        }
+                        const int ntok = stage_ntok[st];
+                        const uint8_t* kt = stages + (size_t)st * SM::kStage;
+                        sf_chunk_f8_tc(kt, kt + SM::kTile, ntok, qb, p.scale_log2, m, s, oc, w, lane);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(empty0 + 8 * st);
+                    }
+                    // lane (g, 0) holds dims 32qd + 4g .. + 3 (see sf_chunk_f8_tc)
+                    if ((lane & 3) == 0) {
+#pragma unroll
+                        for (int qd = 0; qd < 4; ++qd)
+                            *reinterpret_cast<float4*>(xo + w * D + 32 * qd + 4 * (lane >> 2)) =
+                                make_float4(oc[2 * qd][0], oc[2 * qd][2], oc[2 * qd + 1][0], oc[2 * qd + 1][2]);
+                    }
+                } else {
+                    float q[DPL], o[DPL];
+                    {
+                        const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w};
+#pragma unroll
+                        for (int i = 0; i < DPL / 2; ++i) {
+                            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&qw[i]));
+                            q[2 * i] = a.x;
+                            q[2 * i + 1] = a.y;
+                        }
+#pragma unroll
+                        for (int d = 0; d < DPL; ++d) { q[d] *= p.scale_log2; o[d] = 0.f; }
+                    }
+                    for (; L < seg_end; ++L, ++it) {
+                        const int st = it % S;
+                        if (!mbar_wait(full0 + 8 * st, (uint32_t)(it / S) & 1u)) {
+                            set_status(p.status, CA_ERR_TIMEOUT);
+                            return;
+                        }
+                        const int ntok = stage_ntok[st];
+                        const uint8_t* kt = stages + (size_t)st * SM::kStage;
+                        sf_chunk<C, D, EB>(kt, kt + SM::kTile, ntok, q, m, s, o, w, lane);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(empty0 + 8 * st);
                     }
 #pragma unroll
-                    for (int d = 0; d < DPL; ++d) { q[d] *= p.scale_log2; o[d] = 0.f; }
-                }
-                for (; L < seg_end; ++L, ++it) {
-                    const int st = it % S;
-                    if (!mbar_wait(full0 + 8 * st, (uint32_t)(it / S) & 1u)) {
-                        set_status(p.status, CA_ERR_TIMEOUT);
-                        return;
-                    }
-                    const int ntok = stage_ntok[st];
-                    const uint8_t* kt = stages + (size_t)st * SM::kStage;
-                    sf_chunk<C, D, EB>(kt, kt + SM::kTile, ntok, q, m, s, o, w, lane);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(empty0 + 8 * st);
+                    for (int d = 0; d < DPL; ++d) xo[w * D + lane * DPL + d] = o[d];
                 }
                 // Combine the four warps' states and write the partial.  The
                 // exchange area alternates between two halves, so the next
                 // head's writes never meet this head's reads.
-                float* xo = reinterpret_cast<float*>(qreg) + (flush & 1) * kConsumerWarps * D;
-                float* xm = xms + (flush & 1) * 2 * kConsumerWarps;
-#pragma unroll
-                for (int d = 0; d < DPL; ++d) xo[w * D + lane * DPL + d] = o[d];
                 if (lane == 0) { xm[2 * w] = m; xm[2 * w + 1] = s; }
                 consumer_sync();
                 if (w == 0) {
