@@ -6,9 +6,11 @@
 // Self-Attention with Prefix-Aware KV Cache and Two-Phase Partition", §3.2).
 // A shared chunk is multiplied against the batched queries of every sequence
 // holding it (chunk-first, tensor cores); each sequence's own chunks are
-// processed per query (sequence-first, CUDA cores with warp-shuffle
-// reductions — or tensor cores too when a position brings several query rows
-// per key/value head: grouped query heads or several query tokens); every
+// processed per query (sequence-first: CUDA cores with warp-shuffle
+// reductions on an fp16 pool; tensor cores, with the bytes widened straight
+// into fragments, on an fp8 pool with 64-token chunks; tensor cores too when
+// a position brings several query rows per key/value head: grouped query
+// heads or several query tokens); every
 // piece of work leaves a partial triple (o, m, s) that is
 // combined by the rescaled-sum rule of the explainer blog's "Two-Phase
 // Partition" section.

@@ -212,10 +212,11 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, int32_t q_len, Pla
     const int32_t D = p.cfg.head_dim, c = p.cfg.chunk, b = t.b;
     plan.q_len = q_len;
     const double sf_cost = (RW == 1) ? 1.0 : 1.0 + kCfComputePer16 * ((RW + 15) / 16);
-    // An fp8 pool halves a tile's bytes, but the tensor-core phase widens each
-    // tile to fp16 in shared memory first, so there (and only there, when the
-    // sequence-first phase runs on CUDA cores) a chunk-first tile costs more
-    // relative to a sequence-first one.
+    // An fp8 pool halves a tile's bytes, but the chunk-first path widens each
+    // tile to fp16 in shared memory first while single-row sequence-first
+    // tiles go to the tensor cores straight from the bytes, so there (and
+    // only there) a chunk-first tile costs more relative to a sequence-first
+    // one.
     const double cf_mult = ((p.cfg.flags & CA_KV_FP8) && RW == 1) ? kF8CfFactor : 1.0;
     auto rows_cost = [&](int32_t m_rows) {
         return cf_mult * (1.0 + kCfComputePer16 * ((m_rows + 15) / 16)) / sf_cost;
