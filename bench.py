@@ -457,7 +457,8 @@ def run_ours(args):
                      "algorithmic_bytes": alg_bytes},
         "e2e": {"value": round(whole_job_per_call(e2e_us, world), 3), "unit": UNIT, "h2d_bytes_per_step": b * wl.q_len * H * D * 2,
                 "d2h_bytes_per_step": b * wl.q_len * H * D * 2,
-                "path": "ca_decode_attention_host: pinned host q -> device, kernel, device -> host out"},
+                "path": "ca_decode_attention_host: q read from and out written to pinned host memory by the "
+                        "kernels through its device mapping (NVLink-C2C), inside each step's event pair"},
         "gpu_launches": launches,
         "gpu_launches_source": "library launch counter (ca_kernel_launches) read around the timed loop",
         "clocks": clk,

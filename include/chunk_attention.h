@@ -305,10 +305,14 @@ int ca_decode_attention(const ca_pool* pool, const ca_sched* sched, int32_t laye
                         const void* q_dev, void* out_dev, float scale,
                         void* ws_dev, size_t ws_bytes, void* stream);
 
-/* The same computation with q and out in HOST memory (pinned for overlap):
- * copies q in, runs the kernels and copies out back, all on `stream`; the
- * caller synchronises.  ws_dev needs ca_workspace_bytes_host(sched) bytes
- * (the device staging for q and out lives at its end). */
+/* The same computation with q and out in HOST memory, all on `stream`; the
+ * caller synchronises.  When both buffers are pinned memory with a device
+ * mapping (cudaHostGetDevicePointer succeeds, as for cudaHostAlloc memory
+ * under unified addressing), the kernels read q from and the merge writes out
+ * to host memory directly (NVLink-C2C on GB300) and no copy is issued;
+ * otherwise q is copied in and out copied back through device staging.
+ * Either way ws_dev needs ca_workspace_bytes_host(sched) bytes (the staging
+ * for q and out lives at its end). */
 int ca_workspace_bytes_host(const ca_sched* sched, size_t* bytes_out);
 int ca_decode_attention_host(const ca_pool* pool, const ca_sched* sched,
                              int32_t layer, const void* q_host, void* out_host,

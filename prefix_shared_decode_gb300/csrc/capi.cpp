@@ -451,6 +451,17 @@ int ca_decode_attention_host(const ca_pool* pool, const ca_sched* s, int32_t lay
     int st = decode_checks(pool, s, layer, ws_dev, ws_bytes, s ? s->ws.total_host : 0);
     if (st) return st;
     if (!q_host || !out_host) return CA_ERR_INVALID;
+    // Pinned host memory is mapped into the device's address space (on GB300
+    // over NVLink-C2C): when both buffers have a device mapping, the kernels
+    // read q from it and the merge writes out to it directly, so no copy
+    // steps serialise with the kernels.  Otherwise q and out are staged in
+    // the workspace with one copy each way.
+    void* q_map = nullptr;
+    void* out_map = nullptr;
+    if (cudaHostGetDevicePointer(&q_map, const_cast<void*>(q_host), 0) == cudaSuccess &&
+        cudaHostGetDevicePointer(&out_map, out_host, 0) == cudaSuccess)
+        return decode_launch(pool, s, layer, q_map, out_map, scale, ws_dev, stream);
+    (void)cudaGetLastError();   // the failed lookup is not an error of this call
     const size_t bytes = (size_t)s->t.b * s->q_len * pool->cfg.n_heads * pool->cfg.head_dim * 2;
     unsigned char* ws = static_cast<unsigned char*>(ws_dev);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
