@@ -546,16 +546,24 @@ __device__ __forceinline__ void cf_softmax_pv(uint32_t vt, int ntok, int tok0, i
             mx[e >> 1] = fmaxf(mx[e >> 1], x);
         }
     }
+    // The row's reference maximum m is raised lazily: only when the chunk's
+    // maximum exceeds it by more than 2^8 (P then stays below 256, exact in
+    // fp16), so most chunks leave O unscaled; o and s always refer to the
+    // same m, which the partial carries.
     float alpha[2], mu[2];
+    bool grow = false;
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], 1));
         mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], 2));
-        const float mnew = fmaxf(m[r], mx[r]);
-        mu[r] = (mnew == -INFINITY) ? 0.f : mnew;
-        alpha[r] = ex2(m[r] - mu[r]);
-        m[r] = mnew;
-        s[r] *= alpha[r];
+        alpha[r] = 1.f;
+        if (mx[r] > m[r] + 8.f) {                   // also the first finite maximum
+            alpha[r] = ex2(m[r] - mx[r]);           // 0 while m is -inf
+            m[r] = mx[r];
+            s[r] *= alpha[r];
+            grow = true;
+        }
+        mu[r] = (m[r] == -INFINITY) ? 0.f : m[r];
     }
     uint32_t pa[NT / 16][4];
 #pragma unroll
@@ -568,10 +576,12 @@ __device__ __forceinline__ void cf_softmax_pv(uint32_t vt, int ntok, int tok0, i
         pa[nt >> 1][(nt & 1) * 2 + 0] = pack_half2(p0, p1);
         pa[nt >> 1][(nt & 1) * 2 + 1] = pack_half2(p2, p3);
     }
+    if (__any_sync(kFull, grow)) {
 #pragma unroll
-    for (int dt = 0; dt < OD / 8; ++dt) {
-        o[dt][0] *= alpha[0]; o[dt][1] *= alpha[0];
-        o[dt][2] *= alpha[1]; o[dt][3] *= alpha[1];
+        for (int dt = 0; dt < OD / 8; ++dt) {
+            o[dt][0] *= alpha[0]; o[dt][1] *= alpha[0];
+            o[dt][2] *= alpha[1]; o[dt][3] *= alpha[1];
+        }
     }
 #pragma unroll
     for (int j = 0; j < NT / 16; ++j) {
