@@ -111,26 +111,34 @@ def cpu_baseline(wl, seconds: float = CPU_SAMPLE_SECONDS) -> dict:
 # Clock sampling during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples of SM clock and throttle reasons every 10 ms, each
+    with its timestamp, so that the samples inside the timed window (wall
+    clock, set with window()) can be told from the rest."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index: int):
+        import tempfile
         self.idx = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"ca_bench_clocks_{os.getpid()}.csv")
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", "10"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
+    def window(self, t0: float, t1: float):
+        self.t0, self.t1 = t0, t1
+
     def stop(self) -> dict:
+        import datetime
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -139,23 +147,28 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.close()
-        sm, smax, reasons = [], [], set()
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]),
+                             {n for n, v in zip(names, parts[6:10]) if v.lower().startswith("active")}))
             except ValueError:
                 continue
-            for n, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        inside = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= self.t1]
+        use = inside or rows
+        return {"sm_mhz": statistics.median(r[1] for r in use) if use else None,
+                "sm_max_mhz": max(r[2] for r in use) if use else None,
+                "reasons": sorted(set().union(*(r[3] for r in use))) if use else [],
+                "samples": len(rows), "samples_in_timed_region": len(inside)}
 
 
 def measured_peak():
@@ -337,6 +350,7 @@ def run_ours(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
+    win0 = time.time()
     ev_a.record(stream)
     launches0 = kernel_launches()
     for i in range(K):
@@ -350,6 +364,7 @@ def run_ours(args):
     ev_b.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    clocks.window(win0, time.time())
     launches = kernel_launches() - launches0
     if world > 1:
         torch.distributed.barrier()
