@@ -139,6 +139,16 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr));
 }
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+// The 8x8 b16 matrix held in fragment layout (lane L: row L/4, columns
+// 2(L%4), 2(L%4)+1) transposed across the warp.
+__device__ __forceinline__ uint32_t movm_trans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
     asm volatile(
@@ -672,9 +682,212 @@ struct Smem {
 };
 
 // ---------------------------------------------------------------------------
-// The persistent two-phase kernel.
+// A sequence-first unit of one position with at most 8 query rows per key/
+// value head (grouped query heads or several query tokens).  The products
+// are taken transposed, tokens on the mma rows and the query rows on its 8
+// columns: S^T = K Q^T and O^T += V^T P^T, so no mma row is padding (a
+// 16-row block would hold 4 live rows at G = 4).  Warp w < T takes tokens
+// [16w, 16w + 16) of each chunk; lane (g, t) holds the scores of tokens g
+// and g + 8 for query rows 2t and 2t + 1, and O^T for dims 16db + g (+8) of
+// the same rows.  Q^T fragments are read from the Q tile with ldmatrix each
+// chunk; P^T fragments are the score fragments transposed in registers
+// (movmatrix).  The warps' states are tree-combined through the Q tile at
+// each head boundary and warp 0 writes the rows' partials.  It is compiled
+// only into the kernel variant for such schedules, so that its registers do
+// not weigh on the single-row kernel.  Walks [L, L_end) of the unit's
+// (head, chunk) range; false on a timeout.
 // ---------------------------------------------------------------------------
 template <int C, int D, int EB>
+__device__ __forceinline__ bool sf_rows_transposed(
+    const AttnParams& p, uint8_t* stages, uint8_t* conv, uint8_t* qreg, float* xms, uint32_t full0,
+    uint32_t empty0, const volatile int32_t* stage_ntok, const volatile int32_t* stage_tok0, int S, int& it_io,
+    int& L_io, int L_end, int n, int q_lo, int m_rows, int part_first, int part_rest, int w, int lane) {
+    using SM = Smem<C, D, EB>;
+    const int H = p.n_heads, G = p.group, QL = p.q_len;
+    const int Tr = min(kConsumerWarps, C / 16);
+    const bool act = w < Tr;
+    const int g = lane >> 2, t = lane & 3;
+    int it = it_io, L = L_io;
+    int limr[2] = {INT_MAX, INT_MAX};               // causal limits of rows 2t, 2t + 1
+    if (p.causal) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+            if (2 * t + r < m_rows) limr[r] = p.ctx_len[q_lo] - QL + (2 * t + r) / G;
+    }
+    bool ok = true;
+    for (bool first = true; L < L_end && ok; first = false) {
+        const int kvh = L / n;
+        const int seg_end = min(L_end, (kvh + 1) * n);
+        const int upart = first ? part_first : part_rest;
+        if (!first) consumer_sync();   // the previous head's exchange reads are done
+        for (int idx = threadIdx.x; idx < m_rows * (D / 8); idx += kConsumerWarps * 32) {
+            const int r = idx / (D / 8), k = idx % (D / 8);
+            const size_t qrow_tok = (size_t)p.seq_perm[q_lo] * QL + r / G;
+            const uint16_t* src = p.q + (qrow_tok * H + kvh * G + r % G) * D + k * 8;
+            cp_async16(smem_u32(qreg + swz(r, k, q_rows<D>())), src);
+        }
+        cp_async_wait_all();
+        consumer_sync();
+        float ot[D / 16][4], m[2] = {-INFINITY, -INFINITY}, s[2] = {0.f, 0.f};
+#pragma unroll
+        for (int db = 0; db < D / 16; ++db) ot[db][0] = ot[db][1] = ot[db][2] = ot[db][3] = 0.f;
+        for (; L < seg_end; ++L, ++it) {
+            const int st = it % S;
+            if (!mbar_wait(full0 + 8 * st, (uint32_t)(it / S) & 1u)) {
+                set_status(p.status, CA_ERR_TIMEOUT);
+                ok = false;
+                break;
+            }
+            uint32_t kt = smem_u32(stages + (size_t)st * SM::kStage);
+            uint32_t vt = kt + SM::kTile;
+            const int ntok = stage_ntok[st];
+            const int ctx0 = stage_tok0[st];
+            if constexpr (EB == 1) {
+                consumer_sync();
+                const uint8_t* sk = stages + (size_t)st * SM::kStage;
+                f8_tile_to_f16<C>(sk, conv, threadIdx.x);
+                f8_tile_to_f16<C>(sk + SM::kTile, conv + SM::kConvBytes / 2, threadIdx.x);
+                consumer_sync();
+                if (lane == 0) mbar_arrive(empty0 + 8 * st);
+                kt = smem_u32(conv);
+                vt = kt + SM::kConvBytes / 2;
+            }
+            if (act) {
+                const int tok0 = 16 * w;
+                float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    // Q^T as the B operand: n = query row (lane & 7), k = 16 dims
+                    uint32_t a[4], qb0, qb1;
+                    ldsm_x2(smem_u32(qreg) + swz(lane & 7, 2 * kk + ((lane >> 3) & 1), q_rows<D>()), qb0, qb1);
+                    ldsm_x4(kt + swz(tok0 + (lane & 15), 2 * kk + (lane >> 4), C), a[0], a[1], a[2], a[3]);
+                    mma16816(sacc, a, qb0, qb1);
+                }
+                // sacc: (token g, rows 2t, 2t+1), (token g + 8, rows 2t, 2t+1)
+                float x[4], mx[2];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int tok = tok0 + g + 8 * (i >> 1), row = 2 * t + (i & 1);
+                    const bool valid = tok < ntok && row < m_rows && ctx0 + tok <= limr[i & 1];
+                    x[i] = valid ? sacc[i] * p.scale_log2 : -INFINITY;
+                }
+                mx[0] = fmaxf(x[0], x[2]);
+                mx[1] = fmaxf(x[1], x[3]);
+                bool grow = false;
+                float alpha[2] = {1.f, 1.f}, mu[2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+#pragma unroll
+                    for (int off = 4; off <= 16; off <<= 1) mx[r] = fmaxf(mx[r], __shfl_xor_sync(kFull, mx[r], off));
+                    // the reference maximum is raised lazily, as in cf_softmax_pv
+                    if (mx[r] > m[r] + 8.f) {
+                        alpha[r] = ex2(m[r] - mx[r]);
+                        m[r] = mx[r];
+                        s[r] *= alpha[r];
+                        grow = true;
+                    }
+                    mu[r] = (m[r] == -INFINITY) ? 0.f : m[r];
+                }
+                if (__any_sync(kFull, grow)) {
+#pragma unroll
+                    for (int db = 0; db < D / 16; ++db) {
+                        ot[db][0] *= alpha[0]; ot[db][1] *= alpha[1];
+                        ot[db][2] *= alpha[0]; ot[db][3] *= alpha[1];
+                    }
+                }
+                const float p0 = ex2(x[0] - mu[0]), p1 = ex2(x[1] - mu[1]);
+                const float p2 = ex2(x[2] - mu[0]), p3 = ex2(x[3] - mu[1]);
+                float ps[2] = {p0 + p2, p1 + p3};
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+#pragma unroll
+                    for (int off = 4; off <= 16; off <<= 1) ps[r] += __shfl_xor_sync(kFull, ps[r], off);
+                    s[r] += ps[r];
+                }
+                // P^T fragments: k = tokens, n = query rows
+                const uint32_t b0 = movm_trans(pack_half2(p0, p1));   // tokens 0..7
+                const uint32_t b1 = movm_trans(pack_half2(p2, p3));   // tokens 8..15
+#pragma unroll
+                for (int db = 0; db < D / 16; ++db) {
+                    uint32_t a[4];
+                    ldsm_x4_t(vt + swz(tok0 + (lane & 7) + ((lane >> 4) << 3), 2 * db + ((lane >> 3) & 1), C),
+                              a[0], a[1], a[2], a[3]);
+                    mma16816(ot[db], a, b0, b1);
+                }
+            }
+            if constexpr (EB == 2) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8 * st);
+            }
+        }
+        if (!ok) break;
+        // Combine the Tr warps' states through the Q tile (free once every
+        // warp has left the chunk loop: the barrier opening each round).
+        float* xo = reinterpret_cast<float*>(qreg);
+        for (int half = Tr / 2; half >= 1; half /= 2) {
+            consumer_sync();
+            if (w >= half && w < 2 * half) {
+                float* dst = xo + (size_t)(w - half) * (D / 16) * 4 * 32;
+#pragma unroll
+                for (int db = 0; db < D / 16; ++db)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dst[(db * 4 + e) * 32 + lane] = ot[db][e];
+                if (g == 0) {
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        xms[(w - half) * 16 + (2 * t + r) * 2] = m[r];
+                        xms[(w - half) * 16 + (2 * t + r) * 2 + 1] = s[r];
+                    }
+                }
+            }
+            consumer_sync();
+            if (w < half) {
+                const float* so = xo + (size_t)w * (D / 16) * 4 * 32;
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float m2 = xms[w * 16 + (2 * t + r) * 2], s2 = xms[w * 16 + (2 * t + r) * 2 + 1];
+                    const float M = fmaxf(m[r], m2);
+                    const float Mu = (M == -INFINITY) ? 0.f : M;
+                    const float a1 = ex2(m[r] - Mu), a2 = ex2(m2 - Mu);
+                    s[r] = s[r] * a1 + s2 * a2;
+                    m[r] = M;
+#pragma unroll
+                    for (int db = 0; db < D / 16; ++db) {
+                        ot[db][r] = ot[db][r] * a1 + so[(db * 4 + r) * 32 + lane] * a2;
+                        ot[db][r + 2] = ot[db][r + 2] * a1 + so[(db * 4 + r + 2) * 32 + lane] * a2;
+                    }
+                }
+            }
+        }
+        if (w == 0) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int row = 2 * t + r;
+                if (row < m_rows) {
+                    const int pid = p.pbase[((size_t)q_lo * QL + row / G) * H + kvh * G + row % G] + upart;
+                    float* dst = p.part_o + (size_t)pid * D;
+#pragma unroll
+                    for (int db = 0; db < D / 16; ++db) {
+                        dst[16 * db + g] = ot[db][r];
+                        dst[16 * db + g + 8] = ot[db][r + 2];
+                    }
+                    if (g == 0) p.part_ms[pid] = make_float2(m[r], s[r]);
+                }
+            }
+        }
+    }
+    it_io = it;
+    L_io = L;
+    return ok;
+}
+
+// ---------------------------------------------------------------------------
+// The persistent two-phase kernel.
+// ---------------------------------------------------------------------------
+// kRows: the variant for schedules whose positions bring 2..8 query rows per
+// key/value head (head_dim <= 128): it has the transposed few-row path and
+// no single-row sequence-first path; the other variant the reverse.
+template <int C, int D, int EB, bool kRows>
 __global__ void __launch_bounds__(kThreads, 2)
 two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnParams p) {
     using SM = Smem<C, D, EB>;
@@ -925,7 +1138,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
         const int32_t d0 = dn;
         const bool next_sf = next_static && fld(d0, F_KIND) == UNIT_SF;
         consumer_sync();   // previous unit (and its exchange reads) finished
-        if (fld(dc, F_KIND) == UNIT_SF && G == 1 && QL == 1) {
+        if (!kRows && fld(dc, F_KIND) == UNIT_SF && G == 1 && QL == 1) {
             const int pos = fld(dc, F_QLO), n = fld(dc, F_N), base = fld(dc, F_BASE);
             const int qrow = fld(dc, F_QROW), c_end = fld(dc, F_CE), part_next = fld(dc, F_PNEXT);
             int L = fld(dc, F_CB), h = fld(dc, F_HEAD), part = fld(dc, F_PART);
@@ -1063,6 +1276,14 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     if (row < m_rows) lim[r2] = p.ctx_len[q_lo + row / RW] - QL + (row % RW) / G;
                 }
             }
+            if (kRows && !kSplit && is_sf && m_rows <= 8) {
+                // a sequence-first position with at most 8 query rows:
+                // the products transposed (sf_rows_transposed)
+                if (!sf_rows_transposed<C, D, EB>(p, stages, conv, qreg, xms, full0, empty0, stage_ntok,
+                                                  stage_tok0, S, it, L, L_end, n, q_lo, m_rows, part_first,
+                                                  part_rest, w, lane))
+                    return;
+            } else {
             for (bool first = true; L < L_end; first = false) {
                 const int kvh = L / n;
                 const int seg_end = min(L_end, (kvh + 1) * n);
@@ -1205,6 +1426,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     }
                 }
             }
+            }
         }
     }
 }
@@ -1281,27 +1503,36 @@ __global__ void __launch_bounds__(256) kv_scatter_kernel(const __grid_constant__
 // Host launchers.
 // ---------------------------------------------------------------------------
 namespace {
-template <int C, int D, int EB>
+template <int C, int D, int EB, bool R>
 void* kernel_ptr() {
-    return reinterpret_cast<void*>(&dev::two_phase_attention_kernel<C, D, EB>);
+    return reinterpret_cast<void*>(&dev::two_phase_attention_kernel<C, D, EB, R>);
 }
-void* pick_kernel(const ca_pool_config& c) {
+template <int C, int D, int EB>
+void* kernel_ptr(bool rows) {
+    if constexpr (D <= 128) {
+        if (rows) return kernel_ptr<C, D, EB, true>();
+    }
+    return kernel_ptr<C, D, EB, false>();
+}
+// rows: the schedule brings 2..8 query rows per position and key/value head
+// (the few-row variant exists for head_dim <= 128).
+void* pick_kernel(const ca_pool_config& c, bool rows = false) {
     if (kv_elem_bytes(c) == 1) {
         if (c.head_dim != 128) return nullptr;
-        if (c.chunk == 64) return kernel_ptr<64, 128, 1>();
-        if (c.chunk == 32) return kernel_ptr<32, 128, 1>();
-        if (c.chunk == 16) return kernel_ptr<16, 128, 1>();
+        if (c.chunk == 64) return kernel_ptr<64, 128, 1>(rows);
+        if (c.chunk == 32) return kernel_ptr<32, 128, 1>(rows);
+        if (c.chunk == 16) return kernel_ptr<16, 128, 1>(rows);
     } else if (c.head_dim == 256) {                 // chunks of 16 or 32 tokens
-        if (c.chunk == 32) return kernel_ptr<32, 256, 2>();
-        if (c.chunk == 16) return kernel_ptr<16, 256, 2>();
+        if (c.chunk == 32) return kernel_ptr<32, 256, 2>(false);
+        if (c.chunk == 16) return kernel_ptr<16, 256, 2>(false);
     } else if (c.head_dim == 128) {
-        if (c.chunk == 64) return kernel_ptr<64, 128, 2>();
-        if (c.chunk == 32) return kernel_ptr<32, 128, 2>();
-        if (c.chunk == 16) return kernel_ptr<16, 128, 2>();
+        if (c.chunk == 64) return kernel_ptr<64, 128, 2>(rows);
+        if (c.chunk == 32) return kernel_ptr<32, 128, 2>(rows);
+        if (c.chunk == 16) return kernel_ptr<16, 128, 2>(rows);
     } else if (c.head_dim == 64) {
-        if (c.chunk == 64) return kernel_ptr<64, 64, 2>();
-        if (c.chunk == 32) return kernel_ptr<32, 64, 2>();
-        if (c.chunk == 16) return kernel_ptr<16, 64, 2>();
+        if (c.chunk == 64) return kernel_ptr<64, 64, 2>(rows);
+        if (c.chunk == 32) return kernel_ptr<32, 64, 2>(rows);
+        if (c.chunk == 16) return kernel_ptr<16, 64, 2>(rows);
     }
     return nullptr;
 }
@@ -1334,6 +1565,11 @@ int kernel_ctas_per_sm(const ca_pool_config& c, int* ctas) {
     size_t bytes;
     kernel_smem_bytes(c, &st, &bytes);
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+        return CA_ERR_CUDA;
+    // the few-row variant takes the same shared memory (and, by its launch
+    // bounds, the same two CTAs per SM)
+    void* fr = pick_kernel(c, true);
+    if (fr != fn && cudaFuncSetAttribute(fr, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
         return CA_ERR_CUDA;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, dev::kThreads, bytes) != cudaSuccess)
@@ -1410,7 +1646,9 @@ int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_ro
 }
 
 int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void* stream) {
-    void* fn = pick_kernel(p.cfg);
+    // positions with 2..8 query rows per key/value head: the few-row variant
+    const int rw = s.q_len * (p.cfg.n_heads / kv_heads(p.cfg));
+    void* fn = pick_kernel(p.cfg, rw >= 2 && rw <= 8);
     if (!fn) return CA_ERR_UNSUPPORTED;
     int st;
     size_t bytes;
