@@ -451,6 +451,11 @@ def run_ours(args):
 
     unique_tokens = wl.unique_tokens()
     io_bytes = 2 * b * wl.q_len * H * D * 2                    # q in, out
+    # the kernel variant the library launches: the few-row one when positions
+    # bring 2..8 query rows per key/value head (head_dim <= 128)
+    rows_per_kv = wl.q_len * (H // HK)
+    few_rows = 2 <= rows_per_kv <= 8 and D <= 128
+    kname = f"two_phase_attention_kernel<{c},{D},{eb},{'true' if few_rows else 'false'}>"
     alg_bytes = kv_bytes + io_bytes
     us = ms_per_step * 1e3
     peak, peak_kind = measured_peak()
@@ -484,8 +489,8 @@ def run_ours(args):
         "effective_hbm_gbs": round(alg_bytes / (us * 1e-6) / 1e9, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
-                     "traffic": kernel_traffic(f"two_phase_attention_kernel<{c},{D},{eb}>:{wl.name}"),
-                     "kernel": f"two_phase_attention_kernel<{c},{D},{eb}>",
+                     "traffic": kernel_traffic(f"{kname}:{wl.name}"),
+                     "kernel": kname,
                      "kernel_us": round(kern_ms_avg * 1e3, 3),
                      "kernel_timing": f"CUDA events around the main kernel on {len(kev)} of the {K} timed steps",
                      "algorithmic_bytes": alg_bytes},
