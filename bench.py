@@ -411,8 +411,40 @@ def run_ours(args):
         eev[i][1].record(stream)
     torch.cuda.synchronize()
     e2e_us = sum(a.elapsed_time(z) for a, z in eev) / Ke * 1e3
+
+    # The same calls recorded into one CUDA graph (NG calls rotating over the
+    # pool copies as the timed loop does) and replayed: one host launch per
+    # NG calls instead of two kernel launches and the argument checks per
+    # call.  Not for the churn workload, whose schedule changes every step.
+    graph_us = graph_host_us = 0.0
+    NG, RG = 32, 16
+    if not churn:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.graph(g, stream=side):
+            for i in range(NG):
+                r = i % n_copies
+                decode_attention(pools[r], scheds[r], qs[i % 4], out=out, scale=wl.scale, workspace=wss[r])
+        stream.wait_stream(side)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        ga, gz = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        h0 = time.perf_counter()
+        ga.record(stream)
+        for _ in range(RG):
+            g.replay()
+        gz.record(stream)
+        graph_host_us = (time.perf_counter() - h0) * 1e6 / (RG * NG)
+        torch.cuda.synchronize()
+        graph_us = ga.elapsed_time(gz) * 1e3 / (RG * NG)
+        if max((s_.device_status() for s_ in scheds), key=abs) != 0:
+            raise RuntimeError("device status after graph replays")
+        del g
     # the slowest rank's times (one rank: unchanged)
-    ms_per_step, kern_ms_avg, e2e_us, iso_us = max_over_ranks([ms_per_step, kern_ms_avg, e2e_us, iso_us], device=dev)
+    ms_per_step, kern_ms_avg, e2e_us, iso_us, graph_us = max_over_ranks(
+        [ms_per_step, kern_ms_avg, e2e_us, iso_us, graph_us], device=dev)
 
     # Context: the same batch through the flat paged layout (no sharing) and
     # through physically shared KV without the two-phase partition.
@@ -501,6 +533,11 @@ def run_ours(args):
         "isolated_call": {"median_us": round(iso_us, 2), "reps": len(iso),
                           "method": "one call at a time: CUDA events around the call only, median of 200 "
                                     "after 20 warm-up calls, L2 flushed (2 x L2 written) before each call"},
+        "graph_replay": ({"us_per_call": round(graph_us, 3), "calls_per_graph": NG, "replays": RG,
+                          "host_us_per_call": round(graph_host_us, 2),
+                          "method": "decode_attention calls recorded into one CUDA graph (torch.cuda.graph), "
+                                    "replayed back to back; one event pair around all replays"}
+                         if not churn else None),
         "gpu_launches": launches,
         "gpu_launches_source": "library launch counter (ca_kernel_launches) read around the timed loop",
         "clocks": clk,

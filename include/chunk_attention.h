@@ -296,9 +296,23 @@ int ca_workspace_bytes(const ca_sched* sched, size_t* bytes_out);
  * when no insert or append on this pool was launched since its last
  * attention call, so the pool's device memory must be written only through
  * this library's calls.
+ * Stream capture (CUDA graphs): the call may be recorded into a graph
+ * (cudaStreamBeginCapture or torch.cuda.graph on `stream`), with q_dev,
+ * out_dev and ws_dev fixed at capture; the two kernels keep their
+ * programmatic dependencies inside the graph.  The first call a capture
+ * records for a pool does not stream the pool before its dependency wait,
+ * since at replay anything may precede it.  Once an insert or append has
+ * been recorded into a graph, uncaptured calls on that pool no longer do
+ * either (the host cannot see when those replays write the pool).  A graph
+ * stays valid while its schedule is unchanged: appends that fit the
+ * sequences' partial last chunks keep it (the kernels read each chunk's
+ * token count from the pool); anything that rebuilds the schedule (a grown
+ * chunk, an insert or remove, another batch) needs a new capture.  Build
+ * schedules outside capture (ca_build_schedule allocates).
  * Errors: CA_ERR_STALE if the pool changed after the schedule was built;
  * CA_ERR_INVALID for a host-only pool, bad layer, NULL or misaligned pointers
- * or a small workspace; CA_ERR_CUDA if a launch fails.  Kernel-side faults
+ * or a small workspace; CA_ERR_CUDA if a launch fails or `stream`'s capture
+ * was invalidated.  Kernel-side faults
  * (an index out of range, a wait that timed out) are reported by
  * ca_sched_device_status(). */
 int ca_decode_attention(const ca_pool* pool, const ca_sched* sched, int32_t layer,

@@ -20,15 +20,26 @@ import numpy as np
 from . import capi
 from .capi import CAError, check
 
-__all__ = ["Pool", "Schedule", "decode_attention", "decode_attention_host", "kernel_launches",
+__all__ = ["Pool", "Schedule", "DecodeGraph", "decode_attention", "decode_attention_host", "kernel_launches",
            "CAError"]
 
 
+_cuda_ok = None
+
+
 def _stream_ptr(stream) -> int | None:
+    """The raw handle of ``stream`` (default: torch's current stream on the
+    current device; 0 / None is the legacy default stream)."""
     if stream is None:
+        global _cuda_ok
         import torch
-        if not torch.cuda.is_available():
+        if _cuda_ok is None:
+            _cuda_ok = torch.cuda.is_available()
+        if not _cuda_ok:
             return None
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)   # no Stream object per call
+        if raw is not None:
+            return raw(torch.cuda.current_device()) or None
         stream = torch.cuda.current_stream()
     return int(getattr(stream, "cuda_stream", stream)) or None
 
@@ -178,6 +189,11 @@ class Pool:
         check(capi.lib().ca_remove_batch(self._h, len(ids), ids.ctypes.data_as(C.POINTER(C.c_int64))),
               "ca_remove_batch")
 
+    def _generation(self) -> int:
+        st = self.__dict__.setdefault("_stats_buf", capi.Stats())
+        check(capi.lib().ca_pool_stats(self._h, C.byref(st)), "ca_pool_stats")
+        return st.generation
+
     def stats(self) -> dict:
         s = capi.Stats()
         check(capi.lib().ca_pool_stats(self._h, C.byref(s)), "ca_pool_stats")
@@ -197,17 +213,27 @@ class Pool:
         ``q_len`` > 1: that many query tokens per sequence (q / out become
         [b, q_len, H, D]); ``causal``: token j sees context tokens
         [0, len - q_len + j] only."""
-        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
         s = reuse if reuse is not None else Schedule(self)
+        # A decode loop passes the same batch list every step: its int64 copy
+        # (and that copy's address) is kept, so the per-step call converts
+        # nothing; the library itself decides whether the tables are current.
+        if isinstance(seq_ids, list) and s._ids_list is not None and seq_ids == s._ids_list:
+            ids = s._ids
+        else:
+            ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
         h = s._h if s._h is not None else C.c_void_p()
         flags = (capi.CA_SCHED_NO_TPP if no_tpp else 0) | (capi.CA_SCHED_CAUSAL if causal else 0)
-        check(capi.lib().ca_build_schedule_ex(self._h, ids.ctypes.data_as(C.POINTER(C.c_int64)), len(ids),
-                                              int(q_len), flags, C.byref(h),
+        check(capi.lib().ca_build_schedule_ex(self._h, ids.__array_interface__["data"][0] if ids is not s._ids
+                                              else s._ids_ptr, len(ids), int(q_len), flags, C.byref(h),
                                               None if self.host_only else _stream_ptr(stream)),
               "ca_build_schedule_ex")
         s._h = h
         s.b = len(ids)
         s.q_len = int(q_len)
+        if ids is not s._ids:
+            s._ids, s._ids_ptr = ids, ids.__array_interface__["data"][0]
+            s._ids_list = list(seq_ids) if isinstance(seq_ids, list) else None
+        s._flags = flags
         return s
 
 
@@ -220,6 +246,12 @@ class Schedule:
         self.b = 0
         self.q_len = 1
         self._ws = None
+        self._ids, self._ids_ptr, self._ids_list, self._flags = None, None, None, 0
+
+    def _key(self) -> tuple:
+        """What the library's tables depend on: the batch, the flags, q_len and
+        the pool's generation (the library rebuilds them when one changes)."""
+        return (self._ids.tobytes(), self._flags, self.q_len, self.pool._generation())
 
     def __del__(self):
         if getattr(self, "_h", None) is not None and self._h.value:
@@ -295,10 +327,12 @@ def decode_attention(pool: Pool, sched: Schedule, q, out=None, layer: int = 0, s
     context, via the two-phase kernel.  q: fp16 [b, H, D] on the GPU
     ([b, q_len, H, D] for a multi-token schedule)."""
     import torch
-    assert q.dtype == torch.float16 and q.is_contiguous()
+    if q.dtype != torch.float16 or not q.is_contiguous():
+        raise ValueError("q must be a contiguous fp16 tensor")
     want = ((sched.b, pool.n_heads, pool.head_dim) if sched.q_len == 1
             else (sched.b, sched.q_len, pool.n_heads, pool.head_dim))
-    assert tuple(q.shape) == want, (tuple(q.shape), want)
+    if q.shape != want:
+        raise ValueError(f"q has shape {tuple(q.shape)}, the schedule needs {want}")
     if out is None:
         out = torch.empty_like(q)
     if scale is None:
@@ -322,6 +356,47 @@ def decode_attention_host(pool: Pool, sched: Schedule, q_host, out_host, layer: 
                                               ws.numel(), _stream_ptr(stream)),
           "ca_decode_attention_host")
     return out_host
+
+
+class DecodeGraph:
+    """Decode-attention calls recorded once into a CUDA graph and replayed
+    with one launch: the per-call host work (argument checks, two kernel
+    launches each) is paid at capture only.  ``calls`` lists (layer, q, out)
+    device tensors, run in that order on one schedule and workspace; the
+    graph keeps those buffers, so new queries are written into the same q
+    tensors before each replay.  The kernels keep their programmatic
+    dependencies inside the graph.  A replay is valid while the schedule is
+    the one captured: appending tokens that fit the sequences' partial last
+    chunks keeps it (the kernels read each chunk's token count from the pool),
+    while anything that rebuilds the schedule (a grown chunk, an insert or
+    remove, another batch) makes ``replay`` raise; capture again then."""
+
+    def __init__(self, pool: Pool, sched: Schedule, calls, workspace=None, scale: float | None = None):
+        import torch
+        self.pool, self.sched = pool, sched
+        self.calls = [(int(layer), q, out) for layer, q, out in calls]
+        self.workspace = workspace if workspace is not None else sched.workspace()
+        self.scale = scale
+        self._key = sched._key()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self._record()                       # one uncaptured pass first
+        torch.cuda.current_stream().wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._record()
+
+    def _record(self):
+        for layer, q, out in self.calls:
+            decode_attention(self.pool, self.sched, q, out=out, layer=layer, scale=self.scale,
+                             workspace=self.workspace)
+
+    def replay(self) -> None:
+        """Run every recorded call on the current stream."""
+        if self.sched._key() != self._key:
+            raise CAError(capi.CA_ERR_STALE, "DecodeGraph: the pool or the schedule changed after capture")
+        self.graph.replay()
 
 
 def kernel_launches() -> int:

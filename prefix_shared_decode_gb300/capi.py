@@ -11,6 +11,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libchunk_attention.so")
 
 CA_OK = 0
+CA_ERR_STALE = -5
 ERRORS = {
     -1: "CA_ERR_INVALID", -2: "CA_ERR_OOM", -3: "CA_ERR_NOT_FOUND", -4: "CA_ERR_EXISTS",
     -5: "CA_ERR_STALE", -6: "CA_ERR_CUDA", -7: "CA_ERR_DEVICE_BOUNDS", -8: "CA_ERR_TIMEOUT",
@@ -79,7 +80,7 @@ def lib() -> C.CDLL:
         "ca_pool_stats": [vp, P(Stats)],
         "ca_seq_slots": [vp, i64, P(i32), i32, P(i32)],
         "ca_build_schedule": [vp, P(i64), i32, u32, P(vp), vp],
-        "ca_build_schedule_ex": [vp, P(i64), i32, i32, u32, P(vp), vp],
+        "ca_build_schedule_ex": [vp, vp, i32, i32, u32, P(vp), vp],     # seq_ids: int64 array address
         "ca_sched_destroy": [vp],
         "ca_sched_counts": [vp, P(i32)],
         "ca_export_tables": [vp] + [P(i32)] * 7,

@@ -137,6 +137,12 @@ struct Pool {
     // attention launch reads it: while clear, the pool's device contents are
     // not written by any kernel the next attention call could overlap.
     mutable bool kv_written = true;
+    // Stream capture (CUDA graphs): the id of the capture that last recorded
+    // an attention call on this pool, and whether a KV scatter was ever
+    // recorded into a graph (its replays then write the pool at times the
+    // host does not see).
+    mutable unsigned long long capture_id = 0;
+    mutable bool captured_writes = false;
 };
 
 struct Tables {

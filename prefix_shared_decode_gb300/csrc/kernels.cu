@@ -1618,6 +1618,9 @@ int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_ro
                    const std::vector<ScatterChunk>& chunks, void* stream) {
     const ca_pool_config& c = p.cfg;
     p.kv_written = true;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap) != cudaSuccess) return CA_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone) p.captured_writes = true;
     for (size_t i = 0; i < chunks.size(); i += dev::kScatterMaxChunks) {
         const size_t cnt = std::min<size_t>(dev::kScatterMaxChunks, chunks.size() - i);
         dev::ScatterArgs a;
@@ -1657,12 +1660,28 @@ int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void*
     a.n_stages = st;
     // The kernel may read the pool before its dependency wait only when no
     // KV scatter was launched since the last attention launch: every kernel
-    // this launch can overlap then leaves the pool alone.
-    a.kv_stable = p.kv_written ? 0 : 1;
+    // this launch can overlap then leaves the pool alone.  Under stream
+    // capture, the first attention call a graph records for this pool may
+    // follow anything when the graph is replayed, so it waits; and once a
+    // scatter has been recorded into a graph, the host no longer knows when
+    // the pool is written, so uncaptured calls always wait.
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    unsigned long long cap_id = 0;
+    if (cudaStreamGetCaptureInfo(cs, &cap, &cap_id) != cudaSuccess) return CA_ERR_CUDA;
+    bool stable = !p.kv_written;
+    if (cap == cudaStreamCaptureStatusActive) {
+        if (p.capture_id != cap_id) stable = false;
+        p.capture_id = cap_id;
+    } else if (cap != cudaStreamCaptureStatusNone) {
+        return CA_ERR_CUDA;                       // an invalidated capture
+    } else if (p.captured_writes) {
+        stable = false;
+    }
+    a.kv_stable = stable ? 1 : 0;
     p.kv_written = false;
     const CUtensorMap* map = reinterpret_cast<const CUtensorMap*>(p.tmap);
     void* args[] = {const_cast<CUtensorMap*>(map), &a};
-    cudaStream_t cs = static_cast<cudaStream_t>(stream);
     // Both kernels are programmatic dependents of whatever precedes them in
     // the stream: their launch overlaps the previous kernel's tail and each
     // waits (griddepcontrol.wait) before touching data that kernel may write.
