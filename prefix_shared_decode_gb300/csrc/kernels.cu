@@ -10,7 +10,8 @@
 // reductions on an fp16 pool; tensor cores, with the bytes widened straight
 // into fragments, on an fp8 pool with 64-token chunks; tensor cores too when
 // a position brings several query rows per key/value head: grouped query
-// heads or several query tokens); every
+// heads or several query tokens).  On an fp8 pool the chunk-first products
+// also take their operands straight from the E4M3 bytes.  Every
 // piece of work leaves a partial triple (o, m, s) that is
 // combined by the rescaled-sum rule of the explainer blog's "Two-Phase
 // Partition" section.
@@ -138,6 +139,14 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr));
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t r;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r) : "r"(addr));
+    return r;
+}
+__device__ __forceinline__ void lds64(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 __device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
@@ -511,11 +520,33 @@ __device__ __forceinline__ void sf_chunk_f8_tc(const uint8_t* kt, const uint8_t*
 // Scores of a 16-row block against NT tokens [tok0, tok0 + NT) of a chunk
 // tile, over the head dims [16 kk0, 16 kk1): S = Q K^T with the Q fragments
 // read from the swizzled Q tile (row lane%16, 16-byte chunk 2kk + lane/16).
-template <int C, int D, int NT>
+template <int C, int D, int NT, bool F8 = false>
 __device__ __forceinline__ void cf_scores(uint32_t kt, int tok0, uint32_t qrow_addr_base, int kk0, int kk1,
                                           float (&sacc)[NT / 8][4], int lane) {
 #pragma unroll
     for (int i = 0; i < NT / 8; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
+    if constexpr (F8) {
+        // E4M3 keys (128-byte rows, 16-byte chunk kk of row r at chunk
+        // kk ^ (r % 8)).  Inside each 16-dim step the fragment columns are
+        // permuted, 2t (+1) <-> dim 16kk + 4t (+1) and 2t + 8 (+9) <->
+        // 16kk + 4t + 2 (+3), on both operands: one 32-bit load gives a
+        // lane's four key bytes of token g, one 64-bit load its four query
+        // dims of a row.  The scores come out in the usual layout.
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int kk = kk0; kk < kk1; ++kk) {
+            uint32_t qa[4];
+            lds64(qrow_addr_base + swz(g, 2 * kk + (t >> 1), q_rows<D>()) + 8 * (t & 1), qa[0], qa[2]);
+            lds64(qrow_addr_base + swz(g + 8, 2 * kk + (t >> 1), q_rows<D>()) + 8 * (t & 1), qa[1], qa[3]);
+#pragma unroll
+            for (int j = 0; j < NT / 8; ++j) {
+                const int row = tok0 + 8 * j + g;
+                const uint32_t wd = lds32(kt + row * 128 + ((kk ^ (row & 7)) << 4) + 4 * t);
+                mma16816(sacc[j], qa, f16x2_from_e4m3x2(wd & 0xffffu), f16x2_from_e4m3x2(wd >> 16));
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int kk = kk0; kk < kk1; ++kk) {
         uint32_t qa[4];
@@ -538,7 +569,7 @@ __device__ __forceinline__ void cf_scores(uint32_t kt, int tok0, uint32_t qrow_a
 // Online softmax of a scored 16-row block (log2 units; columns past ntok,
 // and under the causal mask past each row's limit, are masked), then
 // O += P V for the OD output dims [16 dp0, 16 dp0 + OD).
-template <int C, int NT, int OD>
+template <int C, int NT, int OD, bool F8 = false>
 __device__ __forceinline__ void cf_softmax_pv(uint32_t vt, int ntok, int tok0, int ctx0, int lim0, int lim1,
                                               float scale_log2, float (&sacc)[NT / 8][4], int dp0,
                                               float (&m)[2], float (&s)[2], float (&o)[OD / 8][4], int lane) {
@@ -593,6 +624,36 @@ __device__ __forceinline__ void cf_softmax_pv(uint32_t vt, int ntok, int tok0, i
             o[dt][2] *= alpha[1]; o[dt][3] *= alpha[1];
         }
     }
+    if constexpr (F8) {
+        // E4M3 values: n-tile 4dq + i holds output dims 32dq + 4n + i
+        // (n = the fragment column), so a lane's B operand for dims
+        // 32dq + 4g .. + 3 of its four tokens (16j + 2t, + 1, + 8, + 9) is
+        // four 32-bit loads paired per dim by byte permutes.  The
+        // accumulator of lane (g, t) then holds dims 32dq + 8t .. + 7 of its
+        // rows: o[4dq + i][c] <-> dim 32dq + 8t + 4c' + i (c' = c % 2).
+        static_assert(OD == 128, "fp8 pools have head_dim 128");
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int j = 0; j < NT / 16; ++j) {
+            const int r0 = tok0 + 16 * j + 2 * t;
+#pragma unroll
+            for (int dq = 0; dq < 4; ++dq) {
+                const int kc = 2 * dq + (g >> 2);
+                const uint32_t off = 4 * (g & 3);
+                const uint32_t wa = lds32(vt + r0 * 128 + ((kc ^ (r0 & 7)) << 4) + off);
+                const uint32_t wb = lds32(vt + (r0 + 1) * 128 + ((kc ^ ((r0 + 1) & 7)) << 4) + off);
+                const uint32_t wc = lds32(vt + (r0 + 8) * 128 + ((kc ^ (r0 & 7)) << 4) + off);
+                const uint32_t wd = lds32(vt + (r0 + 9) * 128 + ((kc ^ ((r0 + 1) & 7)) << 4) + off);
+                const uint32_t x01 = __byte_perm(wa, wb, 0x5140), x23 = __byte_perm(wa, wb, 0x7362);
+                const uint32_t y01 = __byte_perm(wc, wd, 0x5140), y23 = __byte_perm(wc, wd, 0x7362);
+                mma16816(o[4 * dq + 0], pa[j], f16x2_from_e4m3x2(x01 & 0xffffu), f16x2_from_e4m3x2(y01 & 0xffffu));
+                mma16816(o[4 * dq + 1], pa[j], f16x2_from_e4m3x2(x01 >> 16), f16x2_from_e4m3x2(y01 >> 16));
+                mma16816(o[4 * dq + 2], pa[j], f16x2_from_e4m3x2(x23 & 0xffffu), f16x2_from_e4m3x2(y23 & 0xffffu));
+                mma16816(o[4 * dq + 3], pa[j], f16x2_from_e4m3x2(x23 >> 16), f16x2_from_e4m3x2(y23 >> 16));
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int j = 0; j < NT / 16; ++j) {
 #pragma unroll
@@ -608,13 +669,15 @@ __device__ __forceinline__ void cf_softmax_pv(uint32_t vt, int ntok, int tok0, i
 }
 
 // One warp, one 16-row block, NT tokens, every head dim.
-template <int C, int D, int NT>
+// F8: K and V are the stage's E4M3 bytes (head_dim 128), and o comes out
+// with its dims permuted as cf_softmax_pv describes.
+template <int C, int D, int NT, bool F8 = false>
 __device__ __forceinline__ void cf_chunk(uint32_t kt, uint32_t vt, int ntok, int tok0, int ctx0, int lim0,
                                          int lim1, uint32_t qrow_addr_base, float scale_log2,
                                          float (&m)[2], float (&s)[2], float (&o)[D / 8][4], int lane) {
     float sacc[NT / 8][4];
-    cf_scores<C, D, NT>(kt, tok0, qrow_addr_base, 0, D / 16, sacc, lane);
-    cf_softmax_pv<C, NT, D>(vt, ntok, tok0, ctx0, lim0, lim1, scale_log2, sacc, 0, m, s, o, lane);
+    cf_scores<C, D, NT, F8>(kt, tok0, qrow_addr_base, 0, D / 16, sacc, lane);
+    cf_softmax_pv<C, NT, D, F8>(vt, ntok, tok0, ctx0, lim0, lim1, scale_log2, sacc, 0, m, s, o, lane);
 }
 
 // head_dim 256: two warps share a 16-row block, warp `half` owning head dims
@@ -644,7 +707,8 @@ __device__ __forceinline__ void cf_chunk_split(uint32_t kt, uint32_t vt, int nto
 }
 
 // An fp8 chunk-head tile (C rows of 128 one-byte dims, 128-byte swizzled as
-// TMA stores it) widened to the fp16 tile layout the tensor-core code reads
+// TMA stores it) widened to the fp16 tile layout the transposed few-row
+// products read (chunk-first tiles read the bytes directly)
 // (two 64-dim boxes, each 128-byte swizzled).  E4M3 values are exact in fp16.
 // All consumer threads take part.
 template <int C>
@@ -664,7 +728,8 @@ __device__ __forceinline__ void f8_tile_to_f16(const uint8_t* src, uint8_t* dst,
 }
 
 // Shared-memory map of one CTA.  EB: bytes per stored K/V element (2 for
-// fp16, 1 for fp8, which adds an fp16 copy of one stage for the tensor cores).
+// fp16, 1 for fp8, which adds an fp16 copy of one stage for the transposed
+// few-row products).
 template <int C, int D, int EB>
 struct Smem {
     static constexpr int kTile = C * D * EB;    // one K or V tile of one chunk-head
@@ -1318,18 +1383,8 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                     uint32_t vt = kt + SM::kTile;
                     const int ntok = stage_ntok[st];
                     const int ctx0 = stage_tok0[st];
-                    if constexpr (EB == 1) {
-                        // Widen the stage into the fp16 copy (once every warp is
-                        // done with the previous one), then free the stage.
-                        consumer_sync();
-                        const uint8_t* sk = stages + (size_t)st * SM::kStage;
-                        f8_tile_to_f16<C>(sk, conv, threadIdx.x);
-                        f8_tile_to_f16<C>(sk + SM::kTile, conv + SM::kConvBytes / 2, threadIdx.x);
-                        consumer_sync();
-                        if (lane == 0) mbar_arrive(empty0 + 8 * st);
-                        kt = smem_u32(conv);
-                        vt = kt + SM::kConvBytes / 2;
-                    }
+                    // an fp8 stage is read as E4M3 bytes, straight into the
+                    // fragments (cf_chunk<..., true>)
                     if constexpr (kSplit) {
                         if (active) {
                             constexpr int kXs = (C / 8) * 4 * 32;     // floats per warp slot
@@ -1340,19 +1395,17 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                         }
                     } else if (active) {
                         if (NTw == 16) {
-                            cf_chunk<C, D, 16>(kt, vt, ntok, tp * 16, ctx0, lim[0], lim[1], qblock, p.scale_log2,
-                                               m, s, o, lane);
+                            cf_chunk<C, D, 16, EB == 1>(kt, vt, ntok, tp * 16, ctx0, lim[0], lim[1], qblock,
+                                                        p.scale_log2, m, s, o, lane);
                         } else if constexpr (C >= 32) {
                             // 32 tokens at a time keeps the score tile in registers
                             for (int t0 = tp * NTw; t0 < (tp + 1) * NTw; t0 += 32)
-                                cf_chunk<C, D, 32>(kt, vt, ntok, t0, ctx0, lim[0], lim[1], qblock, p.scale_log2,
-                                                   m, s, o, lane);
+                                cf_chunk<C, D, 32, EB == 1>(kt, vt, ntok, t0, ctx0, lim[0], lim[1], qblock,
+                                                            p.scale_log2, m, s, o, lane);
                         }
                     }
-                    if constexpr (EB == 2) {
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(empty0 + 8 * st);
-                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty0 + 8 * st);
                 }
                 // Row sums are per thread so far: reduce over the quad.
 #pragma unroll
@@ -1417,10 +1470,23 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                             const int pos = q_lo + row / RW, jq = (row % RW) / G, qh = kvh * G + row % G;
                             const int pid = p.pbase[((size_t)pos * QL + jq) * H + qh] + upart;
                             float* dst = p.part_o + (size_t)pid * D + dhalf * OD;
+                            if constexpr (EB == 1) {
+                                // o[4dq + i][2r + c] holds dim 32dq + 8t + 4c + i
 #pragma unroll
-                            for (int dt = 0; dt < OD / 8; ++dt)
-                                *reinterpret_cast<float2*>(dst + dt * 8 + 2 * t4) =
-                                    make_float2(o[dt][2 * r], o[dt][2 * r + 1]);
+                                for (int dq = 0; dq < OD / 32; ++dq) {
+                                    *reinterpret_cast<float4*>(dst + 32 * dq + 8 * t4) =
+                                        make_float4(o[4 * dq][2 * r], o[4 * dq + 1][2 * r], o[4 * dq + 2][2 * r],
+                                                    o[4 * dq + 3][2 * r]);
+                                    *reinterpret_cast<float4*>(dst + 32 * dq + 8 * t4 + 4) =
+                                        make_float4(o[4 * dq][2 * r + 1], o[4 * dq + 1][2 * r + 1],
+                                                    o[4 * dq + 2][2 * r + 1], o[4 * dq + 3][2 * r + 1]);
+                                }
+                            } else {
+#pragma unroll
+                                for (int dt = 0; dt < OD / 8; ++dt)
+                                    *reinterpret_cast<float2*>(dst + dt * 8 + 2 * t4) =
+                                        make_float2(o[dt][2 * r], o[dt][2 * r + 1]);
+                            }
                             if (t4 == 0 && dhalf == 0) p.part_ms[pid] = make_float2(m[r], s[r]);
                         }
                     }

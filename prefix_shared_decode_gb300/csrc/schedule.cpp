@@ -187,10 +187,11 @@ int build_tables(const Pool& p, const int64_t* seq_ids, int32_t b, uint32_t flag
 // ---------------------------------------------------------------------------
 namespace {
 constexpr double kCfComputePer16 = 0.2;
-// fp8 pools: a chunk-first tile against a sequence-first one (the latter on
-// tensor cores straight from the E4M3 bytes, the former widened to fp16
-// first); swept on GB300 (1.6 .. 3.2) for the fastest calls
-constexpr double kF8CfFactor = 2.8;
+// fp8 pools: a chunk-first tile against a single-row sequence-first one
+// (both on the tensor cores straight from the E4M3 bytes; the chunk-first
+// tile carries m query rows of work on half the bytes of an fp16 tile);
+// swept on GB300 (1.5 .. 2.8) for the fastest calls
+constexpr double kF8CfFactor = 2.0;
 
 // Share of the sequence-first tiles left to the tail queue that CTAs drain
 // dynamically once their static lists are done (absorbs the run-to-run rate
@@ -212,11 +213,9 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, int32_t q_len, Pla
     const int32_t D = p.cfg.head_dim, c = p.cfg.chunk, b = t.b;
     plan.q_len = q_len;
     const double sf_cost = (RW == 1) ? 1.0 : 1.0 + kCfComputePer16 * ((RW + 15) / 16);
-    // An fp8 pool halves a tile's bytes, but the chunk-first path widens each
-    // tile to fp16 in shared memory first while single-row sequence-first
-    // tiles go to the tensor cores straight from the bytes, so there (and
-    // only there) a chunk-first tile costs more relative to a sequence-first
-    // one.
+    // An fp8 pool halves a tile's bytes while the chunk-first tensor work per
+    // tile stays the same, so against single-row sequence-first tiles (and
+    // only there) a chunk-first tile costs more.
     const double cf_mult = ((p.cfg.flags & CA_KV_FP8) && RW == 1) ? kF8CfFactor : 1.0;
     auto rows_cost = [&](int32_t m_rows) {
         return cf_mult * (1.0 + kCfComputePer16 * ((m_rows + 15) / 16)) / sf_cost;
