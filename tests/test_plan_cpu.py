@@ -230,3 +230,32 @@ def test_multi_token_schedule_limits(lib):
     assert e.value.name == "CA_ERR_INVALID"
     pool.schedule([0, 1], q_len=4)                                       # no mask: fine
     assert len(pool.schedule([0], q_len=16).plan()["pbase"]) == 16 * 8 + 1
+
+
+def test_schedule_reuse_fast_path_and_staleness_key(lib):
+    """The per-step ``pool.schedule(batch, reuse=s)`` keeps the batch's int64
+    copy; a batch list changed in place, or another list, is converted again
+    (the tables follow the new batch).  ``Schedule._key`` (what a captured
+    CUDA graph is checked against) stays put across appends that fit the
+    partial last chunks and changes when a chunk grows or the batch changes."""
+    from prefix_shared_decode_gb300 import Pool
+    c, H, D = 16, 2, 64
+    pool = Pool(1, H, D, c, 200, host_only=True)
+    shared = list(range(2 * c))
+    for i in range(4):
+        pool.insert(i, shared + [1000 + 100 * i + j for j in range(c // 2 + i)])
+    batch = [0, 1, 2, 3]
+    s = pool.schedule(batch)
+    key, perm = s._key(), s.tables()["seq_perm"].copy()
+    assert pool.schedule(batch, reuse=s) is s and s._key() == key
+    assert pool.append(2, [5000]) == 0                      # fits the partial last chunk
+    assert pool.schedule(list(batch), reuse=s)._key() == key
+    batch.reverse()                                          # the same list object, changed in place
+    pool.schedule(batch, reuse=s)
+    assert s._key() != key
+    np.testing.assert_array_equal(s.tables()["seq_perm"], [3 - p for p in perm])
+    key = s._key()
+    assert pool.append(0, [6000 + j for j in range(c)]) == 1  # grows a chunk
+    assert s._key() != key
+    pool.schedule(batch, reuse=s)
+    assert s._key() != key and pool.schedule(batch, reuse=s)._key() == s._key()
