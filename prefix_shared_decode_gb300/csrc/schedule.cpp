@@ -12,7 +12,8 @@
 //  * merge lists: the runs covering each position.
 //
 // Plan (GB300-specific, verified through the outputs): chunk-first runs are
-// cut into units of at most 64 query rows (32 at head_dim 256) and a balanced
+// cut into units of at most 64 query rows (32 at head_dim 256, and in small
+// calls whose positions bring several rows each) and a balanced
 // number of chunks; sequence-first chunk-heads are spread over the CTAs in
 // contiguous pieces so that every CTA gets the same estimated time, with a
 // tail of small units that CTAs claim dynamically.
@@ -202,6 +203,11 @@ constexpr int32_t kTailUnitsPerCta = 2;     // aim: about this many queue units 
 // (its claim, query load, partial writes and one more partial to merge),
 // which two-tile units did not amortise (measured: 2% slower calls).
 constexpr int32_t kTailUnitMin = 4, kTailUnitMax = 8;
+// Below this many tiles per CTA, positions with several query rows take
+// chunk-first groups of at most 32 rows (measured on GB300: a grouped-query
+// call of ~8 tiles per CTA 21.5 -> 19.3 us; a multi-token call of ~32 tiles
+// per CTA was 1% slower with them).
+constexpr double kSmallCallTiles = 16.0;
 }  // namespace
 
 void build_plan(const Pool& p, const Tables& t, int32_t grid, int32_t q_len, Plan& plan) {
@@ -239,14 +245,27 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, int32_t q_len, Pla
         plan.chunk_tok0[R + i] = t.sf_tok0[i];
     }
 
-    // Totals for the per-CTA budget.
-    double sf_total = (double)(t.sf_chunks.size() / 2) * H;
-    double cf_total = 0;
-    for (int32_t u = 0; u < U; ++u) {
-        const int32_t nrows = t.cf_runs[4 * u + 1], m = t.cf_runs[4 * u + 3] - t.cf_runs[4 * u + 2];
-        const int32_t max_pos = std::max(1, max_query_rows(p.cfg) / RW);
-        const int32_t ngroups = (m + max_pos - 1) / max_pos;
-        cf_total += (double)nrows * H * ngroups * rows_cost((m + ngroups - 1) / ngroups * RW);
+    // Totals for the per-CTA budget.  Chunk-first query groups take at most
+    // max_query_rows rows; when positions bring several rows each (RW > 1)
+    // and the call is small (under kSmallCallTiles tiles per CTA), groups of
+    // at most 32 rows instead: twice the units, so the CTAs holding the
+    // chunk-first work no longer finish long after the rest.
+    const double sf_total = (double)(t.sf_chunks.size() / 2) * H;
+    int32_t group_rows = max_query_rows(p.cfg);
+    auto cf_cost_total = [&] {
+        double total = 0;
+        for (int32_t u = 0; u < U; ++u) {
+            const int32_t nrows = t.cf_runs[4 * u + 1], m = t.cf_runs[4 * u + 3] - t.cf_runs[4 * u + 2];
+            const int32_t max_pos = std::max(1, group_rows / RW);
+            const int32_t ngroups = (m + max_pos - 1) / max_pos;
+            total += (double)nrows * H * ngroups * rows_cost((m + ngroups - 1) / ngroups * RW);
+        }
+        return total;
+    };
+    double cf_total = cf_cost_total();
+    if (RW > 1 && group_rows > 32 && (sf_total + cf_total) < kSmallCallTiles * grid) {
+        group_rows = 32;
+        cf_total = cf_cost_total();
     }
     const int32_t tiles_ceiling = (int32_t)std::max(1.0, sf_total + cf_total);
     grid = std::max(1, std::min(grid, tiles_ceiling));
@@ -263,8 +282,8 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, int32_t q_len, Pla
     for (int32_t u = 0; u < U; ++u) {
         const int32_t row0 = t.cf_runs[4 * u], nrows = t.cf_runs[4 * u + 1];
         const int32_t lo = t.cf_runs[4 * u + 2], hi = t.cf_runs[4 * u + 3], m = hi - lo;
-        // query groups of at most 64 (32 at head_dim 256) (position, query token, query head) rows
-        const int32_t max_pos = std::max(1, max_query_rows(p.cfg) / RW);
+        // query groups of at most group_rows (position, query token, query head) rows
+        const int32_t max_pos = std::max(1, group_rows / RW);
         const int32_t ngroups = (m + max_pos - 1) / max_pos;
         const int32_t mg = (m + ngroups - 1) / ngroups;
         const double row_cost = rows_cost(mg * RW);
