@@ -377,7 +377,7 @@ def run_ours(args):
     kern_ms = [a.elapsed_time(z) for a, z in kev]
     kern_ms_avg = sum(kern_ms) / len(kern_ms)
 
-    # The survey's own method, beside the back-to-back number: one call at a
+    # An isolated-call measure beside the back-to-back number: one call at a
     # time, CUDA events around the call only, 20 warm-up calls then the
     # median of 200, L2 flushed (a 2 x L2 buffer written) before every call,
     # outside the event pair.
