@@ -475,7 +475,7 @@ def run_ours(args):
         context = {"paged_flat_us": round(us_flat, 2), "paged_shared_no_tpp_us": round(us_no_tpp, 2),
                    "note": "same kernel with every chunk sequence-first: flat = private copy of the "
                            "prefix per sequence (PagedAttention layout), shared_no_tpp = one copy read "
-                           "once per sharer (the pages' PagedAttn*)"}
+                           "once per sharer (ChunkAttention's PagedAttn* comparator)"}
 
     if world > 1 and rank != 0:
         torch.distributed.destroy_process_group()
@@ -505,7 +505,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": ("f16 q/out, fp8 e4m3 K/V storage (fp32 accumulate)" if wl.kv_dtype == "fp8"
                   else "f16 (fp32 accumulate)"),
-        "data": "synthetic (seeded N(0,1) fp16 Q/K/V; token segments shaped like the pages' shared system prompts)",
+        "data": "synthetic (seeded N(0,1) fp16 Q/K/V; token segments shaped like ChunkAttention's shared system prompts)",
         "config": {"workload": wl.name, "description": wl.description, "batch": b, "q_len": wl.q_len,
                    "n_heads": H,
                    "n_kv_heads": HK,
@@ -581,7 +581,7 @@ def run_reference(args):
            "config": {"workload": wl.name, "description": wl.description},
            "cpu_baseline": cb,
            "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-           "note": "the pages publish no code: the reference arm is the fp64 CPU oracle, timed on a "
+           "note": "ChunkAttention's pages publish no code: the reference arm is the fp64 CPU oracle, timed on a "
                    "bounded sample and scaled to one layer call"}
     print(json.dumps(res), flush=True)
 
