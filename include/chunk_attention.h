@@ -86,12 +86,13 @@ extern "C" {
 typedef struct ca_pool  ca_pool;
 typedef struct ca_sched ca_sched;
 
-/* Shape of a pool.  head_dim must be 64 or 128, chunk 16, 32 or 64 tokens
- * (the paper's kernel default is 64 [CA §4.1]); n_layers, n_heads and
- * capacity_slots >= 1.  n_kv_heads: key/value heads stored in the pool
- * (grouped-query attention: query head h reads key/value head
- * h / (n_heads / n_kv_heads)); 0 means n_heads; n_heads must be a multiple
- * of it and the group n_heads / n_kv_heads at most 64. */
+/* Shape of a pool [CA §3.1: K/V tensors cut into chunks of c tokens].
+ * head_dim 64, 128 or 256 (256 only with chunks of 16 or 32 tokens and an
+ * fp16 pool); chunk 16, 32 or 64 tokens (the paper's kernel default is 64
+ * [CA §4.1]); n_layers, n_heads and capacity_slots >= 1.  Other shapes give
+ * CA_ERR_UNSUPPORTED, bad counts or unknown flags CA_ERR_INVALID.  A pool
+ * made from this struct has one key/value head per query head and (with
+ * CA_KV_FP8) scales of 1; ca_pool_config_ex sets those too. */
 typedef struct {
     int32_t  n_layers;
     int32_t  n_heads;         /* query heads (q and out)                       */
@@ -99,11 +100,26 @@ typedef struct {
     int32_t  chunk;           /* c: tokens per chunk                           */
     int32_t  capacity_slots;  /* chunk slots in the device pool                */
     uint32_t flags;           /* CA_NO_SHARING | CA_KV_FP8, or 0               */
+} ca_pool_config;
+
+/* ca_pool_config plus the variants the summary's tuning discussion leaves
+ * open [CA §7, Model and Hardware Compatibility].  n_kv_heads: key/value
+ * heads stored in the pool (grouped-query attention: query head h reads
+ * key/value head h / (n_heads / n_kv_heads)); 0 means n_heads; n_heads must
+ * be a multiple of it and the group n_heads / n_kv_heads at most 64 (32 at
+ * head_dim 256).  k_scale / v_scale: the CA_KV_FP8 scales (0 means 1.0;
+ * ignored without CA_KV_FP8). */
+typedef struct {
+    ca_pool_config base;
     int32_t  n_kv_heads;      /* key/value heads (0: n_heads)                  */
     float    k_scale;         /* CA_KV_FP8 only: key scale (0: 1.0)            */
     float    v_scale;         /* CA_KV_FP8 only: value scale (0: 1.0)          */
-} ca_pool_config;
+} ca_pool_config_ex;
 
+/* Occupancy of a pool (ca_pool_stats).  The storage model of prefix
+ * sharing [CA-blog, Prefix-Aware KV Cache: a shared prefix of L_p tokens and
+ * N private suffixes of L_s tokens take L_p + N * L_s token slots instead of
+ * N * (L_p + L_s)] is what live_slots counts, in chunks. */
 typedef struct {
     int64_t live_slots;       /* slots holding a chunk                         */
     int64_t free_slots;
@@ -122,8 +138,11 @@ typedef struct {
  * decode-time append can grow a partial chunk without a new schedule).
  */
 
-/* Bytes of device memory a pool with this shape needs (for kv_dev). */
+/* Bytes of device memory a pool with this shape needs (for kv_dev).
+ * Errors: as ca_pool_create's shape checks; CA_ERR_INVALID if bytes_out is
+ * NULL.  [CA §3.1: the chunks live in one preallocated pool.] */
 int ca_pool_bytes(const ca_pool_config* cfg, size_t* bytes_out);
+int ca_pool_bytes_ex(const ca_pool_config_ex* cfg, size_t* bytes_out);
 
 /* Create a pool over caller-owned device memory kv_dev of kv_bytes >=
  * ca_pool_bytes(cfg); kv_dev must be 1024-byte aligned and must outlive the
@@ -132,6 +151,9 @@ int ca_pool_bytes(const ca_pool_config* cfg, size_t* bytes_out);
  * CA_ERR_INVALID).  [CA §3.1: chunked KV tensors in a prefix tree.] */
 int ca_pool_create(const ca_pool_config* cfg, void* kv_dev, size_t kv_bytes,
                    ca_pool** pool_out);
+/* The same with the grouped-query and fp8 fields (ca_pool_config_ex). */
+int ca_pool_create_ex(const ca_pool_config_ex* cfg, void* kv_dev, size_t kv_bytes,
+                      ca_pool** pool_out);
 int ca_pool_destroy(ca_pool* pool);
 
 /* Leading tokens of tokens[0..n) whose K/V the pool already holds: the
@@ -197,6 +219,8 @@ int ca_remove_seq(ca_pool* pool, int64_t seq_id);
  * unknown, CA_ERR_INVALID if an id repeats. */
 int ca_remove_batch(ca_pool* pool, int32_t n_seqs, const int64_t* seq_ids);
 
+/* Occupancy counters (ca_stats above); host only, never touches the GPU.
+ * CA_ERR_INVALID on NULL arguments. */
 int ca_pool_stats(const ca_pool* pool, ca_stats* out);
 
 /* Slots along seq_id's path, root first (test and inspection helper).
@@ -217,9 +241,10 @@ int ca_seq_slots(const ca_pool* pool, int64_t seq_id, int32_t* slots, int32_t ca
  * Errors: CA_ERR_NOT_FOUND (unknown seq_id), CA_ERR_INVALID (b < 1, duplicate
  * ids), CA_ERR_CUDA. */
 int ca_build_schedule(ca_pool* pool, const int64_t* seq_ids, int32_t b,
-                      uint32_t flags, ca_sched** inout, void* stream);
+                      ca_sched** inout, void* stream);
 
-/* The same for q_len query tokens per sequence (multi-token queries: draft
+/* The same with flags (CA_SCHED_NO_TPP, CA_SCHED_CAUSAL; 0 is
+ * ca_build_schedule) and q_len query tokens per sequence (multi-token queries: draft
  * tokens to verify, or a chunk of prompt prefilled over the trie).  The
  * blog's two-phase function takes queries of any length [CA-blog, Two-Phase
  * Partition: queries (batch, heads, seq_len, d_k)] and lets every query
@@ -228,7 +253,7 @@ int ca_build_schedule(ca_pool* pool, const int64_t* seq_ids, int32_t b,
  * tokens attends to tokens [0, n - q_len + j] only — the form for tokens
  * whose own K/V the caller has already appended.  q and out of the decode
  * calls are then [b][q_len][n_heads][head_dim] (row i*q_len + j is token j
- * of seq_ids[i]).  q_len = 1 is ca_build_schedule.  Requires
+ * of seq_ids[i]).  q_len = 1 with flags 0 is ca_build_schedule.  Requires
  * q_len * (n_heads / n_kv_heads) <= 64 (CA_ERR_UNSUPPORTED otherwise) and,
  * with CA_SCHED_CAUSAL, every context at least q_len tokens long
  * (CA_ERR_INVALID otherwise); other errors as ca_build_schedule. */
@@ -237,6 +262,9 @@ int ca_build_schedule_ex(ca_pool* pool, const int64_t* seq_ids, int32_t b, int32
 int ca_sched_destroy(ca_sched* sched);
 
 /* Table sizes, then the tables themselves (host copies; for bit-exact tests).
+ * These are the per-step context the pages describe [CA §3.2: which chunks
+ * the chunk-first phase takes and for which range of sequences; CA §3.3:
+ * the context is kept until the tree changes], exported as built.
  * counts[0..5] = b, R (chunk-first rows), U (runs), S (sequence-first
  * chunks), M (merge entries), n_units (kernel work units). */
 int ca_sched_counts(const ca_sched* sched, int32_t counts[6]);
@@ -272,7 +300,10 @@ int ca_export_plan(const ca_sched* sched, int32_t counts[4], int32_t* units,
                    int32_t* cta_begin, int32_t* pbase, int32_t* chunks);
 
 /* Bytes of caller-owned device workspace ca_decode_attention needs for this
- * schedule (the partial results of the two phases). */
+ * schedule: one partial triple (o: head_dim fp32, m, s: fp32) per piece of
+ * work and (sequence, query token, head) it covers — the per-phase partial
+ * results that the output-combination rule merges [CA-blog, Two-Phase
+ * Partition; CA §3.2].  CA_ERR_INVALID on NULL arguments. */
 int ca_workspace_bytes(const ca_sched* sched, size_t* bytes_out);
 
 /* ---- decode attention -----------------------------------------------------
@@ -344,7 +375,9 @@ int ca_decode_attention_host(const ca_pool* pool, const ca_sched* sched,
  * still passes q_dev and out_dev as for ca_decode_attention.
  *   - The first call on a device looks up the buffer's device address
  *     (cudaGetSymbolAddress); make that first call outside any stream
- *     capture.  The pool's device must be current.
+ *     capture.  The pool's device must be current.  The address is kept
+ *     for the life of the process, so resetting a device (cudaDeviceReset)
+ *     after its first call is not supported.
  *   - Every call shares the one buffer: calls that overlap on the GPU
  *     (other streams, other host threads) race and corrupt each other's
  *     results.  Nothing in the buffer needs clearing between calls.
@@ -373,6 +406,9 @@ int ca_sched_set_profile_events(ca_sched* sched, void* event_begin, void* event_
  * NULL. */
 int ca_kernel_launches(uint64_t* count_out);
 
+/* A static, human-readable name for a status code ("unknown status" for
+ * codes this header does not define); never NULL.  The pages have no
+ * counterpart: it only serves callers of this library. */
 const char* ca_error_string(int status);
 
 #ifdef __cplusplus

@@ -63,14 +63,14 @@ class Pool:
         if kv_dtype not in ("fp16", "fp8"):
             raise ValueError("kv_dtype must be 'fp16' or 'fp8'")
         flags = (capi.CA_NO_SHARING if no_sharing else 0) | (capi.CA_KV_FP8 if kv_dtype == "fp8" else 0)
-        self.cfg = capi.PoolConfig(n_layers, n_heads, head_dim, chunk, capacity_slots, flags,
-                                   n_kv_heads or 0, float(k_scale), float(v_scale))
+        self.cfg = capi.PoolConfigEx(capi.PoolConfig(n_layers, n_heads, head_dim, chunk, capacity_slots, flags),
+                                     n_kv_heads or 0, float(k_scale), float(v_scale))
         self.kv_dtype, self.k_scale, self.v_scale = kv_dtype, float(k_scale), float(v_scale)
         self.n_layers, self.n_heads, self.head_dim, self.chunk = n_layers, n_heads, head_dim, chunk
         self.n_kv_heads = n_kv_heads or n_heads
         self.capacity_slots = capacity_slots
         nbytes = C.c_size_t()
-        check(L.ca_pool_bytes(C.byref(self.cfg), C.byref(nbytes)), "ca_pool_bytes")
+        check(L.ca_pool_bytes_ex(C.byref(self.cfg), C.byref(nbytes)), "ca_pool_bytes_ex")
         self.kv_bytes = nbytes.value
         self._kv = None
         ptr = None
@@ -84,7 +84,7 @@ class Pool:
             self._kv_offset = ptr - base
         self.host_only = host_only
         h = C.c_void_p()
-        check(L.ca_pool_create(C.byref(self.cfg), ptr, self.kv_bytes, C.byref(h)), "ca_pool_create")
+        check(L.ca_pool_create_ex(C.byref(self.cfg), ptr, self.kv_bytes, C.byref(h)), "ca_pool_create_ex")
         self._h = h
 
     def __del__(self):

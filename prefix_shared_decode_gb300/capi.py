@@ -25,7 +25,7 @@ CA_SCHED_CAUSAL = 2
 
 # Every symbol the header declares, in header order.
 EXPORTS = [
-    "ca_pool_bytes", "ca_pool_create", "ca_pool_destroy", "ca_match_prefix", "ca_insert_tokens",
+    "ca_pool_bytes", "ca_pool_bytes_ex", "ca_pool_create", "ca_pool_create_ex", "ca_pool_destroy", "ca_match_prefix", "ca_insert_tokens",
     "ca_insert_batch", "ca_append_tokens", "ca_remove_seq", "ca_remove_batch", "ca_pool_stats", "ca_seq_slots", "ca_build_schedule", "ca_build_schedule_ex", "ca_sched_destroy",
     "ca_sched_counts", "ca_export_tables", "ca_export_plan", "ca_workspace_bytes", "ca_decode_attention",
     "ca_workspace_bytes_host", "ca_decode_attention_host", "ca_decode_attention_static_ws",
@@ -35,9 +35,15 @@ EXPORTS = [
 
 
 class PoolConfig(C.Structure):
+    """ca_pool_config."""
     _fields_ = [("n_layers", C.c_int32), ("n_heads", C.c_int32), ("head_dim", C.c_int32),
-                ("chunk", C.c_int32), ("capacity_slots", C.c_int32), ("flags", C.c_uint32),
-                ("n_kv_heads", C.c_int32), ("k_scale", C.c_float), ("v_scale", C.c_float)]
+                ("chunk", C.c_int32), ("capacity_slots", C.c_int32), ("flags", C.c_uint32)]
+
+
+class PoolConfigEx(C.Structure):
+    """ca_pool_config_ex: a ca_pool_config, then the grouped-query and fp8 fields."""
+    _fields_ = [("base", PoolConfig), ("n_kv_heads", C.c_int32), ("k_scale", C.c_float),
+                ("v_scale", C.c_float)]
 
 
 class Stats(C.Structure):
@@ -69,7 +75,9 @@ def lib() -> C.CDLL:
     P = C.POINTER
     sig = {
         "ca_pool_bytes": [P(PoolConfig), P(sz)],
+        "ca_pool_bytes_ex": [P(PoolConfigEx), P(sz)],
         "ca_pool_create": [P(PoolConfig), vp, sz, P(vp)],
+        "ca_pool_create_ex": [P(PoolConfigEx), vp, sz, P(vp)],
         "ca_pool_destroy": [vp],
         "ca_match_prefix": [vp, P(i32), i32, P(i32)],
         "ca_insert_tokens": [vp, i64, P(i32), i32, vp, vp, vp, P(i32)],
@@ -79,7 +87,7 @@ def lib() -> C.CDLL:
         "ca_remove_batch": [vp, i32, P(i64)],
         "ca_pool_stats": [vp, P(Stats)],
         "ca_seq_slots": [vp, i64, P(i32), i32, P(i32)],
-        "ca_build_schedule": [vp, P(i64), i32, u32, P(vp), vp],
+        "ca_build_schedule": [vp, P(i64), i32, P(vp), vp],
         "ca_build_schedule_ex": [vp, vp, i32, i32, u32, P(vp), vp],     # seq_ids: int64 array address
         "ca_sched_destroy": [vp],
         "ca_sched_counts": [vp, P(i32)],

@@ -34,6 +34,24 @@ namespace ca {
 // ---------------------------------------------------------------------------
 enum : int32_t { UNIT_CF = 0, UNIT_SF = 1 };
 
+// The full shape of a pool: the public ca_pool_config_ex flattened (its
+// ca_pool_config fields, then the grouped-query and fp8 fields).
+struct PoolCfg {
+    int32_t n_layers, n_heads, head_dim, chunk, capacity_slots;
+    uint32_t flags;
+    int32_t n_kv_heads;
+    float k_scale, v_scale;
+};
+inline PoolCfg pool_cfg(const ca_pool_config_ex& e) {
+    return {e.base.n_layers, e.base.n_heads, e.base.head_dim, e.base.chunk, e.base.capacity_slots,
+            e.base.flags,    e.n_kv_heads,   e.k_scale,       e.v_scale};
+}
+inline PoolCfg pool_cfg(const ca_pool_config& b) {
+    ca_pool_config_ex e{};
+    e.base = b;
+    return pool_cfg(e);
+}
+
 struct ChunkRef {      // one chunk the kernel reads
     int32_t slot;      // pool slot
     int32_t ntok;      // valid tokens in it (1..c)
@@ -121,7 +139,7 @@ struct Sequence {
 };
 
 struct Pool {
-    ca_pool_config cfg{};
+    PoolCfg cfg{};
     void* kv = nullptr;            // device pool (nullptr: host only)
     size_t kv_bytes = 0;
     int device = -1;
@@ -203,17 +221,17 @@ struct ScatterChunk {
 
 // Key/value heads of a pool (grouped-query attention; 0 in the config means
 // one per query head).
-inline int32_t kv_heads(const ca_pool_config& c) { return c.n_kv_heads > 0 ? c.n_kv_heads : c.n_heads; }
+inline int32_t kv_heads(const PoolCfg& c) { return c.n_kv_heads > 0 ? c.n_kv_heads : c.n_heads; }
 
 // Device bytes of the pool: the K/V tiles, then the per-slot token counts.
 // Bytes per stored K/V element (fp16, or 1 for an FP8 pool) and the
 // effective dequantisation scales.
-inline int kv_elem_bytes(const ca_pool_config& c) { return (c.flags & CA_KV_FP8) ? 1 : 2; }
+inline int kv_elem_bytes(const PoolCfg& c) { return (c.flags & CA_KV_FP8) ? 1 : 2; }
 inline float kv_scale_of(float s) { return s == 0.f ? 1.f : s; }
 // Query rows one tensor-core unit takes: 64, or 32 at head_dim 256.
-inline int32_t max_query_rows(const ca_pool_config& c) { return c.head_dim == 256 ? 32 : 64; }
-size_t pool_tile_bytes(const ca_pool_config& c);
-size_t pool_total_bytes(const ca_pool_config& c);
+inline int32_t max_query_rows(const PoolCfg& c) { return c.head_dim == 256 ? 32 : 64; }
+size_t pool_tile_bytes(const PoolCfg& c);
+size_t pool_total_bytes(const PoolCfg& c);
 
 // What an append changed, so that a failed copy launch can undo it.
 struct AppendUndo {
@@ -244,8 +262,8 @@ void layout_plan(const Plan& plan, int32_t b, PlanLayout& lay, std::vector<unsig
 void layout_ws(const Plan& plan, const Pool& p, int32_t b, WsLayout& ws);
 
 // kernels.cu
-int kernel_smem_bytes(const ca_pool_config& c, int* n_stages, size_t* bytes);
-int kernel_ctas_per_sm(const ca_pool_config& c, int* ctas);
+int kernel_smem_bytes(const PoolCfg& c, int* n_stages, size_t* bytes);
+int kernel_ctas_per_sm(const PoolCfg& c, int* ctas);
 int make_tensor_map(Pool& p);
 int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_rows,
                    const std::vector<ScatterChunk>& chunks, void* stream);

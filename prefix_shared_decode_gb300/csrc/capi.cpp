@@ -31,7 +31,7 @@ int guard(F&& f) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int check_cfg(const ca_pool_config* c) {
+int check_cfg(const PoolCfg* c) {
     if (!c) return CA_ERR_INVALID;
     if (c->n_layers < 1 || c->n_heads < 1 || c->capacity_slots < 1) return CA_ERR_INVALID;
     if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return CA_ERR_UNSUPPORTED;
@@ -53,7 +53,7 @@ int check_cfg(const ca_pool_config* c) {
     return CA_OK;
 }
 
-size_t pool_bytes(const ca_pool_config& c) { return pool_total_bytes(c); }
+size_t pool_bytes(const PoolCfg& c) { return pool_total_bytes(c); }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? CA_OK : CA_ERR_CUDA; }
 
@@ -82,16 +82,28 @@ int upload_plan(Sched& s, cudaStream_t stream) {
 
 extern "C" {
 
-int ca_pool_bytes(const ca_pool_config* cfg, size_t* bytes_out) {
-    int st = check_cfg(cfg);
+int ca_pool_bytes_ex(const ca_pool_config_ex* cfg_ex, size_t* bytes_out) {
+    if (!cfg_ex) return CA_ERR_INVALID;
+    const PoolCfg cfg = pool_cfg(*cfg_ex);
+    int st = check_cfg(&cfg);
     if (st) return st;
     if (!bytes_out) return CA_ERR_INVALID;
-    *bytes_out = pool_bytes(*cfg);
+    *bytes_out = pool_bytes(cfg);
     return CA_OK;
 }
 
-int ca_pool_create(const ca_pool_config* cfg, void* kv_dev, size_t kv_bytes, ca_pool** pool_out) {
+int ca_pool_bytes(const ca_pool_config* cfg, size_t* bytes_out) {
+    if (!cfg) return CA_ERR_INVALID;
+    ca_pool_config_ex e{};
+    e.base = *cfg;
+    return ca_pool_bytes_ex(&e, bytes_out);
+}
+
+int ca_pool_create_ex(const ca_pool_config_ex* cfg_ex, void* kv_dev, size_t kv_bytes, ca_pool** pool_out) {
     return guard([&] {
+        if (!cfg_ex) return CA_ERR_INVALID;
+        const PoolCfg c = pool_cfg(*cfg_ex);
+        const PoolCfg* cfg = &c;
         int st = check_cfg(cfg);
         if (st) return st;
         if (!pool_out) return CA_ERR_INVALID;
@@ -119,6 +131,13 @@ int ca_pool_create(const ca_pool_config* cfg, void* kv_dev, size_t kv_bytes, ca_
         *pool_out = p.release();
         return CA_OK;
     });
+}
+
+int ca_pool_create(const ca_pool_config* cfg, void* kv_dev, size_t kv_bytes, ca_pool** pool_out) {
+    if (!cfg) return CA_ERR_INVALID;
+    ca_pool_config_ex e{};
+    e.base = *cfg;
+    return ca_pool_create_ex(&e, kv_dev, kv_bytes, pool_out);
 }
 
 int ca_pool_destroy(ca_pool* pool) {
@@ -246,10 +265,8 @@ int ca_seq_slots(const ca_pool* pool, int64_t seq_id, int32_t* slots, int32_t ca
     return CA_OK;
 }
 
-int ca_build_schedule(ca_pool* pool, const int64_t* seq_ids, int32_t b, uint32_t flags,
-                      ca_sched** inout, void* stream) {
-    if (flags & ~CA_SCHED_NO_TPP) return CA_ERR_INVALID;
-    return ca_build_schedule_ex(pool, seq_ids, b, 1, flags, inout, stream);
+int ca_build_schedule(ca_pool* pool, const int64_t* seq_ids, int32_t b, ca_sched** inout, void* stream) {
+    return ca_build_schedule_ex(pool, seq_ids, b, 1, 0u, inout, stream);
 }
 
 int ca_build_schedule_ex(ca_pool* pool, const int64_t* seq_ids, int32_t b, int32_t q_len, uint32_t flags,

@@ -1582,7 +1582,7 @@ void* kernel_ptr(bool rows) {
 }
 // rows: the schedule brings 2..8 query rows per position and key/value head
 // (the few-row variant exists for head_dim <= 128).
-void* pick_kernel(const ca_pool_config& c, bool rows = false) {
+void* pick_kernel(const PoolCfg& c, bool rows = false) {
     if (kv_elem_bytes(c) == 1) {
         if (c.head_dim != 128) return nullptr;
         if (c.chunk == 64) return kernel_ptr<64, 128, 1>(rows);
@@ -1603,7 +1603,7 @@ void* pick_kernel(const ca_pool_config& c, bool rows = false) {
     return nullptr;
 }
 // The kernel's dynamic shared memory (the Smem map above, computed here).
-size_t smem_for(const ca_pool_config& c, int stages) {
+size_t smem_for(const PoolCfg& c, int stages) {
     const size_t eb = (size_t)kv_elem_bytes(c), cd = (size_t)c.chunk * c.head_dim;
     const size_t conv = eb == 1 ? 2 * cd * 2 : 0;
     const size_t qrows = c.head_dim == 256 ? 32 : dev::kQRows;
@@ -1614,7 +1614,7 @@ size_t smem_for(const ca_pool_config& c, int stages) {
 }  // namespace
 
 // Stages that fit two CTAs per SM (113 KiB each, at most 8).
-int kernel_smem_bytes(const ca_pool_config& c, int* n_stages, size_t* bytes) {
+int kernel_smem_bytes(const PoolCfg& c, int* n_stages, size_t* bytes) {
     if (!pick_kernel(c)) return CA_ERR_UNSUPPORTED;
     const size_t budget = 113 * 1024;
     int st = dev::kMaxStages;
@@ -1624,7 +1624,7 @@ int kernel_smem_bytes(const ca_pool_config& c, int* n_stages, size_t* bytes) {
     return CA_OK;
 }
 
-int kernel_ctas_per_sm(const ca_pool_config& c, int* ctas) {
+int kernel_ctas_per_sm(const PoolCfg& c, int* ctas) {
     void* fn = pick_kernel(c);
     if (!fn) return CA_ERR_UNSUPPORTED;
     int st;
@@ -1655,7 +1655,7 @@ int make_tensor_map(Pool& p) {
             cudaSuccess ||
         q != cudaDriverEntryPointSuccess || !fn)
         return CA_ERR_CUDA;
-    const ca_pool_config& c = p.cfg;
+    const PoolCfg& c = p.cfg;
     // The pool as a 2-D tensor: rows of head_dim elements (fp16, or bytes for
     // an fp8 pool), one row per (slot, layer, K|V, head, token-in-chunk);
     // boxes of 128 bytes x c rows.
@@ -1682,7 +1682,7 @@ uint64_t kernel_launches() { return g_launches.load(std::memory_order_relaxed); 
 
 int launch_scatter(const Pool& p, const void* k, const void* v, int32_t total_rows,
                    const std::vector<ScatterChunk>& chunks, void* stream) {
-    const ca_pool_config& c = p.cfg;
+    const PoolCfg& c = p.cfg;
     p.kv_written = true;
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap) != cudaSuccess) return CA_ERR_CUDA;

@@ -162,11 +162,11 @@ int pool_insert(Pool& p, int64_t seq_id, const int32_t* tokens, int32_t n,
     return CA_OK;
 }
 
-size_t pool_tile_bytes(const ca_pool_config& c) {
+size_t pool_tile_bytes(const PoolCfg& c) {
     return (size_t)c.capacity_slots * c.n_layers * 2 * kv_heads(c) * c.chunk * c.head_dim * kv_elem_bytes(c);
 }
 
-size_t pool_total_bytes(const ca_pool_config& c) {
+size_t pool_total_bytes(const PoolCfg& c) {
     return pool_tile_bytes(c) + (((size_t)c.capacity_slots * sizeof(int32_t) + 255) & ~size_t(255));
 }
 

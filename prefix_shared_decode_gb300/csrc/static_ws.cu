@@ -18,6 +18,7 @@
 // threads) would overwrite each other's partials.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "ca_internal.h"
@@ -27,21 +28,28 @@ namespace {
 static __device__ __align__(256) unsigned char g_static_ws[CA_STATIC_WS_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::mutex g_lock;
-void* g_ws_ptr[kMaxDevices] = {};
+std::mutex g_lookup_lock;                       // taken only by a device's first call
+std::atomic<void*> g_ws_ptr[kMaxDevices] = {};
 
 // Device address of g_static_ws on `device` (which must be current).  Looked
 // up once per device: in host code the array's name is only a host-side
-// stand-in, not a device address.
+// stand-in, not a device address.  After the first call a device's address
+// is read without a lock, so host threads driving different GPUs do not
+// serialise here.  The address stays valid for the life of the device's
+// primary context; a cudaDeviceReset after the first call would leave it
+// stale (the entry point does not support that).
 int static_ws_address(int device, void** out) {
     if (device < 0 || device >= kMaxDevices) return CA_ERR_INVALID;
-    std::lock_guard<std::mutex> guard(g_lock);
-    if (!g_ws_ptr[device]) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_static_ws) != cudaSuccess || !ptr) return CA_ERR_CUDA;
-        g_ws_ptr[device] = ptr;
+    void* ptr = g_ws_ptr[device].load(std::memory_order_acquire);
+    if (!ptr) {
+        std::lock_guard<std::mutex> guard(g_lookup_lock);
+        ptr = g_ws_ptr[device].load(std::memory_order_relaxed);
+        if (!ptr) {
+            if (cudaGetSymbolAddress(&ptr, g_static_ws) != cudaSuccess || !ptr) return CA_ERR_CUDA;
+            g_ws_ptr[device].store(ptr, std::memory_order_release);
+        }
     }
-    *out = g_ws_ptr[device];
+    *out = ptr;
     return CA_OK;
 }
 

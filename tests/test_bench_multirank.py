@@ -64,3 +64,28 @@ def test_reference_arm_prints_on_rank_zero_only(monkeypatch):
     with redirect_stdout(buf):
         bench.run_reference(args)
     assert buf.getvalue() == ""
+
+
+def test_reference_arm_reports_the_same_config_and_steps(capsys):
+    """The reference arm (the oracle over the host cores) prints the same
+    workload config the GPU arm prints and times exactly --steps steps."""
+    sys.path.insert(0, ROOT)
+    import json
+
+    import bench
+    import workloads
+    args = bench.parse(["--impl", "reference", "--workload", "tiny", "--steps", "4", "--warmup", "1"])
+    bench.run_reference(args)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 4 and line["warmup"] == 1
+    assert line["config"] == bench.workload_config(workloads.make("tiny"))
+    assert line["cpu_baseline"]["cores"] == bench.host_cores()
+    assert line["e2e"]["value"] == line["value"] and line["unit"] == bench.UNIT
+
+
+def test_cpu_baseline_over_the_host_cores_with_one_thread_figure():
+    sys.path.insert(0, ROOT)
+    import bench
+    cb = bench.cpu_baseline("tiny", seconds=0.3)
+    assert cb["kind"] == "oracle" and cb["cores"] == bench.host_cores() and cb["value"] > 0
+    assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
