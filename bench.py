@@ -526,7 +526,7 @@ class WorkloadRun:
                 r = i % self.n_copies
                 flush.zero_()
                 if mode == "write_then_read":
-                    torch.sum(clean, out=sink)
+                    torch.sum(clean, dim=0, out=sink)
                 a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(self.stream)
                 decode_attention(self.pools[r], self.scheds[r], self.qs[i % 4], out=self.out,

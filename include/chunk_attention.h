@@ -390,8 +390,36 @@ int ca_decode_attention_static_ws(const ca_pool* pool, const ca_sched* sched,
                                   float scale, void* stream);
 
 /* Synchronise `stream` and read the schedule's device status word: CA_OK,
- * CA_ERR_DEVICE_BOUNDS or CA_ERR_TIMEOUT; the word is then cleared. */
+ * CA_ERR_DEVICE_BOUNDS or CA_ERR_TIMEOUT (or a code written by
+ * ca_sched_inject_status); a non-zero word is then cleared, together with
+ * the tail-queue counter a call that stopped early may have left behind.
+ * For a host-only pool's schedule: its host word (0 unless injected). */
 int ca_sched_device_status(const ca_sched* sched, void* stream);
+
+/* ---- failure injection (tests) ---------------------------------------------
+ * The pages have no counterpart: these let the library's own tests exercise
+ * its failure paths without faulting or hanging a GPU.
+ *
+ * ca_sched_inject_status: write `code` (a CA_ERR_* value, negative) into the
+ * schedule's status word, as a kernel that saw a bad index or gave up a wait
+ * would; the next ca_sched_device_status() returns it and clears it.  For a
+ * device pool the word is written on `stream` and the call synchronises it;
+ * a host-only pool's schedule keeps a host word (ca_sched_device_status then
+ * reads that one).  CA_ERR_INVALID for a non-negative or unknown code.
+ *
+ * ca_sched_inject_stall: the next n_calls decode calls on this schedule run
+ * with their producer warps first waiting for a barrier phase that nothing
+ * completes.  No copy is issued; that wait and the consumers' first waits
+ * give up after their limit (~1 s), the call's results are undefined and
+ * ca_sched_device_status() returns CA_ERR_TIMEOUT.  Later calls run normally.
+ *
+ * ca_pool_inject_alloc_failure: the host allocation points of the coming
+ * inserts and appends pass after_n times, then one fails as if the host were
+ * out of memory; that call returns CA_ERR_OOM and leaves the pool exactly as
+ * it was before the call.  after_n < 0 turns the failure off. */
+int ca_sched_inject_status(ca_sched* sched, int32_t code, void* stream);
+int ca_sched_inject_stall(ca_sched* sched, int32_t n_calls);
+int ca_pool_inject_alloc_failure(ca_pool* pool, int32_t after_n);
 
 /* Optional timing hook: when both are non-NULL, ca_decode_attention records
  * event_begin (a cudaEvent_t) just before its main kernel and event_end just

@@ -29,7 +29,7 @@ EXPORTS = [
     "ca_insert_batch", "ca_append_tokens", "ca_remove_seq", "ca_remove_batch", "ca_pool_stats", "ca_seq_slots", "ca_build_schedule", "ca_build_schedule_ex", "ca_sched_destroy",
     "ca_sched_counts", "ca_export_tables", "ca_export_plan", "ca_workspace_bytes", "ca_decode_attention",
     "ca_workspace_bytes_host", "ca_decode_attention_host", "ca_decode_attention_static_ws",
-    "ca_sched_device_status",
+    "ca_sched_device_status", "ca_sched_inject_status", "ca_sched_inject_stall", "ca_pool_inject_alloc_failure",
     "ca_sched_set_profile_events", "ca_kernel_launches", "ca_error_string",
 ]
 
@@ -99,6 +99,9 @@ def lib() -> C.CDLL:
         "ca_decode_attention_host": [vp, vp, i32, vp, vp, C.c_float, vp, sz, vp],
         "ca_decode_attention_static_ws": [vp, vp, i32, vp, vp, C.c_float, vp],
         "ca_sched_device_status": [vp, vp],
+        "ca_sched_inject_status": [vp, i32, vp],
+        "ca_sched_inject_stall": [vp, i32],
+        "ca_pool_inject_alloc_failure": [vp, i32],
         "ca_sched_set_profile_events": [vp, vp, vp],
         "ca_kernel_launches": [vp],
         "ca_error_string": [C.c_int],

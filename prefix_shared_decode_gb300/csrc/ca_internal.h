@@ -102,6 +102,7 @@ struct AttnParams {
     float out_scale;             // value scale of an fp8 pool, else 1
     int32_t n_stages;
     int32_t kv_stable;           // no insert/append wrote the pool since the last call
+    int32_t test_stall;          // test hook: the producer first waits on a barrier nothing completes
 };
 
 // Workspace layout for a schedule.
@@ -161,6 +162,8 @@ struct Pool {
     // host does not see).
     mutable unsigned long long capture_id = 0;
     mutable bool captured_writes = false;
+    // Test hook: allocation points to pass before one fails (-1: none fails).
+    mutable int64_t fail_alloc_in = -1;
 };
 
 struct Tables {
@@ -210,6 +213,11 @@ struct Sched {
     int pinned_next = 0;
     void* ev_begin = nullptr;
     void* ev_end = nullptr;
+    // Test hooks: the status word of a host-only pool's schedule, and the
+    // number of coming decode calls whose producer stalls (every wait then
+    // gives up after its limit and the call reports CA_ERR_TIMEOUT).
+    mutable int32_t host_status = 0;
+    mutable int32_t stall_calls = 0;
 };
 
 // One chunk to fill: rows [src_row, src_row + n_rows) of a packed
@@ -245,6 +253,7 @@ struct AppendUndo {
 };
 
 // pool.cpp
+void alloc_point(const Pool& p);
 int pool_append(Pool& p, int64_t seq_id, const int32_t* tokens, int32_t n,
                 std::vector<ScatterChunk>* copies, AppendUndo* undo);
 void pool_undo_append(Pool& p, int64_t seq_id, const AppendUndo& undo);

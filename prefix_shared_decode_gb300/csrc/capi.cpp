@@ -177,22 +177,34 @@ int ca_insert_batch(ca_pool* pool, int32_t n_seqs, const int64_t* seq_ids, const
         const int64_t gen = pool->generation;
         std::vector<std::pair<int32_t, int32_t>> fresh;
         std::vector<ScatterChunk> copies;
-        int32_t row0 = 0, i = 0, st = CA_OK;
-        for (; i < n_seqs; ++i) {
-            fresh.clear();
-            int32_t shared = 0;
-            st = pool_insert(*pool, seq_ids[i], tokens + row0, lengths[i], &fresh, &shared);
-            if (st) break;
-            for (const auto& f : fresh)
-                copies.push_back({row0 + f.first, std::min(pool->cfg.chunk, lengths[i] - f.first), f.second, 0});
-            if (n_shared_out) n_shared_out[i] = shared;
-            row0 += lengths[i];
-        }
-        if (!st && pool->kv) st = launch_scatter(*pool, k_dev, v_dev, (int32_t)total, copies, stream);
-        if (st) {                              // undo: the pool must be unchanged
-            for (int32_t j = (i < n_seqs ? i : n_seqs) - 1; j >= 0; --j) pool_remove(*pool, seq_ids[j]);
+        int32_t row0 = 0, st = CA_OK, inserted = 0;
+        // The pool must be unchanged after any failure: a failed sequence
+        // undoes itself (pool_insert is all or nothing, exceptions included),
+        // the ones before it are removed again here.
+        auto undo = [&] {
+            for (int32_t j = inserted - 1; j >= 0; --j) pool_remove(*pool, seq_ids[j]);
             pool->generation = gen;
+        };
+        try {
+            for (int32_t i = 0; i < n_seqs; ++i) {
+                fresh.clear();
+                int32_t shared = 0;
+                st = pool_insert(*pool, seq_ids[i], tokens + row0, lengths[i], &fresh, &shared);
+                if (st) break;
+                ++inserted;
+                for (const auto& f : fresh) {
+                    alloc_point(*pool);
+                    copies.push_back({row0 + f.first, std::min(pool->cfg.chunk, lengths[i] - f.first), f.second, 0});
+                }
+                if (n_shared_out) n_shared_out[i] = shared;
+                row0 += lengths[i];
+            }
+            if (!st && pool->kv) st = launch_scatter(*pool, k_dev, v_dev, (int32_t)total, copies, stream);
+        } catch (...) {
+            undo();
+            throw;
         }
+        if (st) undo();
         return st;
     });
 }
@@ -490,7 +502,15 @@ int ca_decode_attention_host(const ca_pool* pool, const ca_sched* s, int32_t lay
 }
 
 int ca_sched_device_status(const ca_sched* s, void* stream) {
-    if (!s || !s->dev) return CA_ERR_INVALID;
+    if (!s) return CA_ERR_INVALID;
+    if (!s->dev) {
+        // A host-only pool's schedule has no device word; its host word is
+        // written only by ca_sched_inject_status.
+        if (!s->pool || s->pool->kv) return CA_ERR_INVALID;
+        const int32_t word = s->host_status;
+        s->host_status = 0;
+        return word;
+    }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (cudaStreamSynchronize(cs) != cudaSuccess) return CA_ERR_CUDA;
     int32_t word = 0;
@@ -505,6 +525,31 @@ int ca_sched_device_status(const ca_sched* s, void* stream) {
             return CA_ERR_CUDA;
     }
     return word;
+}
+
+int ca_sched_inject_status(ca_sched* s, int32_t code, void* stream) {
+    if (!s || code >= 0 || code < CA_ERR_SCRATCH_LIMIT) return CA_ERR_INVALID;
+    if (!s->dev) {
+        if (!s->pool || s->pool->kv) return CA_ERR_INVALID;
+        s->host_status = code;
+        return CA_OK;
+    }
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    int32_t* dev_word = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(s->dev) + s->layout.status);
+    if (cudaMemcpyAsync(dev_word, &code, sizeof(code), cudaMemcpyHostToDevice, cs) != cudaSuccess) return CA_ERR_CUDA;
+    return cuda_status(cudaStreamSynchronize(cs));
+}
+
+int ca_sched_inject_stall(ca_sched* s, int32_t n_calls) {
+    if (!s || n_calls < 0) return CA_ERR_INVALID;
+    s->stall_calls = n_calls;
+    return CA_OK;
+}
+
+int ca_pool_inject_alloc_failure(ca_pool* pool, int32_t after_n) {
+    if (!pool) return CA_ERR_INVALID;
+    pool->fail_alloc_in = after_n < 0 ? -1 : after_n;
+    return CA_OK;
 }
 
 int ca_sched_set_profile_events(ca_sched* s, void* event_begin, void* event_end) {

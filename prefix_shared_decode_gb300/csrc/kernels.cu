@@ -1001,6 +1001,15 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
         if (lane != 0) return;
+        if (p.test_stall) {
+            // Test hook (ca_sched_inject_stall): wait for stage 0's first
+            // phase, which nothing completes since no copy has been issued;
+            // the wait gives up after its limit and the producer leaves
+            // without issuing anything.  The consumers' first waits give up
+            // the same way.
+            if (!mbar_wait(full0, 0u)) set_status(p.status, CA_ERR_TIMEOUT);
+            return;
+        }
         const uint64_t pol = policy_evict_first();
         int it = 0;
         bool ok = true;
@@ -1745,6 +1754,11 @@ int launch_attention(const Pool& p, const Sched& s, const AttnParams& prm, void*
         stable = false;
     }
     a.kv_stable = stable ? 1 : 0;
+    a.test_stall = 0;
+    if (s.stall_calls > 0) {
+        a.test_stall = 1;
+        --s.stall_calls;
+    }
     p.kv_written = false;
     const CUtensorMap* map = reinterpret_cast<const CUtensorMap*>(p.tmap);
     void* args[] = {const_cast<CUtensorMap*>(map), &a};

@@ -15,6 +15,7 @@
 //  * children keep insertion order (the schedule walks them in that order).
 #include <algorithm>
 #include <functional>
+#include <new>
 
 #include "ca_internal.h"
 
@@ -50,6 +51,18 @@ uint64_t chunk_hash(const int32_t* tokens, int32_t c) {
 
 constexpr size_t kIndexAbove = 32;   // children before a node gets a hash index
 
+}  // namespace
+
+// A point where an insert or append may allocate host memory.  A test can
+// make the n-th point from now fail (ca_pool_inject_alloc_failure) to check
+// that the call then leaves the pool unchanged.
+void alloc_point(const Pool& p) {
+    if (p.fail_alloc_in < 0) return;
+    if (p.fail_alloc_in-- == 0) throw std::bad_alloc();
+}
+
+namespace {
+
 const int32_t* chunk_tokens(const Pool& p, const Node* n) {
     return p.tokens.data() + (size_t)n->slot * p.cfg.chunk;
 }
@@ -80,7 +93,8 @@ void add_child(Node* node, Node* ch) {
 
 void drop_child(Node* node, Node* ch) {
     auto& v = node->children;
-    v.erase(std::find(v.begin(), v.end(), ch));
+    auto pos = std::find(v.begin(), v.end(), ch);
+    if (pos != v.end()) v.erase(pos);       // absent only while undoing a failed add_child
     if (node->index && ch->matchable) {
         auto it = node->index->find(ch->hash);
         if (it != node->index->end() && it->second == ch) node->index->erase(it);
@@ -129,34 +143,61 @@ int pool_insert(Pool& p, int64_t seq_id, const int32_t* tokens, int32_t n,
     const int32_t pieces = (n + c - 1) / c;
     Sequence seq;
     seq.length = n;
+    alloc_point(p);
     walk_matched(p, tokens, n, seq.path);
     const int32_t matched = (int32_t)seq.path.size();
     const int32_t n_new = pieces - matched;
     if ((size_t)n_new > p.heap.size()) return CA_ERR_OOM;
+    alloc_point(p);
+    seq.path.reserve(pieces);               // nothing below pushes past it
+    const size_t chunks_before = new_chunks ? new_chunks->size() : 0;
 
-    seq.path.reserve(pieces);
+    // All or nothing: a host allocation that fails part-way (a child list or
+    // hash index growing, the new-chunk list, the sequence map) undoes every
+    // change made so far and rethrows, so the pool is as before the call.
     for (Node* m : seq.path) m->refcount += 1;
-    Node* node = matched ? seq.path.back() : &p.root;
-    const bool share = !(p.cfg.flags & CA_NO_SHARING);
-    for (int32_t i = matched; i < pieces; ++i) {
-        const int32_t a = i * c, len = std::min(c, n - a);
-        const int32_t slot = heap_pop(p.heap);
-        Node* ch = &p.nodes[slot];
-        ch->slot = slot;
-        ch->ntok = len;
-        std::copy(tokens + a, tokens + a + len, p.tokens.begin() + (size_t)slot * c);
-        ch->matchable = share && len == c;
-        ch->hash = ch->matchable ? chunk_hash(tokens + a, c) : 0;
-        ch->parent = node;
-        ch->children.clear();
-        ch->index.reset();
-        ch->refcount = 1;
-        add_child(node, ch);
-        node = ch;
-        seq.path.push_back(node);
-        if (new_chunks) new_chunks->emplace_back(a, slot);
+    try {
+        Node* node = matched ? seq.path.back() : &p.root;
+        const bool share = !(p.cfg.flags & CA_NO_SHARING);
+        for (int32_t i = matched; i < pieces; ++i) {
+            const int32_t a = i * c, len = std::min(c, n - a);
+            const int32_t slot = heap_pop(p.heap);
+            Node* ch = &p.nodes[slot];
+            ch->slot = slot;
+            ch->ntok = len;
+            std::copy(tokens + a, tokens + a + len, p.tokens.begin() + (size_t)slot * c);
+            ch->matchable = share && len == c;
+            ch->hash = ch->matchable ? chunk_hash(tokens + a, c) : 0;
+            ch->parent = node;
+            ch->children.clear();
+            ch->index.reset();
+            ch->refcount = 1;
+            seq.path.push_back(ch);         // reserved: cannot throw
+            alloc_point(p);
+            add_child(node, ch);
+            node = ch;
+            if (new_chunks) {
+                alloc_point(p);
+                new_chunks->emplace_back(a, slot);
+            }
+        }
+        alloc_point(p);
+        p.seqs.emplace(seq_id, std::move(seq));
+    } catch (...) {
+        for (size_t i = seq.path.size(); i-- > (size_t)matched;) {
+            Node* x = seq.path[i];
+            drop_child(x->parent, x);
+            heap_push(p.heap, x->slot);
+            x->children.clear();
+            x->index.reset();
+            x->parent = nullptr;
+            x->matchable = false;
+            x->refcount = 0;
+        }
+        for (int32_t i = 0; i < matched; ++i) seq.path[i]->refcount -= 1;
+        if (new_chunks) new_chunks->resize(chunks_before);
+        throw;
     }
-    p.seqs.emplace(seq_id, std::move(seq));
     p.generation += 1;
     if (n_shared) *n_shared = matched * c;
     return CA_OK;
@@ -182,43 +223,64 @@ int pool_append(Pool& p, int64_t seq_id, const int32_t* tokens, int32_t n,
     const int32_t fill = std::min(c - last->ntok, n);
     const int32_t n_new = (n - fill + c - 1) / c;
     if ((size_t)n_new > p.heap.size()) return CA_ERR_OOM;
-    if (undo) *undo = AppendUndo{last, last->ntok, last->matchable, last->hash, seq.path.size(),
-                                 p.generation, seq.length};
-    if (fill > 0) {
-        // the partial last chunk is private (never matched), so it grows in place
-        std::copy(tokens, tokens + fill, p.tokens.begin() + (size_t)last->slot * c + last->ntok);
-        if (copies) copies->push_back({0, fill, last->slot, last->ntok});
-        last->ntok += fill;
-        if (last->ntok == c && share) {
-            const int32_t* lt = chunk_tokens(p, last);
-            const uint64_t h = chunk_hash(lt, c);
-            if (!find_child(p, last->parent, lt, c, h)) {
-                last->hash = h;
-                last->matchable = true;
-                if (last->parent->index) last->parent->index->emplace(h, last);
+    alloc_point(p);
+    seq.path.reserve(seq.path.size() + n_new);   // nothing below pushes past it
+    const AppendUndo u{last, last->ntok, last->matchable, last->hash, seq.path.size(), p.generation, seq.length};
+    if (undo) *undo = u;
+    const size_t copies_before = copies ? copies->size() : 0;
+    // All or nothing, as for an insert: a host allocation that fails part-way
+    // undoes the append and rethrows.
+    try {
+        if (fill > 0) {
+            // the partial last chunk is private (never matched), so it grows in place
+            std::copy(tokens, tokens + fill, p.tokens.begin() + (size_t)last->slot * c + last->ntok);
+            if (copies) {
+                alloc_point(p);
+                copies->push_back({0, fill, last->slot, last->ntok});
+            }
+            last->ntok += fill;
+            if (last->ntok == c && share) {
+                const int32_t* lt = chunk_tokens(p, last);
+                const uint64_t h = chunk_hash(lt, c);
+                if (!find_child(p, last->parent, lt, c, h)) {
+                    last->hash = h;
+                    last->matchable = true;
+                    if (last->parent->index) {
+                        alloc_point(p);
+                        last->parent->index->emplace(h, last);
+                    }
+                }
             }
         }
-    }
-    Node* node = last;
-    for (int32_t i = 0; i < n_new; ++i) {
-        const int32_t a = fill + i * c, len = std::min(c, n - a);
-        const int32_t slot = heap_pop(p.heap);
-        Node* ch = &p.nodes[slot];
-        ch->slot = slot;
-        ch->ntok = len;
-        std::copy(tokens + a, tokens + a + len, p.tokens.begin() + (size_t)slot * c);
-        const uint64_t h = (share && len == c) ? chunk_hash(tokens + a, c) : 0;
-        // an append never matches, and an equal sibling keeps its place
-        ch->matchable = share && len == c && !find_child(p, node, tokens + a, c, h);
-        ch->hash = h;
-        ch->parent = node;
-        ch->children.clear();
-        ch->index.reset();
-        ch->refcount = 1;
-        add_child(node, ch);
-        seq.path.push_back(ch);
-        if (copies) copies->push_back({a, len, slot, 0});
-        node = ch;
+        Node* node = last;
+        for (int32_t i = 0; i < n_new; ++i) {
+            const int32_t a = fill + i * c, len = std::min(c, n - a);
+            const int32_t slot = heap_pop(p.heap);
+            Node* ch = &p.nodes[slot];
+            ch->slot = slot;
+            ch->ntok = len;
+            std::copy(tokens + a, tokens + a + len, p.tokens.begin() + (size_t)slot * c);
+            const uint64_t h = (share && len == c) ? chunk_hash(tokens + a, c) : 0;
+            // an append never matches, and an equal sibling keeps its place
+            ch->matchable = share && len == c && !find_child(p, node, tokens + a, c, h);
+            ch->hash = h;
+            ch->parent = node;
+            ch->children.clear();
+            ch->index.reset();
+            ch->refcount = 1;
+            seq.path.push_back(ch);             // reserved: cannot throw
+            alloc_point(p);
+            add_child(node, ch);
+            if (copies) {
+                alloc_point(p);
+                copies->push_back({a, len, slot, 0});
+            }
+            node = ch;
+        }
+    } catch (...) {
+        pool_undo_append(p, seq_id, u);
+        if (copies) copies->resize(copies_before);
+        throw;
     }
     seq.length += n;
     if (n_new > 0) p.generation += 1;
