@@ -75,14 +75,27 @@ constexpr int kUnitInts = (int)(sizeof(Unit) / sizeof(int32_t));
 
 // Offsets (in bytes) of the arrays inside the device plan blob.
 struct PlanLayout {
-    size_t chunks, units, cta_begin, seq_perm, pbase, status, counter, chunk_tok0, ctx_len, total;
+    size_t chunks, units, cta_begin, seq_perm, pbase, status, counter, chunk_tok0, ctx_len, cta_head, total;
 };
+
+// One 128-byte line per CTA with what its producer needs to issue its first
+// copies: its static unit range, its first unit, and that unit's first
+// kHeadRefs chunk refs (in walk order), so the first stages go out after one
+// memory round trip instead of a chain of dependent reads.
+constexpr int kHeadRefs = 8;
+struct CtaHead {
+    int32_t u_begin, u_end, pad0, pad1;
+    Unit first;                    // units[u_begin] (zeros when the range is empty)
+    ChunkRef refs[kHeadRefs];      // chunk refs of the first unit's steps 0..kHeadRefs-1
+};
+static_assert(sizeof(CtaHead) == 128, "one line per CTA");
 
 // Parameters of the attention kernel (passed by value).
 struct AttnParams {
     const ChunkRef* chunks;
     const Unit* units;
     const int32_t* cta_begin;    // [grid + 1] unit ranges per CTA
+    const CtaHead* cta_head;     // [grid] first work of each CTA
     const int32_t* seq_perm;     // [b] position -> row of q / out
     const int32_t* pbase;        // [b*H + 1] partial-id CSR per (position, head)
     const int32_t* slot_ntok;    // [capacity] valid tokens per pool slot (device table)

@@ -991,7 +991,11 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
     }
     __syncthreads();
 
-    const int u_begin = p.cta_begin[blockIdx.x], u_end = p.cta_begin[blockIdx.x + 1];
+    // this CTA's first work: one 128-byte line (its unit range, first unit
+    // and that unit's first chunk refs)
+    const CtaHead* hd = p.cta_head + blockIdx.x;
+    const int2 range = *reinterpret_cast<const int2*>(hd);
+    const int u_begin = range.x, u_end = range.y;
     const int H = p.n_heads;            // query heads (q, out, partials)
     const int HK = p.n_kv_heads;        // key/value heads (pool tiles, units)
     const int G = p.group;              // query heads per key/value head
@@ -1001,6 +1005,8 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
         if (lane != 0) return;
+        // the tensor map's descriptor is fetched while the plan line loads
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
         if (p.test_stall) {
             // Test hook (ca_sched_inject_stall): wait for stage 0's first
             // phase, which nothing completes since no copy has been issued;
@@ -1052,8 +1058,12 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
             return (p.dyn_begin + k < p.dyn_end) ? p.dyn_begin + k : -1;
         };
         int cur = (u_begin < u_end) ? s_next++ : -1;
-        Unit Un = (cur >= 0) ? p.units[cur] : Unit{};
-        ChunkRef chn = (cur >= 0) ? p.chunks[first_chunk(Un)] : ChunkRef{0, 0};
+        // The first static unit and its first kHeadRefs chunk refs come from
+        // the CTA's line, so its first stages are issued without waiting on
+        // further plan reads.
+        bool from_head = cur >= 0;
+        Unit Un = (cur >= 0) ? hd->first : Unit{};
+        ChunkRef chn = (cur >= 0) ? hd->refs[0] : ChunkRef{0, 0};
         // context offsets matter only under the causal mask
         int tkn = (cur >= 0 && p.causal) ? p.chunk_tok0[first_chunk(Un)] : 0;
         if (!p.kv_stable) dep_wait();
@@ -1096,7 +1106,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
                 const int head = h;
                 if (++j == n) { j = 0; ++h; }
                 if (L + 1 < L1) {
-                    chn = p.chunks[base + j];
+                    chn = (from_head && L + 1 - L0 < kHeadRefs) ? hd->refs[L + 1 - L0] : p.chunks[base + j];
                     if (p.causal) tkn = p.chunk_tok0[base + j];
                 } else if (nxt >= 0) {
                     chn = p.chunks[first_chunk(Un)];
@@ -1135,6 +1145,7 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
             if (!have_next) {                 // left early on a timeout
                 nxt = -1;
             }
+            from_head = false;
             cur = nxt;
         }
         if (ok) {

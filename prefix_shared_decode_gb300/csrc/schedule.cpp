@@ -522,6 +522,7 @@ void layout_plan(const Plan& plan, int32_t b, PlanLayout& lay, std::vector<unsig
     lay.counter = off;   off = align256(off + sizeof(int32_t));
     lay.chunk_tok0 = off; off = align256(off + plan.chunk_tok0.size() * sizeof(int32_t));
     lay.ctx_len = off;   off = align256(off + (size_t)b * sizeof(int32_t));
+    lay.cta_head = off;  off = align256(off + (size_t)plan.grid * sizeof(CtaHead));
     lay.total = off;
     blob.assign(off, 0);
     std::memcpy(blob.data() + lay.chunks, plan.chunks.data(), plan.chunks.size() * sizeof(ChunkRef));
@@ -531,6 +532,26 @@ void layout_plan(const Plan& plan, int32_t b, PlanLayout& lay, std::vector<unsig
     std::memcpy(blob.data() + lay.pbase, plan.pbase.data(), plan.pbase.size() * sizeof(int32_t));
     std::memcpy(blob.data() + lay.chunk_tok0, plan.chunk_tok0.data(), plan.chunk_tok0.size() * sizeof(int32_t));
     std::memcpy(blob.data() + lay.ctx_len, t.ctx_len.data(), (size_t)b * sizeof(int32_t));
+    // Each CTA's first work, with the chunk refs of its first unit's steps
+    // (a unit walks the linear (head, chunk) range [L0, L1); step L reads
+    // chunk base + L % n, as the kernel's producer does).
+    CtaHead* heads = reinterpret_cast<CtaHead*>(blob.data() + lay.cta_head);
+    for (int32_t c = 0; c < plan.grid; ++c) {
+        CtaHead h{};
+        h.u_begin = plan.cta_begin[c];
+        h.u_end = plan.cta_begin[c + 1];
+        if (h.u_begin < h.u_end) {
+            const Unit& u = plan.units[h.u_begin];
+            h.first = u;
+            const bool sf = u.kind == UNIT_SF;
+            const int32_t n = sf ? u.n_per_head : u.c_end - u.c_begin;
+            const int32_t base = sf ? u.base : u.c_begin;
+            const int32_t L0 = sf ? u.c_begin : u.head * n;
+            const int32_t L1 = sf ? u.c_end : (u.head + u.n_per_head) * n;
+            for (int32_t k = 0; k < kHeadRefs && L0 + k < L1; ++k) h.refs[k] = plan.chunks[base + (L0 + k) % n];
+        }
+        heads[c] = h;
+    }
 }
 
 void layout_ws(const Plan& plan, const Pool& p, int32_t b, WsLayout& ws) {
