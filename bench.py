@@ -64,6 +64,8 @@ def parse(argv=None):
     ap.add_argument("--no-per-config", action="store_true", help="headline workload only")
     ap.add_argument("--configs", default="", help="comma-separated workloads for the per_config block "
                                                   "(default: every configuration and variant)")
+    ap.add_argument("--quick", action="store_true",
+                    help="the workload's W warm-up + K back-to-back steps only (for profiler captures)")
     return ap.parse_args(argv)
 
 
@@ -697,6 +699,16 @@ def run_ours(args):
     run = WorkloadRun(args.workload, dev, stream, max_steps=W + K + 64)
     b2b = run.back_to_back(K, W, clocks=clocks, label="headline", world=world)
     ms_per_step = b2b["us"] / 1e3
+    if args.quick:
+        clocks.stop()
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": round(whole_job_per_call(b2b["us"], world), 3),
+                              "unit": UNIT, "steps": K, "warmup": W, "quick": True,
+                              "config": workload_config(run.wl, world), "gpu_launches": b2b["launches"]}),
+                  flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
     kern = run.kernel_isolated(clocks=clocks, label="kernel")
     iso = run.isolated_call(clocks=clocks, label="isolated")
     e2e_us = run.e2e(min(K, 200))
