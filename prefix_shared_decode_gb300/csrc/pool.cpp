@@ -15,6 +15,7 @@
 //  * children keep insertion order (the schedule walks them in that order).
 #include <algorithm>
 #include <functional>
+#include <memory>
 #include <new>
 
 #include "ca_internal.h"
@@ -85,9 +86,12 @@ void add_child(Node* node, Node* ch) {
     if (node->index) {
         if (ch->matchable) node->index->emplace(ch->hash, ch);
     } else if (node->children.size() > kIndexAbove) {
-        node->index.reset(new std::unordered_map<uint64_t, Node*>());
+        // built aside and installed whole, so a failed allocation leaves no
+        // partial index behind (the linear scan stays right without one)
+        auto idx = std::make_unique<std::unordered_map<uint64_t, Node*>>();
         for (Node* x : node->children)
-            if (x->matchable) node->index->emplace(x->hash, x);
+            if (x->matchable) idx->emplace(x->hash, x);
+        node->index = std::move(idx);
     }
 }
 
@@ -151,10 +155,14 @@ int pool_insert(Pool& p, int64_t seq_id, const int32_t* tokens, int32_t n,
     alloc_point(p);
     seq.path.reserve(pieces);               // nothing below pushes past it
     const size_t chunks_before = new_chunks ? new_chunks->size() : 0;
+    // The sequence's map entry is allocated before anything changes and
+    // filled at the end by a move that cannot throw.
+    alloc_point(p);
+    const auto entry = p.seqs.try_emplace(seq_id).first;
 
     // All or nothing: a host allocation that fails part-way (a child list or
-    // hash index growing, the new-chunk list, the sequence map) undoes every
-    // change made so far and rethrows, so the pool is as before the call.
+    // hash index growing, the new-chunk list) undoes every change made so far
+    // and rethrows, so the pool is as before the call.
     for (Node* m : seq.path) m->refcount += 1;
     try {
         Node* node = matched ? seq.path.back() : &p.root;
@@ -181,8 +189,6 @@ int pool_insert(Pool& p, int64_t seq_id, const int32_t* tokens, int32_t n,
                 new_chunks->emplace_back(a, slot);
             }
         }
-        alloc_point(p);
-        p.seqs.emplace(seq_id, std::move(seq));
     } catch (...) {
         for (size_t i = seq.path.size(); i-- > (size_t)matched;) {
             Node* x = seq.path[i];
@@ -196,8 +202,10 @@ int pool_insert(Pool& p, int64_t seq_id, const int32_t* tokens, int32_t n,
         }
         for (int32_t i = 0; i < matched; ++i) seq.path[i]->refcount -= 1;
         if (new_chunks) new_chunks->resize(chunks_before);
+        p.seqs.erase(entry);
         throw;
     }
+    entry->second = std::move(seq);
     p.generation += 1;
     if (n_shared) *n_shared = matched * c;
     return CA_OK;

@@ -141,7 +141,6 @@ def test_no_tpp_schedule_makes_everything_sequence_first(lib):
 
 
 def test_kernel_launch_counter_on_host_only_pools(lib):
-    import ctypes
     from prefix_shared_decode_gb300 import Pool, kernel_launches
     before = kernel_launches()
     pool = Pool(1, 2, 64, 16, 8, host_only=True)

@@ -1,7 +1,6 @@
 """Pins of the oracle's FP8 E4M3 quantiser against the format's definition
 (landmark codes and values worked out by hand), brute force over every
 finite code, and torch's float8_e4m3fn cast; plus the scale handling."""
-import math
 
 import numpy as np
 import pytest
