@@ -649,7 +649,8 @@ def config_entry(run: WorkloadRun, b2b: dict, kern: dict, iso: dict, ctx: dict |
          "isolated_call_frac_of_8tbs": round(run.alg_bytes / (iso["write"] * 1e-6) / 1e9 / NOMINAL_HBM_GBS, 4),
          "kernel": run.kernel_name, "kernel_us": round(kern["median_us"], 2),
          "kernel_frac_of_measured_peak": round(run.alg_bytes / (kern["median_us"] * 1e-6) / 1e9 / peak, 4),
-         "pool_copies": run.n_copies, "steps": b2b.get("steps"), "warmup": b2b.get("warmup")}
+         "pool_copies": run.n_copies, "partial_scratch_bytes": run.scheds[0].workspace_bytes(),
+         "steps": b2b.get("steps"), "warmup": b2b.get("warmup")}
     if run.churn:
         e["us_per_call"] = None
         e["us_per_step_incl_churn"] = round(us, 2)
@@ -725,6 +726,7 @@ def run_ours(args):
     run_setup = run.setup_s
     cfg = workload_config(run.wl, world)
     launch = {"grid_ctas": run.scheds[0].plan()["grid"],
+              "partial_scratch_bytes": run.scheds[0].workspace_bytes(),
               "sms": torch.cuda.get_device_properties(dev).multi_processor_count,
               "pool_copies": run.n_copies, "l2_bytes": run.l2,
               "l2_note": ("no flush: steps run back to back over %d pool cop%s (%d MB of unique KV each, "

@@ -2,6 +2,7 @@
 // argument checks, object lifetimes and the host side of each call.  No C++
 // exception crosses this boundary.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cstring>
@@ -17,6 +18,17 @@ struct ca_sched : Sched {};
 namespace {
 
 constexpr int32_t kHostOnlyGrid = 2 * 152;   // plan grid for a pool with no GPU
+
+// An NVTX range around a host call (insert, append, remove, schedule,
+// attention), so that a profiler attached to the process shows where each
+// call's host work and kernels belong; without a profiler a push or pop is a
+// call through a no-op pointer.
+struct Range {
+    explicit Range(const char* name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+    Range(const Range&) = delete;
+    Range& operator=(const Range&) = delete;
+};
 
 template <class F>
 int guard(F&& f) {
@@ -161,6 +173,7 @@ int ca_insert_tokens(ca_pool* pool, int64_t seq_id, const int32_t* tokens, int32
 int ca_insert_batch(ca_pool* pool, int32_t n_seqs, const int64_t* seq_ids, const int32_t* tokens,
                     const int32_t* lengths, const void* k_dev, const void* v_dev, void* stream,
                     int32_t* n_shared_out) {
+    const Range range("ca_insert");
     if (!pool || n_seqs < 1 || !seq_ids || !tokens || !lengths) return CA_ERR_INVALID;
     int64_t total = 0;
     for (int32_t i = 0; i < n_seqs; ++i) {
@@ -211,6 +224,7 @@ int ca_insert_batch(ca_pool* pool, int32_t n_seqs, const int64_t* seq_ids, const
 
 int ca_append_tokens(ca_pool* pool, int64_t seq_id, const int32_t* tokens, int32_t n,
                      const void* k_dev, const void* v_dev, void* stream, int32_t* n_new_chunks_out) {
+    const Range range("ca_append_tokens");
     if (!pool || n <= 0 || !tokens) return CA_ERR_INVALID;
     if (pool->kv) {
         if (!k_dev || !v_dev || !aligned(k_dev, 16) || !aligned(v_dev, 16)) return CA_ERR_INVALID;
@@ -236,11 +250,13 @@ int ca_append_tokens(ca_pool* pool, int64_t seq_id, const int32_t* tokens, int32
 }
 
 int ca_remove_seq(ca_pool* pool, int64_t seq_id) {
+    const Range range("ca_remove");
     if (!pool) return CA_ERR_INVALID;
     return guard([&] { return pool_remove(*pool, seq_id); });
 }
 
 int ca_remove_batch(ca_pool* pool, int32_t n_seqs, const int64_t* seq_ids) {
+    const Range range("ca_remove");
     if (!pool || n_seqs < 0 || (n_seqs > 0 && !seq_ids)) return CA_ERR_INVALID;
     return guard([&] {
         for (int32_t i = 0; i < n_seqs; ++i)
@@ -283,6 +299,7 @@ int ca_build_schedule(ca_pool* pool, const int64_t* seq_ids, int32_t b, ca_sched
 
 int ca_build_schedule_ex(ca_pool* pool, const int64_t* seq_ids, int32_t b, int32_t q_len, uint32_t flags,
                          ca_sched** inout, void* stream) {
+    const Range range("ca_build_schedule");
     if (!pool || !inout || !seq_ids || b < 1 || q_len < 1 || (flags & ~(CA_SCHED_NO_TPP | CA_SCHED_CAUSAL)))
         return CA_ERR_INVALID;
     if ((int64_t)q_len * (pool->cfg.n_heads / kv_heads(pool->cfg)) > max_query_rows(pool->cfg))
@@ -469,6 +486,7 @@ static int decode_launch(const ca_pool* pool, const ca_sched* s, int32_t layer, 
 
 int ca_decode_attention(const ca_pool* pool, const ca_sched* s, int32_t layer, const void* q_dev,
                         void* out_dev, float scale, void* ws_dev, size_t ws_bytes, void* stream) {
+    const Range range("ca_decode_attention");
     int st = decode_checks(pool, s, layer, ws_dev, ws_bytes, s ? s->ws.total : 0);
     if (st) return st;
     if (!q_dev || !out_dev || !aligned(q_dev, 16) || !aligned(out_dev, 16)) return CA_ERR_INVALID;
@@ -478,6 +496,7 @@ int ca_decode_attention(const ca_pool* pool, const ca_sched* s, int32_t layer, c
 int ca_decode_attention_host(const ca_pool* pool, const ca_sched* s, int32_t layer,
                              const void* q_host, void* out_host, float scale, void* ws_dev,
                              size_t ws_bytes, void* stream) {
+    const Range range("ca_decode_attention");
     int st = decode_checks(pool, s, layer, ws_dev, ws_bytes, s ? s->ws.total_host : 0);
     if (st) return st;
     if (!q_host || !out_host) return CA_ERR_INVALID;

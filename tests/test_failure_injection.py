@@ -197,3 +197,55 @@ def test_device_status_and_stalled_call_on_the_gpu(lib):
         assert sched.device_status() == 0
         err = np.abs(got - want)
         assert err.max() <= 2e-3 and err.mean() <= 2e-4
+
+
+@pytest.mark.gpu
+def test_decode_call_argument_errors_launch_nothing(lib):
+    """Bad arguments to the decode call are refused on the host with
+    CA_ERR_INVALID before any kernel is launched: missing or misaligned q /
+    out, a workspace that is too small or not 256-byte aligned, a layer out
+    of range, a schedule of another pool.  A valid call then succeeds."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import workloads
+    from oracle import attention as A
+    from prefix_shared_decode_gb300 import Pool, capi, kernel_launches
+    from workloads.device import capacity_for, insert_sequence
+    wl = workloads.make("tiny")
+    pools = []
+    for _ in range(2):
+        p = Pool(wl.n_layers, wl.n_heads, wl.head_dim, wl.chunk, capacity_for(wl))
+        for sid in wl.seq_ids():
+            insert_sequence(p, wl, sid)
+        pools.append(p)
+    pool, other = pools
+    sched, other_sched = pool.schedule(wl.seq_ids()), other.schedule(wl.seq_ids())
+    q = torch.from_numpy(wl.queries(0)).cuda()
+    out = torch.empty_like(q)
+    need = sched.workspace_bytes()
+    ws = torch.zeros(need + 4096, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    L = capi.lib()
+
+    def call(sch=sched, layer=0, qp=q.data_ptr(), op=out.data_ptr(), wp=ws.data_ptr(), wb=ws.numel()):
+        return L.ca_decode_attention(pool.handle, sch.handle, layer, qp, op, float(wl.scale), wp, wb, stream)
+
+    torch.cuda.synchronize()
+    n0 = kernel_launches()
+    for what, st in [("q NULL", call(qp=None)), ("out NULL", call(op=None)),
+                     ("q misaligned", call(qp=q.data_ptr() + 2)), ("out misaligned", call(op=out.data_ptr() + 8)),
+                     ("workspace short", call(wb=need - 1)), ("workspace NULL", call(wp=None)),
+                     ("workspace misaligned", call(wp=ws.data_ptr() + 16, wb=need + 16)),
+                     ("layer past the end", call(layer=wl.n_layers)), ("negative layer", call(layer=-1)),
+                     ("another pool's schedule", call(sch=other_sched))]:
+        assert st == ERR_INVALID, (what, st)
+    assert kernel_launches() == n0
+    assert call() == 0
+    assert sched.device_status() == 0
+    trie = OracleTrie(wl.chunk, 1000)
+    for sid in wl.seq_ids():
+        trie.insert(sid, wl.tokens(sid), *wl.kv_rows(sid))
+    err = np.abs(out.cpu().numpy().astype(np.float64) - A.decode_attention(trie, wl.seq_ids(), 0, wl.queries(0),
+                                                                          wl.scale))
+    assert err.max() <= 2e-3 and err.mean() <= 2e-4
