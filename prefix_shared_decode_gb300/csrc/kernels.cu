@@ -1080,14 +1080,15 @@ two_phase_attention_kernel(const __grid_constant__ CUtensorMap tmap, const AttnP
             const Unit U = Un;
             ring[seq % kRing] = cur;
             // The next unit (the next static one, or in the tail phase a
-            // claim) is taken when three chunks of this one remain: late
+            // claim) is taken when two chunks of this one remain: late
             // enough not to hold queue work long, early enough to hide the
-            // claim and descriptor latency.
+            // claim and descriptor latency (three measured slower on every
+            // workload but one, level there).
             int nxt = -1;
             bool have_next = false;
             const int n = lin_n(U), base = lin_base(U);
             const int L0 = lin_begin(U), L1 = lin_end(U);
-            const int claim_at = max(L0, L1 - 3);
+            const int claim_at = max(L0, L1 - 2);
             int h = L0 / n;
             int j = L0 - h * n;
             for (int L = L0; L < L1; ++L, ++it) {

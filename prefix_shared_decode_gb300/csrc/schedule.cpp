@@ -263,7 +263,9 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, int32_t q_len, Pla
         return total;
     };
     double cf_total = cf_cost_total();
-    if (RW > 1 && group_rows > 32 && (sf_total + cf_total) < kSmallCallTiles * grid) {
+    // a small call whose positions bring several rows each
+    const bool small_multi_row = RW > 1 && (sf_total + cf_total) < kSmallCallTiles * grid;
+    if (small_multi_row && group_rows > 32) {
         group_rows = 32;
         cf_total = cf_cost_total();
     }
@@ -450,13 +452,22 @@ void build_plan(const Pool& p, const Tables& t, int32_t grid, int32_t q_len, Pla
         }
         for (; k < grid; ++k) sf_end[k] = (int32_t)sf_units.size();
         // The rest of the list becomes the tail queue: units of at most
-        // `tail_unit` chunk-heads that never cross a head boundary.
+        // `tail_unit` chunk-heads that never cross a head boundary.  In a
+        // small multi-row call, whose CTAs hold only a few tiles each, the
+        // last 2 x grid chunk-heads (the queue's last claims) go in units of
+        // two, so that the CTAs' finish times spread less.
         const int32_t tail_unit = std::max<int32_t>(
             kTailUnitMin, std::min<int32_t>(kTailUnitMax, (int32_t)((tail_tiles + kTailUnitsPerCta * grid - 1) /
                                                                    ((int64_t)kTailUnitsPerCta * grid))));
+        int64_t remaining = 0;                       // chunk-heads left for the queue
+        for (int32_t ps = pos; ps < b; ++ps) remaining += (int64_t)H * seg_len(ps);
+        if (pos < b) remaining -= (int64_t)hd * seg_len(pos) + jd;
+        const int64_t split_zone = small_multi_row ? 2 * (int64_t)grid : 0;
         while (pos < b) {
             const int32_t n = seg_len(pos);
-            const int32_t a = hd * n + jd, len = std::min(tail_unit, n - jd);
+            const int32_t unit_now = remaining <= split_zone ? std::min<int32_t>(2, tail_unit) : tail_unit;
+            const int32_t a = hd * n + jd, len = std::min(unit_now, n - jd);
+            remaining -= len;
             const int32_t before = (jd == 0) ? 0 : head_pieces;
             tail_units.push_back(unit_at(pos, hd, a, a + len, before));
             npart[(size_t)pos * H + hd] += 1;
