@@ -75,7 +75,7 @@ constexpr int kUnitInts = (int)(sizeof(Unit) / sizeof(int32_t));
 
 // Offsets (in bytes) of the arrays inside the device plan blob.
 struct PlanLayout {
-    size_t chunks, units, cta_begin, seq_perm, pbase, status, counter, chunk_tok0, ctx_len, cta_head, total;
+    size_t chunks, units, seq_perm, pbase, status, counter, chunk_tok0, ctx_len, cta_head, total;
 };
 
 // One 128-byte line per CTA with what its producer needs to issue its first
@@ -94,7 +94,6 @@ static_assert(sizeof(CtaHead) == 128, "one line per CTA");
 struct AttnParams {
     const ChunkRef* chunks;
     const Unit* units;
-    const int32_t* cta_begin;    // [grid + 1] unit ranges per CTA
     const CtaHead* cta_head;     // [grid] first work of each CTA
     const int32_t* seq_perm;     // [b] position -> row of q / out
     const int32_t* pbase;        // [b*H + 1] partial-id CSR per (position, head)

@@ -445,7 +445,6 @@ AttnParams attn_params(const Pool& pool, const Sched& s, int32_t layer, const vo
     AttnParams a{};
     a.chunks = reinterpret_cast<const ChunkRef*>(dev + s.layout.chunks);
     a.units = reinterpret_cast<const Unit*>(dev + s.layout.units);
-    a.cta_begin = reinterpret_cast<const int32_t*>(dev + s.layout.cta_begin);
     a.cta_head = reinterpret_cast<const CtaHead*>(dev + s.layout.cta_head);
     a.seq_perm = reinterpret_cast<const int32_t*>(dev + s.layout.seq_perm);
     a.pbase = reinterpret_cast<const int32_t*>(dev + s.layout.pbase);

@@ -526,7 +526,6 @@ void layout_plan(const Plan& plan, int32_t b, PlanLayout& lay, std::vector<unsig
     size_t off = 0;
     lay.chunks = off;    off = align256(off + plan.chunks.size() * sizeof(ChunkRef));
     lay.units = off;     off = align256(off + plan.units.size() * sizeof(Unit));
-    lay.cta_begin = off; off = align256(off + plan.cta_begin.size() * sizeof(int32_t));
     lay.seq_perm = off;  off = align256(off + (size_t)b * sizeof(int32_t));
     lay.pbase = off;     off = align256(off + plan.pbase.size() * sizeof(int32_t));
     lay.status = off;    off = align256(off + sizeof(int32_t));
@@ -538,7 +537,6 @@ void layout_plan(const Plan& plan, int32_t b, PlanLayout& lay, std::vector<unsig
     blob.assign(off, 0);
     std::memcpy(blob.data() + lay.chunks, plan.chunks.data(), plan.chunks.size() * sizeof(ChunkRef));
     std::memcpy(blob.data() + lay.units, plan.units.data(), plan.units.size() * sizeof(Unit));
-    std::memcpy(blob.data() + lay.cta_begin, plan.cta_begin.data(), plan.cta_begin.size() * sizeof(int32_t));
     std::memcpy(blob.data() + lay.seq_perm, t.seq_perm.data(), (size_t)b * sizeof(int32_t));
     std::memcpy(blob.data() + lay.pbase, plan.pbase.data(), plan.pbase.size() * sizeof(int32_t));
     std::memcpy(blob.data() + lay.chunk_tok0, plan.chunk_tok0.data(), plan.chunk_tok0.size() * sizeof(int32_t));
