@@ -156,10 +156,12 @@ class OraclePool:
         self.cores = cores or host_cores()
         self.pool = mp.get_context("spawn").Pool(self.cores, initializer=_cpu_setup, initargs=(name,))
 
-    def call(self, rows):
-        """Wall time (s) to compute the given batch rows through the pool."""
+    def call(self, rows, timeout: float = 600.0):
+        """Wall time (s) to compute the given batch rows through the pool.
+        Bounded: a worker whose set-up keeps failing would otherwise make the
+        pool respawn it for ever."""
         t0 = time.perf_counter()
-        self.pool.map(_cpu_one, rows, chunksize=1)
+        self.pool.map_async(_cpu_one, rows, chunksize=1).get(timeout)
         return time.perf_counter() - t0
 
     def close(self):
@@ -188,7 +190,16 @@ def cpu_baseline_single(name: str, seconds: float = CPU_SAMPLE_SECONDS) -> dict:
 
 def cpu_baseline(name: str, seconds: float = CPU_SAMPLE_SECONDS) -> dict:
     """The oracle over every host core (the figure reported), with the
-    one-thread figure beside it."""
+    one-thread figure beside it.  A failure here is reported in the line
+    rather than stopping the GPU measurement."""
+    try:
+        return _cpu_baseline(name, seconds)
+    except Exception as e:                       # noqa: BLE001 (reported, not raised)
+        return {"value": None, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                "error": f"{type(e).__name__}: {e}"[:300]}
+
+
+def _cpu_baseline(name: str, seconds: float) -> dict:
     import workloads
     b = len(workloads.make(name).seqs)
     op = OraclePool(name)
@@ -852,24 +863,16 @@ def run_reference(args):
     import workloads
     wl = workloads.make(args.workload)
     b = len(wl.seqs)
-    op = OraclePool(wl.name)
     try:
-        t_warm = op.call(list(range(b)))                         # workers build their tries
-        # sample size: whole rounds of one sequence per core, so that the
-        # K + W steps take about two minutes at most
-        per_round = op.call(list(range(min(b, op.cores))))
-        rounds = max(1, min(-(-b // op.cores), int(120.0 / max(1e-3, per_round) / max(1, args.steps + args.warmup))))
-        n = min(b, rounds * op.cores)
-        rows = list(range(n))
-        for _ in range(args.warmup):
-            op.call(rows)
-        per_step = [op.call(rows) * 1e6 * b / n for _ in range(args.steps)]
-    finally:
-        op.close()
+        per_step, n, t_warm, cores = _reference_steps(wl, args)
+    except Exception as e:                       # noqa: BLE001
+        print(json.dumps({"impl": "reference", "unavailable": f"the CPU oracle failed: {type(e).__name__}: {e}"[:300]}),
+              flush=True)
+        return
     v = statistics.median(per_step)
-    cb = {"value": v, "unit": UNIT, "cores": op.cores, "kind": "oracle",
+    cb = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
           "sample": f"each step: the fp64 oracle decode (materialise K/V from the oracle trie + softmax "
-                    f"attention) of {n} of the {b} sequences, spread over {op.cores} worker processes (one per "
+                    f"attention) of {n} of the {b} sequences, spread over {cores} worker processes (one per "
                     f"host core), scaled x{b}/{n} to one layer call; median of {args.steps} steps after "
                     f"{args.warmup} warm-up (set-up {t_warm:.1f} s untimed)"}
     res = {"metric": METRIC, "value": round(v, 1), "unit": UNIT, "impl": "reference",
@@ -884,6 +887,27 @@ def run_reference(args):
            "note": "ChunkAttention's pages publish no code: the reference arm is the fp64 CPU oracle on the host "
                    "cores, timed on a bounded sample and scaled to one layer call"}
     print(json.dumps(res), flush=True)
+
+
+def _reference_steps(wl, args):
+    """Per-step µs of the reference arm (one layer call over a bounded
+    sample of the batch, scaled to the whole batch)."""
+    b = len(wl.seqs)
+    op = OraclePool(wl.name)
+    try:
+        t_warm = op.call(list(range(b)))                         # workers build their tries
+        # sample size: whole rounds of one sequence per core, so that the
+        # K + W steps take about two minutes at most
+        per_round = op.call(list(range(min(b, op.cores))))
+        rounds = max(1, min(-(-b // op.cores), int(120.0 / max(1e-3, per_round) / max(1, args.steps + args.warmup))))
+        n = min(b, rounds * op.cores)
+        rows = list(range(n))
+        for _ in range(args.warmup):
+            op.call(rows)
+        per_step = [op.call(rows) * 1e6 * b / n for _ in range(args.steps)]
+    finally:
+        op.close()
+    return per_step, n, t_warm, op.cores
 
 
 if __name__ == "__main__":

@@ -89,3 +89,24 @@ def test_cpu_baseline_over_the_host_cores_with_one_thread_figure():
     cb = bench.cpu_baseline("tiny", seconds=0.3)
     assert cb["kind"] == "oracle" and cb["cores"] == bench.host_cores() and cb["value"] > 0
     assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
+
+
+def test_oracle_pool_calls_are_bounded_when_worker_setup_fails():
+    """A pool whose workers cannot set up (an unknown workload here) makes
+    multiprocessing respawn them for ever; the benchmark's calls give up
+    after their limit instead of hanging, and the CPU baseline reports the
+    failure in the line instead of raising."""
+    import multiprocessing
+    import time
+    sys.path.insert(0, ROOT)
+    import bench
+    op = bench.OraclePool("no_such_workload", cores=2)
+    t0 = time.perf_counter()
+    try:
+        with pytest.raises(multiprocessing.TimeoutError):
+            op.call([0, 1], timeout=3.0)
+    finally:
+        op.close()
+    assert time.perf_counter() - t0 < 60
+    cb = bench.cpu_baseline("no_such_workload", seconds=0.1)
+    assert cb["value"] is None and "KeyError" in cb["error"]
