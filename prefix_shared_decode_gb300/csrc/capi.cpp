@@ -324,10 +324,15 @@ int ca_build_schedule_ex(ca_pool* pool, const int64_t* seq_ids, int32_t b, int32
         int st = build_tables(*pool, seq_ids, b, flags, s->t_next);
         if (st) return st;                  // s (if reused) keeps its previous tables
         std::swap(s->t, s->t_next);
+        // Invalid until the plan for these tables is built and uploaded: a
+        // failure from here on leaves a schedule that every later call
+        // rebuilds and every decode call refuses as stale.
+        s->generation = -1;
         s->pool = pool;
         s->flags = flags;
         s->q_len = q_len;
         s->seq_ids.assign(seq_ids, seq_ids + b);
+        alloc_point(*pool);                 // the plan's vectors may grow below
         build_plan(*pool, s->t, pool->kv ? pool->num_sms : kHostOnlyGrid, q_len, s->plan);
         layout_plan(s->plan, b, s->layout, s->blob, s->t);
         layout_ws(s->plan, *pool, b, s->ws);

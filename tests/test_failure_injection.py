@@ -249,3 +249,25 @@ def test_decode_call_argument_errors_launch_nothing(lib):
     err = np.abs(out.cpu().numpy().astype(np.float64) - A.decode_attention(trie, wl.seq_ids(), 0, wl.queries(0),
                                                                           wl.scale))
     assert err.max() <= 2e-3 and err.mean() <= 2e-4
+
+
+def test_failed_schedule_rebuild_is_never_reused(lib):
+    """A schedule rebuild that fails part-way (host allocation) on a reused
+    schedule, with the tree unchanged, must not leave new tables beside the
+    old plan: the next call for the same batch rebuilds, and its plan equals
+    a fresh schedule's."""
+    from prefix_shared_decode_gb300 import CAError
+    c = 16
+    pool = host_pool(c)
+    build_tree(pool, OracleTrie(c, 400), c)
+    a, b = list(range(0, 44, 2)), list(range(1, 44, 3))
+    sched = pool.schedule(a)
+    assert lib.ca_pool_inject_alloc_failure(pool.handle, 0) == 0
+    with pytest.raises(CAError) as e:
+        pool.schedule(b, reuse=sched)
+    assert e.value.name == "CA_ERR_OOM"
+    assert lib.ca_pool_inject_alloc_failure(pool.handle, -1) == 0
+    again = pool.schedule(b, reuse=sched).plan()
+    fresh = pool.schedule(b).plan()
+    for k in ("units", "cta_begin", "pbase", "chunks"):
+        np.testing.assert_array_equal(again[k], fresh[k], err_msg=k)
